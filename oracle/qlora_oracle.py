@@ -1,0 +1,225 @@
+"""Plain fp64 CPU oracle for the LoRA linear over a frozen block-quantised base.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's ``cpu_baseline`` / reference leg may import this module.  It shares
+no code with the CUDA library and imports nothing from it.
+
+What it computes, and where it comes from:
+
+* The layer (forward and "fast backward" formulas of LoRA, bytechap GGUF blog,
+  "How it works"; frozen base "read, never written", Soup show post, first
+  paragraph):
+      T  = X A^T                     (rank-r down projection)
+      Y  = X deq(Wq)^T + s T B^T,    s = alpha / r
+      U  = dY B
+      dX = dY deq(Wq) + s U A
+      dB = s dY^T T
+      dA = s U^T X
+  There is no gradient for the frozen base.  All products are evaluated in
+  fp64 on the stored (bf16 / dequantised) values.
+
+* Block formats (Surogate README, "LoRA & QLoRA" row: BnB/NF4 bases; GGUF
+  blog: GGUF Q8_0/Q4_0 bases).  The pages print no table or block layout; the
+  readings used here:
+      NF4   64 codes per block along K, two per byte (element 2j in the high
+            nibble of byte j), fp32 absmax per block, or int8 absmax with one
+            fp32 scale per 256 blocks (double quantisation).  Levels: the
+            NormalFloat-4 construction (16 normal quantiles incl. an exact 0,
+            scaled to [-1, 1]), stored as fp32.
+            value = bf16_rn( f32_rn( level[c] * absmax' ) ),
+            absmax' = absmax or f32_rn( f32(q) * scale2 ).
+      Q4_0  32 elements per 18-byte block {fp16 d, 16 bytes}; element i < 16
+            in the low nibble of byte i, element i+16 in its high nibble.
+            value = bf16_rn( (nib - 8) * f32(d) )   (the product is exact)
+      Q8_0  32 elements per 34-byte block {fp16 d, int8[32]}.
+            value = bf16_rn( q * f32(d) )           (the product is exact)
+      bf16  the stored value.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+# NormalFloat-4 levels, fp32 (QLoRA's NormalFloat: 8 positive and 7 negative
+# standard-normal quantiles at probabilities evenly spaced from
+# delta = ((1 - 1/30) + (1 - 1/32)) / 2 to 1/2, plus an exact zero, divided by
+# the largest quantile, rounded to fp32).
+NF4_LEVELS = np.array([
+    -1.0, -0.6961928, -0.52507293, -0.39491743,
+    -0.28444132, -0.1847734, -0.09104998, 0.0,
+    0.079580314, 0.16093014, 0.24611226, 0.33791512,
+    0.44070974, 0.5626169, 0.72295666, 1.0,
+], dtype=np.float32)
+
+
+# ----------------------------------------------------------------------------
+# rounding helpers
+# ----------------------------------------------------------------------------
+def bf16_round_f32(x: np.ndarray) -> np.ndarray:
+    """Round fp32 to the nearest bf16 value (ties to even), returned as fp32."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    u = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)
+    return u.astype(np.uint32).view(np.float32)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+# ----------------------------------------------------------------------------
+# dequantisation (block decode)
+# ----------------------------------------------------------------------------
+def _dequant_nf4(w: Dict, N: int, K: int) -> np.ndarray:
+    packed = np.asarray(w["data"], dtype=np.uint8).reshape(-1)
+    assert packed.size == N * K // 2
+    codes = np.empty(N * K, dtype=np.uint8)
+    codes[0::2] = packed >> 4
+    codes[1::2] = packed & 0x0F
+    codes = codes.reshape(-1, 64)
+    nblk = codes.shape[0]
+    if "absmax" in w and w["absmax"] is not None:
+        amax = np.asarray(w["absmax"], dtype=np.float32).reshape(-1)
+    else:
+        q = np.asarray(w["absmax_q"], dtype=np.int8).reshape(-1).astype(np.float32)
+        scale2 = np.asarray(w["absmax_scale"], dtype=np.float32).reshape(-1)
+        group = int(w.get("dq_group", 256))
+        g = np.arange(nblk) // group
+        amax = (q * scale2[g]).astype(np.float32)          # fp32 product
+    assert amax.size == nblk
+    prod = (NF4_LEVELS[codes] * amax[:, None]).astype(np.float32)  # fp32 product
+    return bf16_round_f32(prod).astype(np.float64).reshape(N, K)
+
+
+def _gguf_blocks(w: Dict, N: int, K: int, rec: int) -> np.ndarray:
+    data = np.asarray(w["data"], dtype=np.uint8).reshape(-1)
+    assert data.size == N * K // 32 * rec
+    return data.reshape(-1, rec)
+
+
+def _dequant_q4_0(w: Dict, N: int, K: int) -> np.ndarray:
+    blk = _gguf_blocks(w, N, K, 18)
+    d = blk[:, 0:2].copy().view("<f2").astype(np.float32).reshape(-1)
+    qs = blk[:, 2:18]
+    nib = np.concatenate([qs & 0x0F, qs >> 4], axis=1).astype(np.int32)  # [nb, 32]
+    prod = ((nib - 8).astype(np.float32) * d[:, None]).astype(np.float32)
+    return bf16_round_f32(prod).astype(np.float64).reshape(N, K)
+
+
+def _dequant_q8_0(w: Dict, N: int, K: int) -> np.ndarray:
+    blk = _gguf_blocks(w, N, K, 34)
+    d = blk[:, 0:2].copy().view("<f2").astype(np.float32).reshape(-1)
+    q = blk[:, 2:34].copy().view(np.int8).astype(np.float32)
+    prod = (q * d[:, None]).astype(np.float32)
+    return bf16_round_f32(prod).astype(np.float64).reshape(N, K)
+
+
+def dequant(w: Dict) -> np.ndarray:
+    """Decoded base weight deq(Wq) as fp64 [N, K] (every value a bf16 value)."""
+    N, K, fmt = int(w["N"]), int(w["K"]), w["fmt"]
+    if fmt == "bf16":
+        return bf16_bits_to_f64(w["data"]).reshape(N, K)
+    if fmt == "nf4":
+        return _dequant_nf4(w, N, K)
+    if fmt == "q4_0":
+        return _dequant_q4_0(w, N, K)
+    if fmt == "q8_0":
+        return _dequant_q8_0(w, N, K)
+    raise ValueError(fmt)
+
+
+def dequant_bf16_bits(w: Dict) -> np.ndarray:
+    """deq(Wq) as bf16 bit patterns (uint16 [N, K]) for bit-exact comparison."""
+    v = dequant(w).astype(np.float32)
+    return (v.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+# the layer
+# ----------------------------------------------------------------------------
+def _f64(a) -> np.ndarray:
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return bf16_bits_to_f64(a)
+    return a.astype(np.float64)
+
+
+def linear_fwd(X, Wd, A, B, alpha: float):
+    """Y = X Wd^T + s (X A^T) B^T, s = alpha / r.  Returns (Y, T)."""
+    X, Wd, A, B = _f64(X), _f64(Wd), _f64(A), _f64(B)
+    r = A.shape[0]
+    s = float(alpha) / r
+    T = X @ A.T
+    Y = X @ Wd.T + s * (T @ B.T)
+    return Y, T
+
+
+def linear_fwd_rows(X_rows, Wd, A, B, alpha: float):
+    """Forward on a subset of rows (rows are independent)."""
+    return linear_fwd(X_rows, Wd, A, B, alpha)
+
+
+def linear_bwd(X, Wd, A, B, dY, alpha: float):
+    """Backward of the layer.  Returns dict with U, dX, dA, dB (fp64)."""
+    X, Wd, A, B, dY = _f64(X), _f64(Wd), _f64(A), _f64(B), _f64(dY)
+    r = A.shape[0]
+    s = float(alpha) / r
+    T = X @ A.T
+    U = dY @ B
+    dX = dY @ Wd + s * (U @ A)
+    dB = s * (dY.T @ T)
+    dA = s * (U.T @ X)
+    return {"T": T, "U": U, "dX": dX, "dA": dA, "dB": dB}
+
+
+def linear_bwd_rows(dY_rows, Wd, A, B, alpha: float):
+    """dX on a subset of rows: dY_rows Wd + s (dY_rows B) A."""
+    dY, Wd, A, B = _f64(dY_rows), _f64(Wd), _f64(A), _f64(B)
+    s = float(alpha) / A.shape[0]
+    return dY @ Wd + s * ((dY @ B) @ A)
+
+
+def linear_bwd_adapter_grads(X, A, B, dY, alpha: float):
+    """dA, dB (and T, U) over all rows without touching the base weight."""
+    X, A, B, dY = _f64(X), _f64(A), _f64(B), _f64(dY)
+    s = float(alpha) / A.shape[0]
+    T = X @ A.T
+    U = dY @ B
+    return {"T": T, "U": U, "dA": s * (U.T @ X), "dB": s * (dY.T @ T)}
+
+
+# ----------------------------------------------------------------------------
+# grouped (mixture-of-experts) variant: the same layer per expert over the
+# rows routed to it (rows sorted by expert, offsets[E+1]).
+# ----------------------------------------------------------------------------
+def grouped_fwd(X, Wds: Sequence[np.ndarray], A, B, offsets, alpha: float):
+    X = _f64(X)
+    E = len(Wds)
+    N = Wds[0].shape[0]
+    r = np.asarray(A).shape[1]
+    Y = np.zeros((X.shape[0], N))
+    T = np.zeros((X.shape[0], r))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            Y[lo:hi], T[lo:hi] = linear_fwd(X[lo:hi], Wds[e], A[e], B[e], alpha)
+    return Y, T
+
+
+def grouped_bwd(X, Wds: Sequence[np.ndarray], A, B, dY, offsets, alpha: float):
+    X, dY = _f64(X), _f64(dY)
+    E = len(Wds)
+    K = X.shape[1]
+    N = Wds[0].shape[0]
+    r = np.asarray(A).shape[1]
+    dX = np.zeros((X.shape[0], K))
+    dA = np.zeros((E, r, K))
+    dB = np.zeros((E, N, r))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            g = linear_bwd(X[lo:hi], Wds[e], A[e], B[e], dY[lo:hi], alpha)
+            dX[lo:hi], dA[e], dB[e] = g["dX"], g["dA"], g["dB"]
+    return {"dX": dX, "dA": dA, "dB": dB}
