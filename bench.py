@@ -1,0 +1,367 @@
+#!/usr/bin/env python
+"""Throughput of the LoRA linear over a frozen block-quantised base, fwd+bwd.
+
+One step = forward of the 7 LoRA-adapted linears of one decoder layer (q, k,
+v, o, gate, up, down), then their backward in reverse order, through the C ABI
+(qlora_linear_fwd / qlora_linear_bwd).  Default workload: Llama-3.1-8B layer
+shapes, NF4 base with double-quantised absmax, M = 4096 tokens, rank 16,
+alpha 16; inputs synthetic and seeded.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica on its own GPU (the layer needs no exchange between replicas).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import qlora_synth as syn  # noqa: E402
+
+METRIC = "QLoRA linear fwd+bwd tokens/s and TFLOP/s vs GB300 dense BF16 roofline"
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 7900.0
+CPU_SAMPLE_ROWS = 64
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="llama31_8b_nf4dq", choices=sorted(syn.WORKLOADS))
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16": float(d["bf16_tflops"]), "bf16_sustained": float(d["bf16_tflops_sustained"]),
+                "hbm": float(d["hbm_gbs"]), "source": "measured"}
+    return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas)
+# ----------------------------------------------------------------------------
+def dist_init(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (baseline only; never part of the GPU path)
+# ----------------------------------------------------------------------------
+def oracle_step(inputs, rows: int):
+    import oracle
+
+    for inp in inputs:
+        Wd = oracle.dequant(inp["W"])
+        X, dY = inp["X"][:rows], inp["dY"][:rows]
+        oracle.linear_fwd(X, Wd, inp["A"], inp["B"], inp["alpha"])
+        oracle.linear_bwd(X, Wd, inp["A"], inp["B"], dY, inp["alpha"])
+
+
+def cpu_threads() -> int:
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            return int(os.environ[k])
+    return os.cpu_count() or 1
+
+
+def time_oracle(inputs, rows: int, reps: int = 1) -> float:
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(inputs, rows)
+    return (time.perf_counter() - t0) / reps
+
+
+# ----------------------------------------------------------------------------
+def make_inputs(wl):
+    return [syn.make_linear_inputs(wl, i, seed=0) for i in range(len(wl.linears))]
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_init(args.gpus)
+    if rank != 0:
+        return
+    inputs = make_inputs(wl)
+    rows = 16
+    for _ in range(args.warmup):
+        oracle_step(inputs, rows)
+    t = time_oracle(inputs, rows, reps=args.steps)
+    value = rows / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"{rows} of {wl.M} rows per step, all {len(wl.linears)} linears fwd+bwd, "
+                                   f"block decode of every base weight included"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl):
+    return {"workload": f"{wl.name}_layer", "format": wl.fmt + ("+dq" if wl.double_quant else ""), "M": wl.M,
+            "rank": wl.rank, "alpha": wl.alpha,
+            "linears": [f"{l.name}:{l.K}->{l.N}" for l in wl.linears],
+            "step": "fwd of the 7 linears, then bwd in reverse order",
+            "l2": "per-step working set (weights + activations) > 1 GB, larger than the 129 MB L2; no flush",
+            "parallelism": "replicas"}
+
+
+def main():
+    args = parse_args()
+    wl = syn.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+
+    import quantized_base_lora_block_gb300 as q
+
+    rank, world, local = dist_init(args.gpus)
+    torch.cuda.set_device(local)
+    q.load()
+    dev = torch.device("cuda", local)
+    inputs = make_inputs(wl)
+    M, r, alpha = wl.M, wl.rank, wl.alpha
+    L = []
+    ws_bytes = 0
+    for inp in inputs:
+        w = q.DeviceWeight.from_packed(inp["W"], device=dev)
+        d = {"W": w, "K": inp["K"], "N": inp["N"]}
+        for k in ("X", "A", "B", "dY"):
+            d[k] = q.bf16_from_bits(inp[k], device=dev)
+        d["Y"] = torch.empty((M, inp["N"]), dtype=torch.bfloat16, device=dev)
+        d["T"] = torch.empty((M, r), dtype=torch.float32, device=dev)
+        d["dX"] = torch.empty((M, inp["K"]), dtype=torch.bfloat16, device=dev)
+        d["dA"] = torch.empty((r, inp["K"]), dtype=torch.float32, device=dev)
+        d["dB"] = torch.empty((inp["N"], r), dtype=torch.float32, device=dev)
+        ws_bytes = max(ws_bytes, q.workspace_bytes(w, M, r))
+        L.append(d)
+    ws = q.alloc_workspace(ws_bytes, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for d in L:
+            q.linear_fwd(d["W"], d["X"], d["A"], d["B"], alpha, Y=d["Y"], T=d["T"], workspace=ws, stream=stream)
+        for d in reversed(L):
+            q.linear_bwd(d["W"], d["X"], d["A"], d["B"], d["T"], d["dY"], alpha, dX=d["dX"], dA=d["dA"],
+                         dB=d["dB"], workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert q.device_error() == 0, "device error during warm-up"
+
+    # --------------------------------------------------------- timed region
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    q.profile_gemm(True)
+    n0 = q.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = q.launch_count() - n0
+    q.profile_gemm(False)
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop() if clocks else None
+    gemm_ms, gemm_n, gemm_flops = q.profile_gemm_read()
+    assert q.device_error() == 0, "device error in the timed region"
+    ms_max = max_over_ranks(ms, world)
+
+    flops_step = sum(syn.linear_flops(M, l.K, l.N, r) for l in wl.linears)
+    t_step = ms_max / args.steps / 1e3
+    value = world * M / t_step
+    peaks = measured_peaks()
+    ach = gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else 0.0
+    roofline = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_sustained"], "traffic": None,
+                "kernel": "qgemm_kernel (fused decode + tcgen05 GEMM + adapter chunk), fwd and dX launches",
+                "peak_kind": f"{peaks['source']} sustained bf16",
+                "frac_of_burst": ach / peaks["bf16"], "frac_of_nominal_2250": ach / NOMINAL_BF16_TFLOPS,
+                "launches": gemm_n, "share_of_step": gemm_ms / ms if ms > 0 else None}
+
+    # --------------------------------------------------------- end to end
+    e2e = None
+    if not args.no_e2e:
+        hX = [torch.empty(d["X"].shape, dtype=torch.bfloat16).pin_memory() for d in L]
+        hdY = [torch.empty(d["dY"].shape, dtype=torch.bfloat16).pin_memory() for d in L]
+        for h, d in zip(hX, L):
+            h.copy_(d["X"])
+        for h, d in zip(hdY, L):
+            h.copy_(d["dY"])
+        hdA = [torch.empty(d["dA"].shape, dtype=torch.float32).pin_memory() for d in L]
+        hdB = [torch.empty(d["dB"].shape, dtype=torch.float32).pin_memory() for d in L]
+        h2d = sum(h.numel() * 2 for h in hX + hdY)
+        d2h = sum(h.numel() * 4 for h in hdA + hdB)
+
+        def e2e_step():
+            for d, hx, hy in zip(L, hX, hdY):
+                d["X"].copy_(hx, non_blocking=True)
+                d["dY"].copy_(hy, non_blocking=True)
+            step()
+            for d, ha, hb in zip(L, hdA, hdB):
+                ha.copy_(d["dA"], non_blocking=True)
+                hb.copy_(d["dB"], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world)
+        e2e = {"value": world * M * args.steps / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h,
+               "note": "pinned host X and dY copied in, dA and dB copied out, every step, same stream"}
+
+    # --------------------------------------------------------- CPU oracle
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = CPU_SAMPLE_ROWS
+        t = time_oracle(inputs, rows, reps=2)
+        cpu = {"value": rows / t, "unit": "tokens/s", "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"{rows} of {M} rows, all {len(wl.linears)} linears fwd+bwd, fp64, block decode of "
+                         f"every base weight included; {2 * t:.1f} s for 2 repetitions"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(wl),
+            "tflops": flops_step / t_step / 1e12 * world,
+            "frac_of_nominal_2250": flops_step / t_step / 1e12 / NOMINAL_BF16_TFLOPS,
+            "frac_of_measured_sustained": flops_step / t_step / 1e12 / peaks["bf16_sustained"],
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

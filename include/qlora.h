@@ -1,0 +1,206 @@
+/*
+ * qlora.h -- C ABI of the GB300 (sm_103a) LoRA linear over a frozen,
+ * block-quantised base weight.
+ *
+ * The operation (forward and the "fast backward formulas" of LoRA; bytechap
+ * GGUF blog, "How it works"; the base is frozen, "read, never written", Soup
+ * show post, first paragraph):
+ *
+ *     s  = alpha / r
+ *     T  = X A^T                          [M x r]
+ *     Y  = X deq(Wq)^T + s T B^T          [M x N]
+ *     U  = dY B                           [M x r]
+ *     dX = dY deq(Wq) + s U A             [M x K]
+ *     dB = s dY^T T                       [N x r]
+ *     dA = s U^T X                        [r x K]
+ *
+ * Base formats (Surogate README, capability table, "LoRA & QLoRA": BF16 and
+ * BnB/NF4 bases; bytechap GGUF blog, "How it works": GGUF bases):
+ *   BF16  W itself, bf16 [N x K] row-major.
+ *   NF4   64 consecutive K-elements per block, two 4-bit codes per byte
+ *         (element 2j in the high nibble of byte j), codes [N*K/2] bytes;
+ *         per block an fp32 absmax [N*K/64], or (double quantisation) an int8
+ *         absmax_q [N*K/64] with one fp32 absmax_scale per dq_group (=256)
+ *         consecutive blocks.  Decoded value:
+ *             bf16_rn( f32_rn( level[c] * absmax' ) ),
+ *             absmax' = absmax or f32_rn( f32(absmax_q) * absmax_scale ).
+ *         level[] = the 16 NormalFloat-4 levels (normal quantiles incl. an
+ *         exact 0, scaled to [-1, 1]) as fp32.
+ *   Q8_0  GGUF: blocks of 32 along K, 34 bytes {fp16 d; int8 q[32]};
+ *         value = bf16_rn( q * f32(d) ).
+ *   Q4_0  GGUF: blocks of 32 along K, 18 bytes {fp16 d; uint8 qs[16]};
+ *         element i < 16 = low nibble of qs[i], element i+16 = high nibble;
+ *         value = bf16_rn( (nib - 8) * f32(d) ).
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise, owned
+ *     and allocated by the caller, 16-byte aligned, row-major, densely packed.
+ *   - X, A, B, Y, dY, dX are bf16 (passed as void*); T_save, dA, dB are fp32;
+ *     dA and dB are overwritten (not accumulated).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     only enqueues work on it and returns; nothing synchronises.
+ *   - Arguments are validated before anything is launched; a rejected call
+ *     launches nothing and returns a negative qlora_status.
+ *   - A kernel whose internal wait runs out (it never should) records
+ *     QLORA_ERR_TIMEOUT in a device error word, which qlora_device_error()
+ *     reads after the caller has synchronised.
+ *   - Limits: N % 64 == 0, K % 64 == 0, 8 <= rank <= 64 with rank % 8 == 0,
+ *     M >= 0 (M == 0 is a no-op that returns QLORA_OK).
+ */
+#ifndef QLORA_H_
+#define QLORA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QLORA_FMT_BF16 = 0,
+  QLORA_FMT_NF4 = 1,
+  QLORA_FMT_Q8_0 = 2,
+  QLORA_FMT_Q4_0 = 3
+} qlora_format;
+
+typedef enum {
+  QLORA_OK = 0,
+  QLORA_ERR_INVALID = -1,     /* bad shape, rank, null pointer, format */
+  QLORA_ERR_UNSUPPORTED = -2, /* valid request this library does not cover */
+  QLORA_ERR_ALIGN = -3,       /* pointer not 16-byte aligned */
+  QLORA_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed */
+  QLORA_ERR_TIMEOUT = -5,     /* a bounded device wait gave up */
+  QLORA_ERR_WORKSPACE = -6,   /* workspace missing or too small */
+  QLORA_ERR_STATE = -7        /* streaming pool used out of order */
+} qlora_status;
+
+/* Frozen base weight W [N x K] in one of the four formats.  Every pointer is
+ * a read-only device pointer; unused ones must be NULL. */
+typedef struct {
+  int32_t fmt;                /* qlora_format */
+  int32_t dq_group;           /* NF4 double quantisation group (256), else 0 */
+  int64_t N;                  /* output features (rows of W) */
+  int64_t K;                  /* input features (columns of W) */
+  const void* data;           /* BF16: bf16[N*K]; NF4: uint8[N*K/2];
+                                 Q8_0: 34-byte blocks [N*K/32];
+                                 Q4_0: 18-byte blocks [N*K/32] */
+  const float* absmax;        /* NF4 without double quantisation: fp32[N*K/64] */
+  const int8_t* absmax_q;     /* NF4 with double quantisation: int8[N*K/64] */
+  const float* absmax_scale;  /* NF4 with double quantisation:
+                                 fp32[ceil(N*K/64 / dq_group)] */
+} qlora_weight_desc;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* qlora_status_string(int32_t status);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t qlora_version(void);
+
+/* Bytes of device workspace that qlora_linear_fwd and qlora_linear_bwd need
+ * for this weight shape, M and rank (the larger of the two).  0 on invalid
+ * arguments.  The workspace holds the scaled adapter activations s*T, s*U
+ * (bf16) and fp32 partial sums of the split reductions. */
+size_t qlora_workspace_bytes(const qlora_weight_desc* w, int64_t M, int32_t rank);
+
+/* Decode the whole base weight to bf16: W_bf16[N*K] (device, caller-owned)
+ * receives deq(Wq) bit-exactly as defined above.  For QLORA_FMT_BF16 it is a
+ * copy. */
+int32_t dequant_blocks(const qlora_weight_desc* w, void* W_bf16, void* stream);
+
+/* Forward: Y[M x N] = X deq(Wq)^T + s (X A^T) B^T, and T_save[M x rank] =
+ * X A^T (fp32, kept for the backward pass).
+ *   X [M x K], A [rank x K], B [N x rank], Y [M x N] bf16; T_save [M x rank]
+ *   fp32.  The adapter term enters Y through bf16(s T).
+ *   workspace: device, at least qlora_workspace_bytes(w, M, rank) bytes.
+ * The base is decoded inside the GEMM's operand producer; the decoded weight
+ * never goes to global memory. */
+int32_t qlora_linear_fwd(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha,
+                         const void* X, const void* A, const void* B,
+                         void* Y, float* T_save,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+/* Backward: dX[M x K] = dY deq(Wq) + s (dY B) A;  dA[rank x K] (fp32) =
+ * s (dY B)^T X;  dB[N x rank] (fp32) = s dY^T T_save.  dX may be NULL (then
+ * only dA and dB are produced).  T_save is the forward's fp32 output.  U = dY B
+ * is kept in fp32 for dA; the adapter term of dX enters through bf16(s U).
+ * The base is never written. */
+int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha,
+                         const void* X, const void* A, const void* B,
+                         const float* T_save, const void* dY,
+                         void* dX, float* dA, float* dB,
+                         void* workspace, size_t ws_bytes, void* stream);
+
+/* ---- grouped (mixture-of-experts) variant -------------------------------
+ * The same layer for E experts (bytechap GGUF blog: fast LoRA backward for
+ * linear and MoE layers).  Rows of X / dY / Y / dX / T_save are sorted by
+ * expert: expert e owns rows offsets[e] .. offsets[e+1]-1 (offsets: HOST
+ * int32[E+1], offsets[0] == 0, non-decreasing, offsets[E] == M_total; empty
+ * experts allowed).  experts: HOST array of E weight descriptors, all with the
+ * same fmt, N and K.  A: bf16 [E][rank][K], B: bf16 [E][N][rank], dA: fp32
+ * [E][rank][K], dB: fp32 [E][N][rank]; experts with no rows get dA = dB = 0.
+ * E <= 256.  Workspace: qlora_grouped_workspace_bytes(). */
+size_t qlora_grouped_workspace_bytes(const qlora_weight_desc* experts, int32_t E,
+                                     const int32_t* offsets, int32_t rank);
+
+int32_t grouped_moe_qlora_fwd(const qlora_weight_desc* experts, int32_t E,
+                              const int32_t* offsets, int32_t rank, float alpha,
+                              const void* X, const void* A, const void* B,
+                              void* Y, float* T_save,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+int32_t grouped_moe_qlora_bwd(const qlora_weight_desc* experts, int32_t E,
+                              const int32_t* offsets, int32_t rank, float alpha,
+                              const void* X, const void* A, const void* B,
+                              const float* T_save, const void* dY,
+                              void* dX, float* dA, float* dB,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+/* ---- layer streaming ------------------------------------------------------
+ * A frozen base kept in pinned host memory is streamed into a fixed pool of
+ * device buffers one layer ahead of use on a dedicated copy stream (Soup show
+ * post, first paragraph: "a small pool of pre-allocated VRAM buffers, one
+ * decoder layer at a time, prefetched one ahead on a dedicated CUDA stream").
+ *
+ * qlora_stream_create: allocates `slots` device buffers of `slot_bytes` each
+ *   (the only memory this library allocates), a copy stream and events.
+ * qlora_stream_prefetch: enqueue the host->device copy of `bytes` bytes at
+ *   `host_src` (pinned host memory, must stay valid until the copy ran) into
+ *   the next slot in round-robin order, tagged with `layer`.  The copy waits
+ *   until every earlier compute-stream use of that slot was released.
+ *   Returns QLORA_ERR_STATE if that slot is still acquired.
+ * qlora_stream_acquire: make `compute_stream` wait for the copy of `layer`
+ *   and return the slot's device address in *dev_ptr.  QLORA_ERR_STATE if no
+ *   slot holds `layer` (never prefetched, or already overwritten).
+ * qlora_stream_release: record on `compute_stream` that work reading `layer`
+ *   has been enqueued; the slot may be refilled after that work.
+ * qlora_stream_destroy: synchronise and free everything. */
+int32_t qlora_stream_create(int32_t slots, size_t slot_bytes, void** handle);
+int32_t qlora_stream_prefetch(void* handle, int32_t layer, const void* host_src, size_t bytes);
+int32_t qlora_stream_acquire(void* handle, int32_t layer, void* compute_stream, void** dev_ptr);
+int32_t qlora_stream_release(void* handle, int32_t layer, void* compute_stream);
+int32_t qlora_stream_destroy(void* handle);
+
+/* Read the device error word written by bounded waits (QLORA_OK if none).
+ * Call after synchronising the streams the library used.  clear != 0 resets
+ * it.  This call synchronises the device. */
+int32_t qlora_device_error(int32_t clear);
+
+/* Number of this library's kernels launched since load (host-side count). */
+int64_t qlora_launch_count(void);
+
+/* Instrumentation of the fused tensor-core GEMM (the dominant kernel).
+ * qlora_profile_gemm(1) clears the record and starts recording a CUDA event
+ * pair around every fused-GEMM launch, on the stream it is launched on;
+ * qlora_profile_gemm(0) stops recording.  qlora_profile_gemm_read()
+ * synchronises on the recorded events and returns the summed device time
+ * (ms), the number of launches and their summed algorithmic flops
+ * (2 M n_out (k_red + rank) per launch).  Host pointers; any may be NULL. */
+int32_t qlora_profile_gemm(int32_t enable);
+int32_t qlora_profile_gemm_read(double* total_ms, int64_t* launches, double* flops);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLORA_H_ */

@@ -1,0 +1,277 @@
+"""Python binding of the GB300 quantised-base LoRA linear library (libqlora.so).
+
+Argument marshalling only: every computation runs in the CUDA library.  PyTorch
+provides device memory and streams.  If the compiled library is missing, every
+call raises; there is no fallback path.
+
+    import quantized_base_lora_block_gb300 as q
+    w = q.DeviceWeight.from_packed(packed)          # frozen base on the GPU
+    Y, T = q.linear_fwd(w, X, A, B, alpha)
+    dX, dA, dB = q.linear_bwd(w, X, A, B, T, dY, alpha)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libqlora.so")
+
+FMT = {"bf16": 0, "nf4": 1, "q8_0": 2, "q4_0": 3}
+
+STATUS = {
+    0: "ok", -1: "invalid argument", -2: "unsupported", -3: "pointer not 16-byte aligned",
+    -4: "CUDA error", -5: "device wait timed out", -6: "workspace missing or too small",
+    -7: "streaming pool used out of order",
+}
+
+
+class QloraError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)} ({status})")
+        self.status = status
+
+
+class WeightDesc(ctypes.Structure):
+    _fields_ = [
+        ("fmt", ctypes.c_int32),
+        ("dq_group", ctypes.c_int32),
+        ("N", ctypes.c_int64),
+        ("K", ctypes.c_int64),
+        ("data", ctypes.c_void_p),
+        ("absmax", ctypes.c_void_p),
+        ("absmax_q", ctypes.c_void_p),
+        ("absmax_scale", ctypes.c_void_p),
+    ]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+# name -> (restype, argtypes)
+_P, _I32, _I64, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_WD = ctypes.POINTER(WeightDesc)
+SIGNATURES = {
+    "qlora_status_string": (ctypes.c_char_p, [_I32]),
+    "qlora_version": (_I32, []),
+    "qlora_workspace_bytes": (_SZ, [_WD, _I64, _I32]),
+    "dequant_blocks": (_I32, [_WD, _P, _P]),
+    "qlora_linear_fwd": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "qlora_linear_bwd": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "qlora_grouped_workspace_bytes": (_SZ, [_WD, _I32, ctypes.POINTER(ctypes.c_int32), _I32]),
+    "grouped_moe_qlora_fwd": (_I32, [_WD, _I32, ctypes.POINTER(ctypes.c_int32), _I32, _F32, _P, _P, _P, _P, _P,
+                                     _P, _SZ, _P]),
+    "grouped_moe_qlora_bwd": (_I32, [_WD, _I32, ctypes.POINTER(ctypes.c_int32), _I32, _F32, _P, _P, _P, _P, _P,
+                                     _P, _P, _P, _P, _SZ, _P]),
+    "qlora_stream_create": (_I32, [_I32, _SZ, ctypes.POINTER(ctypes.c_void_p)]),
+    "qlora_stream_prefetch": (_I32, [_P, _I32, _P, _SZ]),
+    "qlora_stream_acquire": (_I32, [_P, _I32, _P, ctypes.POINTER(ctypes.c_void_p)]),
+    "qlora_stream_release": (_I32, [_P, _I32, _P]),
+    "qlora_stream_destroy": (_I32, [_P]),
+    "qlora_device_error": (_I32, [_I32]),
+    "qlora_launch_count": (_I64, []),
+    "qlora_profile_gemm": (_I32, [_I32]),
+    "qlora_profile_gemm_read": (_I32, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
+                                       ctypes.POINTER(ctypes.c_double)]),
+}
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libqlora.so (built by ``build.py``).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m quantized_base_lora_block_gb300.build`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise QloraError(fn, status)
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream_ptr(stream=None) -> int:
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+# ---------------------------------------------------------------------------
+# host <-> device helpers (torch only as an allocator)
+# ---------------------------------------------------------------------------
+def bf16_from_bits(bits: np.ndarray, device="cuda"):
+    torch = _torch()
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+    return t.to(device)
+
+
+def bits_from_bf16(t) -> np.ndarray:
+    torch = _torch()
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _bytes_to_device(a: np.ndarray, device="cuda"):
+    torch = _torch()
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).reshape(-1)).to(device)
+
+
+class DeviceWeight:
+    """A frozen base weight resident on the GPU plus its C descriptor."""
+
+    def __init__(self, fmt: str, N: int, K: int, data, absmax=None, absmax_q=None, absmax_scale=None,
+                 dq_group: int = 0):
+        self.fmt, self.N, self.K = fmt, int(N), int(K)
+        self.data, self.absmax, self.absmax_q, self.absmax_scale = data, absmax, absmax_q, absmax_scale
+        self.desc = WeightDesc(FMT[fmt], int(dq_group), self.N, self.K, _ptr(data), _ptr(absmax), _ptr(absmax_q),
+                               _ptr(absmax_scale))
+
+    @classmethod
+    def from_packed(cls, p: Dict, device="cuda") -> "DeviceWeight":
+        torch = _torch()
+        data = _bytes_to_device(p["data"], device)
+        absmax = absmax_q = absmax_scale = None
+        if p["fmt"] == "nf4":
+            if "absmax" in p:
+                absmax = torch.from_numpy(np.ascontiguousarray(p["absmax"], np.float32)).to(device)
+            else:
+                absmax_q = torch.from_numpy(np.ascontiguousarray(p["absmax_q"], np.int8)).to(device)
+                absmax_scale = torch.from_numpy(np.ascontiguousarray(p["absmax_scale"], np.float32)).to(device)
+        return cls(p["fmt"], p["N"], p["K"], data, absmax, absmax_q, absmax_scale, p.get("dq_group", 0))
+
+    def nbytes(self) -> int:
+        n = 0
+        for t in (self.data, self.absmax, self.absmax_q, self.absmax_scale):
+            if t is not None:
+                n += t.numel() * t.element_size()
+        return n
+
+
+# ---------------------------------------------------------------------------
+# calls
+# ---------------------------------------------------------------------------
+def workspace_bytes(w: DeviceWeight, M: int, rank: int) -> int:
+    return int(load().qlora_workspace_bytes(ctypes.byref(w.desc), int(M), int(rank)))
+
+
+def alloc_workspace(nbytes: int, device="cuda"):
+    torch = _torch()
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def dequant_blocks(w: DeviceWeight, out=None, stream=None):
+    torch = _torch()
+    if out is None:
+        out = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=w.data.device)
+    _check("dequant_blocks", load().dequant_blocks(ctypes.byref(w.desc), _ptr(out), _stream_ptr(stream)))
+    return out
+
+
+def linear_fwd(w: DeviceWeight, X, A, B, alpha: float, Y=None, T=None, workspace=None, stream=None):
+    """Y = X deq(W)^T + (alpha/r) (X A^T) B^T; returns (Y, T_save)."""
+    torch = _torch()
+    M, r = X.shape[0], A.shape[0]
+    if Y is None:
+        Y = torch.empty((M, w.N), dtype=torch.bfloat16, device=X.device)
+    if T is None:
+        T = torch.empty((M, r), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_bytes(w, M, r), X.device)
+    st = load().qlora_linear_fwd(ctypes.byref(w.desc), M, r, float(alpha), _ptr(X), _ptr(A), _ptr(B), _ptr(Y),
+                                 _ptr(T), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check("qlora_linear_fwd", st)
+    return Y, T
+
+
+def linear_bwd(w: DeviceWeight, X, A, B, T, dY, alpha: float, dX=None, dA=None, dB=None, workspace=None,
+               stream=None, want_dx: bool = True):
+    """Returns (dX, dA, dB); dX is None when want_dx is False."""
+    torch = _torch()
+    M, r = X.shape[0], A.shape[0]
+    if dX is None and want_dx:
+        dX = torch.empty((M, w.K), dtype=torch.bfloat16, device=X.device)
+    if dA is None:
+        dA = torch.empty((r, w.K), dtype=torch.float32, device=X.device)
+    if dB is None:
+        dB = torch.empty((w.N, r), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_bytes(w, M, r), X.device)
+    st = load().qlora_linear_bwd(ctypes.byref(w.desc), M, r, float(alpha), _ptr(X), _ptr(A), _ptr(B), _ptr(T),
+                                 _ptr(dY), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(workspace), workspace.numel(),
+                                 _stream_ptr(stream))
+    _check("qlora_linear_bwd", st)
+    return dX, dA, dB
+
+
+def device_error(clear: bool = True) -> int:
+    return int(load().qlora_device_error(1 if clear else 0))
+
+
+def launch_count() -> int:
+    return int(load().qlora_launch_count())
+
+
+def profile_gemm(enable: bool) -> None:
+    _check("qlora_profile_gemm", load().qlora_profile_gemm(1 if enable else 0))
+
+
+def profile_gemm_read() -> Tuple[float, int, float]:
+    """(summed device ms, launches, summed algorithmic flops) of the fused GEMM."""
+    ms, n, fl = ctypes.c_double(), ctypes.c_int64(), ctypes.c_double()
+    _check("qlora_profile_gemm_read", load().qlora_profile_gemm_read(ctypes.byref(ms), ctypes.byref(n),
+                                                                     ctypes.byref(fl)))
+    return ms.value, n.value, fl.value
+
+
+# ---------------------------------------------------------------------------
+# layer streaming
+# ---------------------------------------------------------------------------
+class LayerStream:
+    """Pool of device slots fed from pinned host memory one layer ahead."""
+
+    def __init__(self, slots: int, slot_bytes: int):
+        h = ctypes.c_void_p()
+        _check("qlora_stream_create", load().qlora_stream_create(int(slots), int(slot_bytes), ctypes.byref(h)))
+        self.h = h
+
+    def prefetch(self, layer: int, host_pinned) -> None:
+        nbytes = host_pinned.numel() * host_pinned.element_size()
+        _check("qlora_stream_prefetch", load().qlora_stream_prefetch(self.h, int(layer), _ptr(host_pinned), nbytes))
+
+    def acquire(self, layer: int, stream=None) -> int:
+        p = ctypes.c_void_p()
+        _check("qlora_stream_acquire",
+               load().qlora_stream_acquire(self.h, int(layer), _stream_ptr(stream), ctypes.byref(p)))
+        return int(p.value)
+
+    def release(self, layer: int, stream=None) -> None:
+        _check("qlora_stream_release", load().qlora_stream_release(self.h, int(layer), _stream_ptr(stream)))
+
+    def close(self) -> None:
+        if self.h is not None and self.h.value:
+            _check("qlora_stream_destroy", load().qlora_stream_destroy(self.h))
+        self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,259 @@
+// Block decoders: one "line" = 64 consecutive K-elements of one weight row,
+// decoded to 64 bf16 values = 8 x uint4 (chunk j holds elements 8j..8j+7,
+// element 8j in the low half of .x).
+//
+// Decode rules (bit-exact):
+//   NF4  bf16_rn( f32_rn(level[c] * absmax') ),  absmax' = absmax or
+//        f32_rn(f32(absmax_q) * absmax_scale)
+//   Q4_0 bf16_rn( (nib - 8) * f32(d) )   (the fp32 product is exact)
+//   Q8_0 bf16_rn( q * f32(d) )           (the fp32 product is exact)
+//
+// NF4 and Q4_0 have 16 possible values per block: the block's 16 decoded
+// bf16 values are computed once (16 fp32 multiplies + 8 conversions) and split
+// into a low-byte and a high-byte plane of 16 bytes each (4 registers each).
+// Each 4-bit code then picks its two bytes with byte permutes (prmt), so the
+// per-element work is a handful of integer ops and no memory lookup.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace qlora {
+
+// NormalFloat-4 levels as fp32 (16 standard-normal quantiles incl. an exact
+// zero, divided by the largest).
+__device__ __forceinline__ float nf4_level(int c) {
+  switch (c) {
+    case 0: return -1.0f;
+    case 1: return -0.6961928f;
+    case 2: return -0.52507293f;
+    case 3: return -0.39491743f;
+    case 4: return -0.28444132f;
+    case 5: return -0.1847734f;
+    case 6: return -0.09104998f;
+    case 7: return 0.0f;
+    case 8: return 0.079580314f;
+    case 9: return 0.16093014f;
+    case 10: return 0.24611226f;
+    case 11: return 0.33791512f;
+    case 12: return 0.44070974f;
+    case 13: return 0.5626169f;
+    case 14: return 0.72295666f;
+    default: return 1.0f;
+  }
+}
+
+// 16-entry byte-plane table of one block.
+struct Lut16 {
+  uint32_t lo[4];  // low bytes of entries 0..15
+  uint32_t hi[4];  // high bytes of entries 0..15
+};
+
+// pairs[i] = bf16(v[2i]) | bf16(v[2i+1]) << 16
+__device__ __forceinline__ Lut16 lut_from_pairs(const uint32_t (&pairs)[8]) {
+  Lut16 t;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    t.lo[i] = prmt(pairs[2 * i], pairs[2 * i + 1], 0x6420);
+    t.hi[i] = prmt(pairs[2 * i], pairs[2 * i + 1], 0x7531);
+  }
+  return t;
+}
+
+__device__ __forceinline__ Lut16 lut_nf4(float amax) {
+  uint32_t pairs[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float a = __fmul_rn(nf4_level(2 * i), amax);
+    float b = __fmul_rn(nf4_level(2 * i + 1), amax);
+    pairs[i] = pack_bf16x2(a, b);
+  }
+  return lut_from_pairs(pairs);
+}
+
+__device__ __forceinline__ Lut16 lut_q4_0(float d) {
+  uint32_t pairs[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float a = __fmul_rn((float)(2 * i - 8), d);
+    float b = __fmul_rn((float)(2 * i + 1 - 8), d);
+    pairs[i] = pack_bf16x2(a, b);
+  }
+  return lut_from_pairs(pairs);
+}
+
+// Look up 4 codes held in the 4 nibbles of s (bits 0..15): byte i of *L / *H
+// receives the low / high byte of entry (nibble i).
+__device__ __forceinline__ void lut_lookup4(const Lut16& t, uint32_t s, uint32_t& L, uint32_t& H) {
+  const uint32_t sel = s & 0x7777u;
+  const uint32_t m = prmt(0x0000FF00u, 0u, (s >> 3) & 0x1111u);  // 0xFF where code >= 8
+  const uint32_t la = prmt(t.lo[0], t.lo[1], sel);
+  const uint32_t lb = prmt(t.lo[2], t.lo[3], sel);
+  const uint32_t ha = prmt(t.hi[0], t.hi[1], sel);
+  const uint32_t hb = prmt(t.hi[2], t.hi[3], sel);
+  L = (la & ~m) | (lb & m);
+  H = (ha & ~m) | (hb & m);
+}
+
+// ---------------------------------------------------------------- NF4 -------
+// codes: 32 bytes (64 codes, element 2j in the high nibble of byte j).
+__device__ __forceinline__ void decode_nf4_line(const uint4 c0, const uint4 c1, float amax, uint4 (&out)[8]) {
+  const Lut16 t = lut_nf4(amax);
+  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t L, H, r[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      lut_lookup4(t, w[j] >> (16 * h), L, H);
+      // byte order of L/H: e(4h+1), e(4h+0), e(4h+3), e(4h+2)
+      r[2 * h + 0] = prmt(L, H, 0x4051);  // elements 4h+0, 4h+1
+      r[2 * h + 1] = prmt(L, H, 0x6273);  // elements 4h+2, 4h+3
+    }
+    out[j] = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+}
+
+// ---------------------------------------------------------------- Q4_0 ------
+// words: the 36 bytes of two consecutive 18-byte blocks (4-byte aligned).
+__device__ __forceinline__ void decode_q4_0_block(uint32_t d_bits, const uint32_t (&qs)[4], uint4* out4) {
+  const float d = __half2float(__ushort_as_half((unsigned short)(d_bits & 0xFFFFu)));
+  const Lut16 t = lut_q4_0(d);
+  uint32_t lowp[8], highp[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t L, H;
+      lut_lookup4(t, qs[q] >> (16 * h), L, H);
+      // byte order: e(4q+2h), e(16+4q+2h), e(4q+2h+1), e(16+4q+2h+1)
+      lowp[2 * q + h] = prmt(L, H, 0x6240);
+      highp[2 * q + h] = prmt(L, H, 0x7351);
+    }
+  }
+  out4[0] = make_uint4(lowp[0], lowp[1], lowp[2], lowp[3]);
+  out4[1] = make_uint4(lowp[4], lowp[5], lowp[6], lowp[7]);
+  out4[2] = make_uint4(highp[0], highp[1], highp[2], highp[3]);
+  out4[3] = make_uint4(highp[4], highp[5], highp[6], highp[7]);
+}
+
+__device__ __forceinline__ void decode_q4_0_line(const uint32_t (&W)[9], uint4 (&out)[8]) {
+  uint32_t qs0[4], qs1[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    qs0[q] = prmt(W[q], W[q + 1], 0x5432);  // bytes 2+4q .. 5+4q
+    qs1[q] = W[5 + q];                      // bytes 20+4q .. 23+4q
+  }
+  decode_q4_0_block(W[0], qs0, &out[0]);
+  decode_q4_0_block(W[4] >> 16, qs1, &out[4]);
+}
+
+// ---------------------------------------------------------------- Q8_0 ------
+// Four int8 in one word -> two bf16x2 words.  int -> float by the magic
+// number 2^23: float bits 0x4B0000uu = 8388608 + uu, exact for bytes.
+__device__ __forceinline__ void decode_q8_word(uint32_t q, float d, uint32_t& r0, uint32_t& r1) {
+  const uint32_t u = q ^ 0x80808080u;  // q + 128 as unsigned bytes
+  float f[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[i] = __uint_as_float(prmt(u, 0x4B000000u, 0x7440u + i)) - 8388736.0f;  // exact: q
+    f[i] = __fmul_rn(f[i], d);                                            // exact product
+  }
+  r0 = pack_bf16x2(f[0], f[1]);
+  r1 = pack_bf16x2(f[2], f[3]);
+}
+
+__device__ __forceinline__ void decode_q8_0_block(uint32_t d_bits, const uint32_t (&qw)[8], uint4* out4) {
+  const float d = __half2float(__ushort_as_half((unsigned short)(d_bits & 0xFFFFu)));
+  uint32_t r[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) decode_q8_word(qw[j], d, r[2 * j], r[2 * j + 1]);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) out4[c] = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+}
+
+// words: the 68 bytes of two consecutive 34-byte blocks (4-byte aligned).
+__device__ __forceinline__ void decode_q8_0_line(const uint32_t (&W)[17], uint4 (&out)[8]) {
+  uint32_t q0[8], q1[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    q0[j] = prmt(W[j], W[j + 1], 0x5432);  // bytes 2+4j .. 5+4j
+    q1[j] = W[9 + j];                      // bytes 36+4j .. 39+4j
+  }
+  decode_q8_0_block(W[0], q0, &out[0]);
+  decode_q8_0_block(W[8] >> 16, q1, &out[4]);
+}
+
+// ------------------------------------------------- raw line loads -------------
+// Where line L (= row * K/64 + kb) of each format lives.
+struct WeightView {
+  const uint8_t* data;
+  const float* absmax;
+  const int8_t* absmax_q;
+  const float* absmax_scale;
+  int dq_group;
+  int fmt;
+};
+
+// Raw bytes of one line, kept in registers between load and decode so the
+// loads of the next line can be in flight while this one is decoded.
+struct RawLine {
+  uint32_t w[17];
+  float scale;  // NF4 absmax' (unused otherwise)
+};
+
+enum { FMT_BF16 = 0, FMT_NF4 = 1, FMT_Q8_0 = 2, FMT_Q4_0 = 3 };
+
+template <int FMT>
+__device__ __forceinline__ void load_line(const WeightView& v, int64_t line, RawLine& r) {
+  if constexpr (FMT == FMT_NF4) {
+    const uint4 a = ldg_nc_v4(v.data + line * 32);
+    const uint4 b = ldg_nc_v4(v.data + line * 32 + 16);
+    r.w[0] = a.x; r.w[1] = a.y; r.w[2] = a.z; r.w[3] = a.w;
+    r.w[4] = b.x; r.w[5] = b.y; r.w[6] = b.z; r.w[7] = b.w;
+    if (v.absmax != nullptr) {
+      r.scale = __ldg(v.absmax + line);
+    } else {
+      const float q = (float)__ldg(v.absmax_q + line);
+      r.scale = __fmul_rn(q, __ldg(v.absmax_scale + line / v.dq_group));
+    }
+  } else if constexpr (FMT == FMT_Q8_0) {
+    const uint8_t* p = v.data + line * 68;
+#pragma unroll
+    for (int i = 0; i < 17; ++i) r.w[i] = ldg_nc_u32(p + 4 * i);
+  } else if constexpr (FMT == FMT_Q4_0) {
+    const uint8_t* p = v.data + line * 36;
+#pragma unroll
+    for (int i = 0; i < 9; ++i) r.w[i] = ldg_nc_u32(p + 4 * i);
+  } else {  // BF16: 128 bytes
+    const uint4* p = reinterpret_cast<const uint4*>(v.data + line * 128);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 a = ldg_nc_v4(p + i);
+      r.w[4 * i] = a.x; r.w[4 * i + 1] = a.y; r.w[4 * i + 2] = a.z; r.w[4 * i + 3] = a.w;
+    }
+  }
+}
+
+// Only for the quantised formats.
+template <int FMT>
+__device__ __forceinline__ void decode_line(const RawLine& r, uint4 (&out)[8]) {
+  if constexpr (FMT == FMT_NF4) {
+    decode_nf4_line(make_uint4(r.w[0], r.w[1], r.w[2], r.w[3]), make_uint4(r.w[4], r.w[5], r.w[6], r.w[7]),
+                    r.scale, out);
+  } else if constexpr (FMT == FMT_Q8_0) {
+    uint32_t W[17];
+#pragma unroll
+    for (int i = 0; i < 17; ++i) W[i] = r.w[i];
+    decode_q8_0_line(W, out);
+  } else if constexpr (FMT == FMT_Q4_0) {
+    uint32_t W[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) W[i] = r.w[i];
+    decode_q4_0_line(W, out);
+  }
+}
+
+}  // namespace qlora

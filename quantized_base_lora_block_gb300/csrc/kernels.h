@@ -1,0 +1,97 @@
+// Internal interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "decode.cuh"
+
+namespace qlora {
+
+void count_launch(int n);
+int* device_error_word();  // address of the device error word on the current device
+
+// ---- skinny adapter contractions (skinny.cu) --------------------------------
+struct SplitPlan {
+  int splits;     // number of partial sums
+  int64_t chunk;  // reduction elements per split (multiple of 64)
+};
+
+// Target number of CTAs for the split reductions.  A fixed constant (not the
+// device's SM count) so workspace sizes and summation order do not depend on
+// the device.
+constexpr int kSplitTargetCtas = 608;
+
+inline SplitPlan plan_split(int64_t outer_tiles, int64_t red_len) {
+  const int64_t red_tiles = (red_len + 63) / 64;
+  int64_t s = (kSplitTargetCtas + outer_tiles - 1) / (outer_tiles > 0 ? outer_tiles : 1);
+  if (s < 1) s = 1;
+  if (s > red_tiles) s = red_tiles;
+  if (s < 1) s = 1;
+  int64_t per = (red_tiles + s - 1) / s;
+  SplitPlan p;
+  p.chunk = per * 64;
+  p.splits = (int)((red_tiles + per - 1) / per);
+  if (p.splits < 1) p.splits = 1;
+  return p;
+}
+
+cudaError_t launch_row_reduce(const __nv_bfloat16* L, int64_t P, int64_t J, const __nv_bfloat16* S, int Q,
+                              bool s_qj, float* partial, const SplitPlan& sp, cudaStream_t st);
+cudaError_t launch_col_reduce(const __nv_bfloat16* L, int64_t P, int64_t J, const float* S, int Q,
+                              float* partial, const SplitPlan& sp, cudaStream_t st);
+cudaError_t launch_fin_rows(const float* partial, int splits, int64_t P, int Q, float scale, float* out_f32,
+                            __nv_bfloat16* out_scaled, cudaStream_t st);
+cudaError_t launch_fin_cols(const float* partial, int splits, int64_t J, int Q, float scale, float* out,
+                            bool transposed, cudaStream_t st);
+
+// ---- standalone decode (dequant.cu) -------------------------------------------
+cudaError_t launch_dequant(int fmt, const WeightView& wv, int64_t lines, __nv_bfloat16* out, cudaStream_t st);
+
+// ---- fused tcgen05 GEMM (gemm_tc.cu) --------------------------------------------
+// Tile: 128 output rows x 256 output columns, reduction in chunks of 64.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+
+// Grouped problems: up to kMaxGroups row groups (experts), each with its own
+// base weight.  Dense problems use one group.
+constexpr int kMaxGroups = 256;
+
+struct GroupTable {
+  WeightView w[kMaxGroups];
+};
+
+struct GemmArgs {
+  int M;                 // total rows (of X / dY / output)
+  int n_out;             // output columns (N forward, K for dX)
+  int k_red;             // reduction length (K forward, N for dX); multiple of 64
+  int rank;              // LoRA rank (0: no adapter chunk)
+  int num_n_blk;         // ceil(n_out / 256)
+  int num_tiles;         // total output tiles
+  int64_t w_lines_per_row;  // K_w / 64
+  int64_t w_rows;           // N_w
+  __nv_bfloat16* out;    // [M x n_out] bf16
+  // grouped schedule (device): tile -> (group, row0, rows); null for dense
+  const int4* tile_sched;   // x = group, y = row0, z = rows, w = n block
+  int num_groups;
+  const GroupTable* groups;  // device copy (grouped); dense uses wv below
+  WeightView wv;
+  int* err;              // device error word
+};
+
+// Tensor maps: A operand [M x k_red] (X or dY), bf16 W (format BF16 only),
+// adapter A-operand (sT / sU [M x r]), adapter B-operand (B [N x r] forward,
+// A [r x K] for dX).  Grouped bf16 / adapter maps are 3-D with the group
+// index outermost.
+struct GemmMaps {
+  CUtensorMap a, w, la, lb;
+};
+
+cudaError_t launch_qgemm(int fmt, bool dx, bool grouped, const GemmMaps& maps, const GemmArgs& args,
+                         int num_sms, cudaStream_t st);
+
+}  // namespace qlora

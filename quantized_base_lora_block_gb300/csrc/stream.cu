@@ -1,0 +1,145 @@
+// Layer streaming of a frozen base: pinned host memory -> a fixed pool of
+// device slots, copied one layer ahead on a dedicated copy stream, ordered
+// against the compute stream with events.
+//
+// Each slot carries the layer id it holds.  acquire() checks the id, so a
+// slot that was refilled with another layer is never read as the old one (a
+// stale buffer is an error, not a silent wrong answer).  A layer that is
+// still resident is not copied again (the backward pass starts on the layers
+// the forward pass ended with).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include "../../include/qlora.h"
+#include "kernels.h"
+
+namespace qlora {
+
+struct StreamPool {
+  int slots = 0;
+  size_t slot_bytes = 0;
+  uint8_t* dev = nullptr;
+  cudaStream_t copy = nullptr;
+  std::vector<cudaEvent_t> ready, freed;
+  std::vector<int> layer;     // layer held by the slot, -1 = none
+  std::vector<int> acquired;  // compute work holding the slot not yet released
+  std::vector<int> freed_valid;
+  std::vector<uint64_t> last_use;
+  uint64_t clock = 0;
+  std::mutex mu;
+};
+
+}  // namespace qlora
+
+using namespace qlora;
+
+extern "C" {
+
+int32_t qlora_stream_create(int32_t slots, size_t slot_bytes, void** handle) {
+  if (!handle || slots < 1 || slots > 64 || slot_bytes == 0) return QLORA_ERR_INVALID;
+  *handle = nullptr;
+  StreamPool* p = new StreamPool();
+  p->slots = slots;
+  p->slot_bytes = (slot_bytes + 255) & ~size_t(255);
+  if (cudaMalloc(&p->dev, p->slot_bytes * slots) != cudaSuccess) {
+    delete p;
+    return QLORA_ERR_CUDA;
+  }
+  if (cudaStreamCreateWithFlags(&p->copy, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaFree(p->dev);
+    delete p;
+    return QLORA_ERR_CUDA;
+  }
+  p->ready.resize(slots);
+  p->freed.resize(slots);
+  for (int i = 0; i < slots; ++i) {
+    cudaEventCreateWithFlags(&p->ready[i], cudaEventDisableTiming);
+    cudaEventCreateWithFlags(&p->freed[i], cudaEventDisableTiming);
+  }
+  p->layer.assign(slots, -1);
+  p->acquired.assign(slots, 0);
+  p->freed_valid.assign(slots, 0);
+  p->last_use.assign(slots, 0);
+  *handle = p;
+  return QLORA_OK;
+}
+
+int32_t qlora_stream_prefetch(void* handle, int32_t layer, const void* host_src, size_t bytes) {
+  StreamPool* p = static_cast<StreamPool*>(handle);
+  if (!p || !host_src || layer < 0) return QLORA_ERR_INVALID;
+  if (bytes == 0 || bytes > p->slot_bytes) return QLORA_ERR_INVALID;
+  std::lock_guard<std::mutex> g(p->mu);
+  for (int i = 0; i < p->slots; ++i)
+    if (p->layer[i] == layer) {  // already resident
+      p->last_use[i] = ++p->clock;
+      return QLORA_OK;
+    }
+  int victim = -1;
+  for (int i = 0; i < p->slots; ++i) {
+    if (p->acquired[i]) continue;
+    if (victim < 0 || p->last_use[i] < p->last_use[victim]) victim = i;
+  }
+  if (victim < 0) return QLORA_ERR_STATE;  // every slot is in use
+  if (p->freed_valid[victim] && cudaStreamWaitEvent(p->copy, p->freed[victim], 0) != cudaSuccess)
+    return QLORA_ERR_CUDA;
+  p->layer[victim] = -1;
+  if (cudaMemcpyAsync(p->dev + (size_t)victim * p->slot_bytes, host_src, bytes, cudaMemcpyHostToDevice, p->copy) !=
+      cudaSuccess)
+    return QLORA_ERR_CUDA;
+  if (cudaEventRecord(p->ready[victim], p->copy) != cudaSuccess) return QLORA_ERR_CUDA;
+  p->layer[victim] = layer;
+  p->last_use[victim] = ++p->clock;
+  return QLORA_OK;
+}
+
+int32_t qlora_stream_acquire(void* handle, int32_t layer, void* compute_stream, void** dev_ptr) {
+  StreamPool* p = static_cast<StreamPool*>(handle);
+  if (!p || !dev_ptr) return QLORA_ERR_INVALID;
+  std::lock_guard<std::mutex> g(p->mu);
+  for (int i = 0; i < p->slots; ++i) {
+    if (p->layer[i] != layer) continue;
+    if (cudaStreamWaitEvent(static_cast<cudaStream_t>(compute_stream), p->ready[i], 0) != cudaSuccess)
+      return QLORA_ERR_CUDA;
+    p->acquired[i] += 1;
+    p->last_use[i] = ++p->clock;
+    *dev_ptr = p->dev + (size_t)i * p->slot_bytes;
+    return QLORA_OK;
+  }
+  *dev_ptr = nullptr;
+  return QLORA_ERR_STATE;
+}
+
+int32_t qlora_stream_release(void* handle, int32_t layer, void* compute_stream) {
+  StreamPool* p = static_cast<StreamPool*>(handle);
+  if (!p) return QLORA_ERR_INVALID;
+  std::lock_guard<std::mutex> g(p->mu);
+  for (int i = 0; i < p->slots; ++i) {
+    if (p->layer[i] != layer || p->acquired[i] == 0) continue;
+    if (cudaEventRecord(p->freed[i], static_cast<cudaStream_t>(compute_stream)) != cudaSuccess)
+      return QLORA_ERR_CUDA;
+    p->freed_valid[i] = 1;
+    p->acquired[i] -= 1;
+    return QLORA_OK;
+  }
+  return QLORA_ERR_STATE;
+}
+
+int32_t qlora_stream_destroy(void* handle) {
+  StreamPool* p = static_cast<StreamPool*>(handle);
+  if (!p) return QLORA_ERR_INVALID;
+  cudaStreamSynchronize(p->copy);
+  for (int i = 0; i < p->slots; ++i) {
+    if (p->freed_valid[i]) cudaEventSynchronize(p->freed[i]);
+    cudaEventDestroy(p->ready[i]);
+    cudaEventDestroy(p->freed[i]);
+  }
+  cudaStreamDestroy(p->copy);
+  cudaFree(p->dev);
+  delete p;
+  return QLORA_OK;
+}
+
+}  // extern "C"
