@@ -131,6 +131,25 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
                          void* dX, float* dA, float* dB,
                          void* workspace, size_t ws_bytes, void* stream);
 
+/* Forward pass that allocates nothing, for callers that cannot allocate
+ * device memory (e.g. a plug-in that may only use the buffers its host
+ * application passes in, or a loop that must not call cudaMalloc because it
+ * can synchronise the device).  The paper has no counterpart to this call.
+ * Same arguments and results as qlora_linear_fwd, minus the workspace: the
+ * workspace is a fixed 16 MiB array kept in device memory by the library
+ * (qlora_noalloc_scratch_bytes()), reserved on every GPU that loads the
+ * library until the process exits.  Returns QLORA_ERR_WORKSPACE, launching
+ * nothing, when qlora_workspace_bytes(w, M, rank) exceeds that size.  The
+ * first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls on a device share the array: calls whose GPU work
+ * overlaps (e.g. on two unordered streams) race on it and may give wrong
+ * results.  No part of the array needs to start at zero. */
+int32_t qlora_linear_fwd_noalloc(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha,
+                                 const void* X, const void* A, const void* B,
+                                 void* Y, float* T_save, void* stream);
+size_t qlora_noalloc_scratch_bytes(void);
+
 /* ---- grouped (mixture-of-experts) variant -------------------------------
  * The same layer for E experts (bytechap GGUF blog: fast LoRA backward for
  * linear and MoE layers).  Rows of X / dY / Y / dX / T_save are sorted by

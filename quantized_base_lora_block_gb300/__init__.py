@@ -72,6 +72,8 @@ SIGNATURES = {
     "qlora_stream_destroy": (_I32, [_P]),
     "qlora_device_error": (_I32, [_I32]),
     "qlora_launch_count": (_I64, []),
+    "qlora_linear_fwd_noalloc": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P]),
+    "qlora_noalloc_scratch_bytes": (_SZ, []),
     "qlora_profile_gemm": (_I32, [_I32]),
     "qlora_profile_gemm_read": (_I32, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
                                        ctypes.POINTER(ctypes.c_double)]),
@@ -198,6 +200,24 @@ def linear_fwd(w: DeviceWeight, X, A, B, alpha: float, Y=None, T=None, workspace
     st = load().qlora_linear_fwd(ctypes.byref(w.desc), M, r, float(alpha), _ptr(X), _ptr(A), _ptr(B), _ptr(Y),
                                  _ptr(T), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
     _check("qlora_linear_fwd", st)
+    return Y, T
+
+
+def linear_fwd_noalloc(w: DeviceWeight, X, A, B, alpha: float, Y=None, T=None, stream=None):
+    """Forward pass without a workspace argument, for callers that cannot
+    allocate device memory: the library uses its own fixed device scratch
+    (qlora_noalloc_scratch_bytes() bytes, shared by every such call on the
+    device, so calls must not overlap on the GPU).  Y and T are still the
+    caller's buffers.  Returns (Y, T_save)."""
+    torch = _torch()
+    M, r = X.shape[0], A.shape[0]
+    if Y is None:
+        Y = torch.empty((M, w.N), dtype=torch.bfloat16, device=X.device)
+    if T is None:
+        T = torch.empty((M, r), dtype=torch.float32, device=X.device)
+    st = load().qlora_linear_fwd_noalloc(ctypes.byref(w.desc), M, r, float(alpha), _ptr(X), _ptr(A), _ptr(B),
+                                         _ptr(Y), _ptr(T), _stream_ptr(stream))
+    _check("qlora_linear_fwd_noalloc", st)
     return Y, T
 
 
