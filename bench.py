@@ -41,7 +41,7 @@ CPU_SAMPLE_ROWS = 64
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="llama31_8b_nf4dq", choices=sorted(syn.WORKLOADS))
@@ -64,7 +64,7 @@ def measured_peaks():
 # clocks during the timed region
 # ----------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -77,7 +77,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -88,6 +88,10 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def mark(self, which: str):
+        """Wall-clock bounds of the timed region (samples outside are dropped)."""
+        setattr(self, which, time.time())
 
     def stop(self):
         if self.proc is None:
@@ -101,9 +105,18 @@ class ClockSampler:
             self.thread.join(timeout=5)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        t0, t1 = getattr(self, "t0", None), getattr(self, "t1", None)
+        import datetime
+
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            if ts is not None and t0 is not None and t1 is not None and not (t0 - 0.05 <= ts <= t1 + 0.05):
                 continue
             try:
                 sm.append(float(parts[1]))
@@ -267,10 +280,13 @@ def main():
 
     # --------------------------------------------------------- timed region
     clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(1.0)  # let the sampler start before the timed region
     barrier(world)
     torch.cuda.synchronize()
     if clocks:
-        clocks.start()
+        clocks.mark("t0")
     q.profile_gemm(True)
     n0 = q.launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -279,6 +295,8 @@ def main():
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    if clocks:
+        clocks.mark("t1")
     launches = q.launch_count() - n0
     q.profile_gemm(False)
     barrier(world)

@@ -191,22 +191,65 @@ static cudaEvent_t prof_event() {
 }
 
 // Launch the fused GEMM, bracketed by events when instrumentation is on.
-static cudaError_t gemm_launch(int fmt, bool dx, bool grouped, const GemmMaps& maps, const GemmArgs& a,
+static cudaError_t gemm_dispatch(int fmt, bool dx, bool pair, const GemmMaps& maps, const GemmArgs& a,
+                                cudaStream_t st) {
+  return pair ? launch_qgemm_pair(fmt, dx, maps, a, st) : launch_qgemm(fmt, dx, false, maps, a, sm_count(), st);
+}
+
+static cudaError_t gemm_launch(int fmt, bool dx, bool pair, const GemmMaps& maps, const GemmArgs& a,
                                cudaStream_t st) {
   std::unique_lock<std::mutex> g(g_prof_mu);
   if (!g_prof_on) {
     g.unlock();
-    return launch_qgemm(fmt, dx, grouped, maps, a, sm_count(), st);
+    return gemm_dispatch(fmt, dx, pair, maps, a, st);
   }
   GemmRec r;
   r.a = prof_event();
   r.b = prof_event();
   r.flops = 2.0 * (double)a.M * (double)a.n_out * (double)(a.k_red + a.rank);
   cudaEventRecord(r.a, st);
-  cudaError_t e = launch_qgemm(fmt, dx, grouped, maps, a, sm_count(), st);
+  cudaError_t e = gemm_dispatch(fmt, dx, pair, maps, a, st);
   cudaEventRecord(r.b, st);
   g_prof_recs.push_back(r);
   return e;
+}
+
+// Dense fused GEMM: forward (dx = false) out = A_op W^T + la lb^T with
+// A_op = X [M x K], la = sT, lb = B [N x r]; dX (dx = true) out = A_op W +
+// la lb with A_op = dY [M x N], la = sU, lb = A [r x K].
+static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M, int rank, const void* a_op,
+                                  const void* la, const void* lb, void* out, cudaStream_t st) {
+  const int64_t N = w->N, K = w->K;
+  const bool pair = M > kBM;  // 256-row tiles on a CTA pair; short problems use one CTA per tile
+  const uint32_t brows = pair ? 128 : 256;
+  GemmMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  bool ok;
+  if (!dx) {
+    ok = map2d(&maps.a, a_op, K, M, 64, 128) && map2d(&maps.la, la, rank, M, 64, 128) &&
+         map2d(&maps.lb, lb, rank, N, 64, brows);
+    if (w->fmt == QLORA_FMT_BF16) ok = ok && map2d(&maps.w, w->data, K, N, 64, brows);
+  } else {
+    ok = map2d(&maps.a, a_op, N, M, 64, 128) && map2d(&maps.la, la, rank, M, 64, 128) &&
+         map2d(&maps.lb, lb, K, rank, 64, 64);
+    if (w->fmt == QLORA_FMT_BF16) ok = ok && map2d(&maps.w, w->data, K, N, 64, 64);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.M = (int)M;
+  a.n_out = (int)(dx ? K : N);
+  a.k_red = (int)(dx ? N : K);
+  a.rank = rank;
+  a.num_n_blk = (a.n_out + kBN - 1) / kBN;
+  const int64_t row_tile = pair ? 256 : kBM;
+  a.num_tiles = (int)(((M + row_tile - 1) / row_tile) * a.num_n_blk);
+  a.w_lines_per_row = K / 64;
+  a.w_rows = N;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.wv = view_of(w);
+  a.err = device_error_word();
+  return gemm_launch(w->fmt, dx, pair, maps, a, st);
 }
 
 }  // namespace qlora
@@ -322,26 +365,7 @@ int32_t qlora_linear_fwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
 
   // 2) Y = X deq(W)^T + sT B^T
-  GemmMaps maps;
-  std::memset(&maps, 0, sizeof(maps));
-  bool ok = map2d(&maps.a, X, K, M, 64, 128) && map2d(&maps.la, sT, rank, M, 64, 128) &&
-            map2d(&maps.lb, B, rank, N, 64, 256);
-  if (w->fmt == QLORA_FMT_BF16) ok = ok && map2d(&maps.w, w->data, K, N, 64, 256);
-  if (!ok) return QLORA_ERR_CUDA;
-  GemmArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.M = (int)M;
-  a.n_out = (int)N;
-  a.k_red = (int)K;
-  a.rank = rank;
-  a.num_n_blk = (int)((N + kBN - 1) / kBN);
-  a.num_tiles = (int)(((M + kBM - 1) / kBM) * a.num_n_blk);
-  a.w_lines_per_row = K / 64;
-  a.w_rows = N;
-  a.out = static_cast<__nv_bfloat16*>(Y);
-  a.wv = view_of(w);
-  a.err = device_error_word();
-  return cuda_status(gemm_launch(w->fmt, false, false, maps, a, st));
+  return cuda_status(run_dense_gemm(w, false, M, rank, X, sT, B, Y, st));
 }
 
 int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha, const void* X,
@@ -385,26 +409,7 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
 
   // 3) dX = dY deq(W) + sU A
   if (dX) {
-    GemmMaps maps;
-    std::memset(&maps, 0, sizeof(maps));
-    bool ok = map2d(&maps.a, dY, N, M, 64, 128) && map2d(&maps.la, sU, rank, M, 64, 128) &&
-              map2d(&maps.lb, A, K, rank, 64, 64);
-    if (w->fmt == QLORA_FMT_BF16) ok = ok && map2d(&maps.w, w->data, K, N, 64, 64);
-    if (!ok) return QLORA_ERR_CUDA;
-    GemmArgs a;
-    std::memset(&a, 0, sizeof(a));
-    a.M = (int)M;
-    a.n_out = (int)K;
-    a.k_red = (int)N;
-    a.rank = rank;
-    a.num_n_blk = (int)((K + kBN - 1) / kBN);
-    a.num_tiles = (int)(((M + kBM - 1) / kBM) * a.num_n_blk);
-    a.w_lines_per_row = K / 64;
-    a.w_rows = N;
-    a.out = static_cast<__nv_bfloat16*>(dX);
-    a.wv = view_of(w);
-    a.err = device_error_word();
-    e = gemm_launch(w->fmt, true, false, maps, a, st);
+    e = run_dense_gemm(w, true, M, rank, dY, sU, A, dX, st);
     if (e != cudaSuccess) return QLORA_ERR_CUDA;
   }
 

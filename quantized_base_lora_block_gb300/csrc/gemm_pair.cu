@@ -1,0 +1,367 @@
+// Fused quantised-base LoRA GEMM on a CTA pair (tcgen05 cta_group::2).
+//
+// Same operation as gemm_tc.cu (forward Y = X deq(W)^T + sT B^T, or
+// dX = dY deq(W) + sU A), with a 256 x 256 output tile per pair of SMs:
+//   - CTA r of the pair loads rows [m0 + 128 r, +128) of the A operand and
+//     decodes (or loads) its half of the B operand: output columns
+//     [n0 + 128 r, +128);
+//   - one thread of CTA 0 issues tcgen05.mma.cta_group::2 (M 256, N 256,
+//     K 16); the tensor cores of both SMs read their own halves and each
+//     SM's TMEM receives its 128 rows x 256 fp32 columns;
+//   - the MMA's completion is multicast to both CTAs' "stage empty" and
+//     "accumulator full" barriers.
+// Each decoded weight therefore feeds 256 output rows instead of 128, and
+// each SM reads only half of the B tile from its shared memory.
+//
+// Synchronisation across the pair: both CTAs' TMA copies (2-CTA form) land in
+// their own shared memory and complete their bytes on CTA 0's "stage full"
+// barrier, whose expected byte count covers both CTAs.  (Relaying CTA 1's
+// completion through a thread of CTA 1 instead cost 2.4x in throughput.)
+// Decode warps and epilogue warps of both CTAs arrive on CTA 0's "B ready" /
+// "accumulator empty" barriers with cluster-scope release.  All waits are
+// bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace qlora {
+
+namespace {
+
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = 128 * kBK * 2;  // this CTA's 128 A rows x 64
+constexpr int P_B_BYTES = 128 * kBK * 2;  // this CTA's half of B: 128 x 64
+constexpr int P_DQ_WARPS = 8;             // two groups of 4, alternating stages
+constexpr int P_TMEM_COLS = 512;
+
+struct __align__(8) PairBarriers {
+  uint64_t full[P_STAGES];    // CTA 0: bytes of both CTAs' copies (CTA 1: unused)
+  uint64_t bready[P_STAGES];  // CTA 0: decode warps of both CTAs
+  uint64_t empty[P_STAGES];   // both: MMA completion (multicast)
+  uint64_t acc_full[2];       // both: MMA completion (multicast)
+  uint64_t acc_empty[2];      // CTA 0: epilogue warps of both CTAs
+  uint32_t tmem_base;
+  int abort;
+};
+
+constexpr size_t P_SMEM_BYTES = 1024 + (size_t)P_STAGES * (P_A_BYTES + P_B_BYTES) + sizeof(PairBarriers);
+
+template <int FMT>
+constexpr int p_threads() {
+  return (FMT == FMT_BF16) ? 6 * 32 : (6 + P_DQ_WARPS) * 32;
+}
+
+struct PairTile {
+  int m0, n0;
+};
+
+// forward: row blocks fastest (the activation block stays in L2 while the
+// weight slab streams); dX: column blocks fastest (the dY row block stays in
+// L2 while every output column block of it runs).
+template <bool DX>
+__device__ __forceinline__ PairTile pair_tile(const GemmArgs& a, int t) {
+  const int num_m = (a.M + 255) / 256;
+  const int num_n = a.num_n_blk;
+  PairTile p;
+  if (!DX) {
+    p.m0 = (t % num_m) * 256;
+    p.n0 = (t / num_m) * kBN;
+  } else {
+    p.n0 = (t % num_n) * kBN;
+    p.m0 = (t / num_n) * 256;
+  }
+  return p;
+}
+
+}  // namespace
+
+template <int FMT, bool DX>
+__global__ void __launch_bounds__(p_threads<FMT>(), 1)
+    qgemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
+                      const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_lb,
+                      const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sA0 = smem_u32(smem);
+  const uint32_t sB0 = sA0 + P_STAGES * P_A_BYTES;
+  PairBarriers* bars = reinterpret_cast<PairBarriers*>(smem + P_STAGES * (P_A_BYTES + P_B_BYTES));
+  volatile int* abort = &bars->abort;
+
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool has_lora = args.rank > 0;
+  const int nkb = args.k_red / kBK;
+  const int nkb_total = nkb + (has_lora ? 1 : 0);
+  const int my_tiles = pair < args.num_tiles ? (args.num_tiles - pair + num_pairs - 1) / num_pairs : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(smem_u32(&bars->full[s]), 1);
+      mbar_init(smem_u32(&bars->bready[s]), 2 * (P_DQ_WARPS / 2));
+      mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&bars->acc_full[b]), 1);
+      mbar_init(smem_u32(&bars->acc_empty[b]), 8);
+    }
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc_pair(smem_u32(&bars->tmem_base), P_TMEM_COLS);
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_a);
+    if (FMT == FMT_BF16) prefetch_tmap(&tm_w);
+    if (has_lora) {
+      prefetch_tmap(&tm_la);
+      prefetch_tmap(&tm_lb);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // peer barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      for (int lt = 0; lt < my_tiles; ++lt) {
+        const PairTile tc = pair_tile<DX>(args, pair + lt * num_pairs);
+        const int am = tc.m0 + 128 * (int)rank;  // this CTA's A rows
+        const int bn = tc.n0 + 128 * (int)rank;  // this CTA's half of B
+        for (int kb = 0; kb < nkb_total; ++kb, ++it) {
+          const int s = it % P_STAGES;
+          const uint32_t ph = (it / P_STAGES) & 1;
+          if (!mbar_wait_cluster(smem_u32(&bars->empty[s]), ph ^ 1, abort, args.err)) goto producer_done;
+          const bool lora = kb == nkb;
+          const uint32_t sa = sA0 + s * P_A_BYTES, sb = sB0 + s * P_B_BYTES;
+          const uint32_t bytes = P_A_BYTES + ((FMT == FMT_BF16 || lora) ? P_B_BYTES : 0);
+          // CTA 0 expects both CTAs' bytes; every copy completes on CTA 0's barrier
+          if (rank == 0) mbar_arrive_expect_tx(smem_u32(&bars->full[s]), 2 * bytes);
+          const uint32_t fb = mapa_shared(smem_u32(&bars->full[s]), 0);
+          if (!lora) {
+            tma_load_2d_pair(sa, &tm_a, fb, kb * kBK, am);
+            if (FMT == FMT_BF16) {
+              if (!DX) {
+                tma_load_2d_pair(sb, &tm_w, fb, kb * kBK, bn);
+              } else {
+                tma_load_2d_pair(sb, &tm_w, fb, bn, kb * kBK);
+                tma_load_2d_pair(sb + 8192, &tm_w, fb, bn + 64, kb * kBK);
+              }
+            }
+          } else {
+            tma_load_2d_pair(sa, &tm_la, fb, 0, am);
+            if (!DX) {
+              tma_load_2d_pair(sb, &tm_lb, fb, 0, bn);
+            } else {
+              tma_load_2d_pair(sb, &tm_lb, fb, bn, 0);
+              tma_load_2d_pair(sb + 8192, &tm_lb, fb, bn + 64, 0);
+            }
+          }
+        }
+      }
+    producer_done:
+      // CTA 0 waits for the last copies of every stage; CTA 1's copies complete
+      // on those same barriers
+      if (rank == 0)
+        for (uint32_t k = (it >= P_STAGES ? it - P_STAGES : 0); k < it; ++k)
+          mbar_drain(smem_u32(&bars->full[k % P_STAGES]), (k / P_STAGES) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(256, kBN, DX);
+      uint32_t it = 0;
+      for (int lt = 0; lt < my_tiles; ++lt) {
+        const uint32_t ab = lt & 1, aph = (lt >> 1) & 1;
+        if (!mbar_wait_cluster(smem_u32(&bars->acc_empty[ab]), aph ^ 1, abort, args.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + ab * kBN;
+        bool ok = true;
+        for (int kb = 0; kb < nkb_total; ++kb, ++it) {
+          const int s = it % P_STAGES;
+          const uint32_t ph = (it / P_STAGES) & 1;
+          if (!mbar_wait_cluster(smem_u32(&bars->full[s]), ph, abort, args.err)) { ok = false; break; }
+          if (FMT != FMT_BF16) {
+            if (!mbar_wait_cluster(smem_u32(&bars->bready[s]), ph, abort, args.err)) { ok = false; break; }
+          }
+          // operands arrive through mbarriers (TMA complete_tx, or decode
+          // warps' proxy fence + release arrive): no tcgen05 fence is needed
+          // here, and none is issued so consecutive stages' MMAs overlap
+          const bool lora = kb == nkb;
+          const int nk = lora ? (args.rank + 15) / 16 : kBK / 16;
+          const uint32_t sa = sA0 + s * P_A_BYTES, sb = sB0 + s * P_B_BYTES;
+          for (int kk = 0; kk < nk; ++kk) {
+            const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bdesc = DX ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
+                                      : smem_desc_sw128(sb + kk * 32, 16, 1024);
+            tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit_pair_mc(smem_u32(&bars->empty[s]));
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(smem_u32(&bars->acc_full[ab]));
+      }
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    for (int lt = 0; lt < my_tiles; ++lt) {
+      const PairTile tc = pair_tile<DX>(args, pair + lt * num_pairs);
+      const uint32_t ab = lt & 1, aph = (lt >> 1) & 1;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_cluster(smem_u32(&bars->acc_full[ab]), aph, abort, args.err);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const int row = tc.m0 + 128 * (int)rank + row_in_tile;
+      const bool row_ok = row < args.M;
+      __nv_bfloat16* orow = args.out + (int64_t)row * args.n_out + tc.n0;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kBN + c * 32, v);
+        tc_wait_ld();
+        if (row_ok && tc.n0 + c * 32 < args.n_out) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+            o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+            o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+            o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+            dst[q] = o;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[ab]), 0));
+    }
+  } else if (FMT != FMT_BF16) {
+    // ------------------------------------------------------------ decode
+    // group g (4 warps) handles the stages with it % 2 == g; thread d of the
+    // group decodes one 64-element line of this CTA's half of B per item.
+    const int g = (warp - 6) >> 2;
+    const int d = ((warp - 6) & 3) * 32 + lane;  // 0..127
+    const int srow = DX ? (d & 63) : d;
+    const uint32_t soff = DX ? (uint32_t)((d >> 6) * 8192 + srow * 128) : (uint32_t)(srow * 128);
+    const int swz = srow & 7;
+    const uint32_t total = (uint32_t)my_tiles * (uint32_t)nkb_total;
+    const uint32_t bready0 = mapa_shared(smem_u32(&bars->bready[0]), 0);
+
+    auto line_of = [&](uint32_t it, bool& valid) -> int64_t {
+      const int lt = (int)(it / (uint32_t)nkb_total), kb = (int)(it % (uint32_t)nkb_total);
+      valid = false;
+      if (kb >= nkb) return 0;  // adapter chunk: nothing to decode
+      const PairTile tc = pair_tile<DX>(args, pair + lt * num_pairs);
+      int64_t row, kl;
+      if (!DX) {
+        row = tc.n0 + 128 * (int)rank + d;
+        kl = kb;
+      } else {
+        row = (int64_t)kb * kBK + (d & 63);
+        kl = (tc.n0 + 128 * (int)rank) / 64 + (d >> 6);
+      }
+      valid = row < args.w_rows && kl < args.w_lines_per_row;
+      return row * args.w_lines_per_row + kl;
+    };
+
+    RawLine cur;
+    bool cur_valid = false;
+    if ((uint32_t)g < total) {
+      const int64_t ln = line_of((uint32_t)g, cur_valid);
+      if (cur_valid) load_line<FMT>(args.wv, ln, cur);
+    }
+    for (uint32_t it = (uint32_t)g; it < total; it += 2) {
+      RawLine nxt;
+      bool nxt_valid = false;
+      if (it + 2 < total) {
+        const int64_t ln = line_of(it + 2, nxt_valid);
+        if (nxt_valid) load_line<FMT>(args.wv, ln, nxt);
+      }
+      const int s = it % P_STAGES;
+      const uint32_t ph = (it / P_STAGES) & 1;
+      if (!mbar_wait_cluster(smem_u32(&bars->empty[s]), ph ^ 1, abort, args.err)) break;
+      const bool decode_item = (int)(it % (uint32_t)nkb_total) < nkb;
+      if (decode_item) {
+        const uint32_t dst = sB0 + s * P_B_BYTES + soff;
+        if (cur_valid) {
+          uint4 out[8];
+          decode_line<FMT>(cur, out);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) sts_v4(dst + ((c ^ swz) << 4), out[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) sts_v4(dst + (c << 4), make_uint4(0, 0, 0, 0));
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(bready0 + s * 8);
+      cur = nxt;
+      cur_valid = nxt_valid;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while its peer may still signal it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, P_TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+template <int FMT, bool DX>
+static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, cudaStream_t st) {
+  auto kern = qgemm_pair_kernel<FMT, DX>;
+  static int max_clusters = -1;  // per instantiation
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(p_threads<FMT>());
+  cfg.dynamicSmemBytes = P_SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_clusters < 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters = n > 0 ? n : 1;
+  }
+  const int pairs = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
+  if (pairs <= 0) return cudaSuccess;
+  cfg.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&cfg, kern, maps.a, maps.w, maps.la, maps.lb, args);
+}
+
+cudaError_t launch_qgemm_pair(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args, cudaStream_t st) {
+  count_launch(1);
+  switch (fmt) {
+    case FMT_BF16: return dx ? launch_pair_one<FMT_BF16, true>(maps, args, st) : launch_pair_one<FMT_BF16, false>(maps, args, st);
+    case FMT_NF4: return dx ? launch_pair_one<FMT_NF4, true>(maps, args, st) : launch_pair_one<FMT_NF4, false>(maps, args, st);
+    case FMT_Q8_0: return dx ? launch_pair_one<FMT_Q8_0, true>(maps, args, st) : launch_pair_one<FMT_Q8_0, false>(maps, args, st);
+    case FMT_Q4_0: return dx ? launch_pair_one<FMT_Q4_0, true>(maps, args, st) : launch_pair_one<FMT_Q4_0, false>(maps, args, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace qlora

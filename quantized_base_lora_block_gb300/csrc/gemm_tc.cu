@@ -198,7 +198,9 @@ __global__ void __launch_bounds__(num_threads<FMT>(), 1)
           if (FMT != FMT_BF16) {
             if (!mbar_wait(smem_u32(&bars->bready[s]), ph, abort, args.err)) { ok = false; break; }
           }
-          tc_fence_after();
+          // operands arrive through mbarriers (TMA complete_tx, or decode
+          // warps' proxy fence + release arrive): no tcgen05 fence is needed
+          // here, and none is issued so consecutive stages' MMAs overlap
           const bool lora = kb == nkb;
           const int nk = lora ? (args.rank + 15) / 16 : kBK / 16;
           const uint32_t sa = sA0 + s * A_BYTES, sb = sB0 + s * B_BYTES;

@@ -94,4 +94,9 @@ struct GemmMaps {
 cudaError_t launch_qgemm(int fmt, bool dx, bool grouped, const GemmMaps& maps, const GemmArgs& args,
                          int num_sms, cudaStream_t st);
 
+// CTA-pair variant (gemm_pair.cu): 256 x 256 tiles, dense problems only.
+// Tensor-map boxes: A / adapter-A [64 x 128]; bf16 W and adapter-B
+// [64 x 128] forward, [64 x 64] for dX.  args.num_tiles counts 256-row tiles.
+cudaError_t launch_qgemm_pair(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args, cudaStream_t st);
+
 }  // namespace qlora
