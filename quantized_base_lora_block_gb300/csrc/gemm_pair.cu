@@ -36,7 +36,9 @@ namespace {
 constexpr int P_STAGES = 6;
 constexpr int P_A_BYTES = 128 * kBK * 2;  // this CTA's 128 A rows x 64
 constexpr int P_B_BYTES = 128 * kBK * 2;  // this CTA's half of B: 128 x 64
-constexpr int P_DQ_WARPS = 8;             // two groups of 4, alternating stages
+constexpr int P_DQ_GROUPS = 3;            // groups of 4 decode warps, rotating over stages
+constexpr int P_DQ_WARPS = 4 * P_DQ_GROUPS;
+static_assert(P_STAGES % P_DQ_GROUPS == 0, "a stage must always be decoded by the same group");
 constexpr int P_TMEM_COLS = 512;
 
 struct __align__(8) PairBarriers {
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < P_STAGES; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
-      mbar_init(smem_u32(&bars->bready[s]), 2 * (P_DQ_WARPS / 2));
+      mbar_init(smem_u32(&bars->bready[s]), 2 * 4);  // 4 warps of one group, both CTAs
       mbar_init(smem_u32(&bars->empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -249,8 +251,9 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
     }
   } else if (FMT != FMT_BF16) {
     // ------------------------------------------------------------ decode
-    // group g (4 warps) handles the stages with it % 2 == g; thread d of the
-    // group decodes one 64-element line of this CTA's half of B per item.
+    // group g (4 warps) handles the items with it % P_DQ_GROUPS == g; thread
+    // d of the group decodes one 64-element line of this CTA's half of B per
+    // item, with the next item's bytes loaded while it decodes this one.
     const int g = (warp - 6) >> 2;
     const int d = ((warp - 6) & 3) * 32 + lane;  // 0..127
     const int srow = DX ? (d & 63) : d;
@@ -282,16 +285,18 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
       const int64_t ln = line_of((uint32_t)g, cur_valid);
       if (cur_valid) load_line<FMT>(args.wv, ln, cur);
     }
-    for (uint32_t it = (uint32_t)g; it < total; it += 2) {
+    for (uint32_t it = (uint32_t)g; it < total; it += P_DQ_GROUPS) {
       RawLine nxt;
       bool nxt_valid = false;
-      if (it + 2 < total) {
-        const int64_t ln = line_of(it + 2, nxt_valid);
+      if (it + P_DQ_GROUPS < total) {
+        const int64_t ln = line_of(it + P_DQ_GROUPS, nxt_valid);
         if (nxt_valid) load_line<FMT>(args.wv, ln, nxt);
       }
       const int s = it % P_STAGES;
       const uint32_t ph = (it / P_STAGES) & 1;
-      if (!mbar_wait_cluster(smem_u32(&bars->empty[s]), ph ^ 1, abort, args.err)) break;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_cluster(smem_u32(&bars->empty[s]), ph ^ 1, abort, args.err);
+      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
       const bool decode_item = (int)(it % (uint32_t)nkb_total) < nkb;
       if (decode_item) {
         const uint32_t dst = sB0 + s * P_B_BYTES + soff;
