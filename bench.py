@@ -47,6 +47,9 @@ def parse_args():
     p.add_argument("--workload", default="llama31_8b_nf4dq", choices=sorted(syn.WORKLOADS))
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--stream-layers", type=int, default=32,
+                   help="layers for the streamed leg (0 = skip); Llama workload only")
+    p.add_argument("--no-moe", action="store_true", help="skip the grouped MoE leg")
     return p.parse_args()
 
 
@@ -197,6 +200,111 @@ def time_oracle(inputs, rows: int, reps: int = 1) -> float:
 
 
 # ----------------------------------------------------------------------------
+# streamed leg: L layers of the same shapes, bases in pinned host memory,
+# one layer per pool slot, prefetched one layer ahead
+# ----------------------------------------------------------------------------
+def stream_leg(q, torch, inputs, L_dev, wl, n_layers, steps, stream, resident_ms_per_layer):
+    blobs = [q.pack_weight_blob(inp["W"]) for inp in inputs]
+    offs, o = [], 0
+    for b, _ in blobs:
+        offs.append(o)
+        o = (o + b.nbytes + 255) // 256 * 256
+    layer_bytes = o
+    one = np.zeros(layer_bytes, dtype=np.uint8)
+    for (b, _), off in zip(blobs, offs):
+        one[off:off + b.nbytes] = b
+    src = torch.from_numpy(one)
+    hosts = []
+    for _ in range(n_layers):
+        h = torch.empty(layer_bytes, dtype=torch.uint8).pin_memory()
+        h.copy_(src)
+        hosts.append(h)
+    pool = q.LayerStream(2, layer_bytes)
+    M, r, alpha = wl.M, wl.rank, wl.alpha
+
+    def views(base):
+        return [q.weight_in_slot(inp["W"], bo, base + off) for inp, (_, bo), off in zip(inputs, blobs, offs)]
+
+    def one_pass():
+        pool.prefetch(0, hosts[0])
+        for i in range(n_layers):
+            if i + 1 < n_layers:
+                pool.prefetch(i + 1, hosts[i + 1])
+            ws = views(pool.acquire(i, stream))
+            for d, w in zip(L_dev, ws):
+                q.linear_fwd(w, d["X"], d["A"], d["B"], alpha, Y=d["Y"], T=d["T"], workspace=d["ws"], stream=stream)
+            pool.release(i, stream)
+        for i in reversed(range(n_layers)):
+            pool.prefetch(i, hosts[i])
+            if i > 0:
+                pool.prefetch(i - 1, hosts[i - 1])
+            ws = views(pool.acquire(i, stream))
+            for d, w in zip(reversed(L_dev), reversed(ws)):
+                q.linear_bwd(w, d["X"], d["A"], d["B"], d["T"], d["dY"], alpha, dX=d["dX"], dA=d["dA"], dB=d["dB"],
+                             workspace=d["ws"], stream=stream)
+            pool.release(i, stream)
+
+    one_pass()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one_pass()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    pool.close()
+    # every layer is copied for the forward pass and again for the backward
+    # pass, except the two the forward pass leaves resident
+    h2d = (2 * n_layers - 2) * layer_bytes
+    return {"layers": n_layers, "slots": 2, "layer_bytes": layer_bytes, "ms_per_pass": ms,
+            "value": M / (ms / n_layers / 1e3), "unit": "tokens/s per layer (fwd+bwd)",
+            "h2d_bytes_per_pass": h2d, "h2d_GBps": h2d / (ms / 1e3) / 1e9,
+            "streamed_over_resident": ms / (n_layers * resident_ms_per_layer),
+            "note": "pinned host -> 2-slot device pool, one layer ahead on the library's copy stream; "
+                    "fwd 0..L-1 then bwd L-1..0; each layer's 7 bases in one blob"}
+
+
+def moe_leg(q, torch, steps, stream):
+    mw = syn.MOE
+    off, _, counts = syn.moe_routing(seed=0)
+    lins = syn.moe_linears(mw)
+    data = [syn.make_moe_linear_inputs(mw, i, off, seed=0) for i in range(len(lins))]
+    dev = []
+    for d in data:
+        ws = [q.DeviceWeight.from_packed(w) for w in d["W"]]
+        X, dY = q.bf16_from_bits(d["X"]), q.bf16_from_bits(d["dY"])
+        A, B = q.bf16_from_bits(d["A"]), q.bf16_from_bits(d["B"])
+        nb = q.grouped_workspace_bytes(ws, off, mw.rank)
+        dev.append({"W": ws, "X": X, "dY": dY, "A": A, "B": B, "alpha": d["alpha"], "ws": q.alloc_workspace(nb)})
+
+    def step():
+        Ts = []
+        for d in dev:
+            _, T = q.grouped_fwd(d["W"], off, d["X"], d["A"], d["B"], d["alpha"], workspace=d["ws"], stream=stream)
+            Ts.append(T)
+        for d, T in zip(reversed(dev), reversed(Ts)):
+            q.grouped_bwd(d["W"], off, d["X"], d["A"], d["B"], T, d["dY"], d["alpha"], workspace=d["ws"],
+                          stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    rows = int(off[-1])
+    flops = sum(syn.linear_flops(rows, l.K, l.N, mw.rank) for l in lins)
+    return {"workload": "moe_q8_0: 128 experts, top-8 of 4096 tokens (32768 rows, Zipf-skewed, "
+                        f"{int((counts == 0).sum())} experts empty), gate/up 2048->768, down 768->2048, rank 16",
+            "ms_per_step": ms, "tokens_per_s": mw.tokens / (ms / 1e3), "rows_per_s": rows / (ms / 1e3),
+            "tflops": flops / (ms / 1e3) / 1e12}
+
+
 def make_inputs(wl):
     return [syn.make_linear_inputs(wl, i, seed=0) for i in range(len(wl.linears))]
 
@@ -264,6 +372,8 @@ def main():
         ws_bytes = max(ws_bytes, q.workspace_bytes(w, M, r))
         L.append(d)
     ws = q.alloc_workspace(ws_bytes, dev)
+    for d in L:
+        d["ws"] = ws
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -353,6 +463,14 @@ def main():
                "d2h_bytes_per_step": d2h,
                "note": "pinned host X and dY copied in, dA and dB copied out, every step, same stream"}
 
+    # --------------------------------------------------------- other legs
+    stream_res = None
+    if args.stream_layers > 0 and wl.name == "llama31_8b_nf4dq":
+        stream_res = stream_leg(q, torch, inputs, L, wl, args.stream_layers, 2, stream, ms_max / args.steps)
+    moe_res = None
+    if not args.no_moe and rank == 0:
+        moe_res = moe_leg(q, torch, 10, stream)
+
     # --------------------------------------------------------- CPU oracle
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -372,7 +490,7 @@ def main():
             "frac_of_nominal_2250": flops_step / t_step / 1e12 / NOMINAL_BF16_TFLOPS,
             "frac_of_measured_sustained": flops_step / t_step / 1e12 / peaks["bf16_sustained"],
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk,
+            "clocks": clk, "stream": stream_res, "moe": moe_res,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -183,11 +183,14 @@ int32_t grouped_moe_qlora_bwd(const qlora_weight_desc* experts, int32_t E,
  *
  * qlora_stream_create: allocates `slots` device buffers of `slot_bytes` each
  *   (the only memory this library allocates), a copy stream and events.
- * qlora_stream_prefetch: enqueue the host->device copy of `bytes` bytes at
- *   `host_src` (pinned host memory, must stay valid until the copy ran) into
- *   the next slot in round-robin order, tagged with `layer`.  The copy waits
- *   until every earlier compute-stream use of that slot was released.
- *   Returns QLORA_ERR_STATE if that slot is still acquired.
+ * qlora_stream_prefetch: announce that `layer` is needed next.  If it is
+ *   still resident nothing is copied; otherwise enqueue the host->device copy
+ *   of `bytes` bytes at `host_src` (pinned host memory, valid until the copy
+ *   ran) into the least recently used slot that is neither acquired nor
+ *   holding an announced, not yet acquired layer, tagged with `layer`.  The
+ *   copy waits until every earlier compute-stream use of that slot was
+ *   released.  QLORA_ERR_STATE if no slot is free (prefetching too far ahead),
+ *   QLORA_ERR_INVALID if `bytes` exceeds the slot size.
  * qlora_stream_acquire: make `compute_stream` wait for the copy of `layer`
  *   and return the slot's device address in *dev_ptr.  QLORA_ERR_STATE if no
  *   slot holds `layer` (never prefetched, or already overwritten).

@@ -159,6 +159,18 @@ class DeviceWeight:
                 absmax_scale = torch.from_numpy(np.ascontiguousarray(p["absmax_scale"], np.float32)).to(device)
         return cls(p["fmt"], p["N"], p["K"], data, absmax, absmax_q, absmax_scale, p.get("dq_group", 0))
 
+    @classmethod
+    def from_pointers(cls, fmt: str, N: int, K: int, data: int, absmax: int = 0, absmax_q: int = 0,
+                      absmax_scale: int = 0, dq_group: int = 0, keepalive=None) -> "DeviceWeight":
+        """Descriptor over raw device addresses (e.g. a streaming-pool slot)."""
+        self = cls.__new__(cls)
+        self.fmt, self.N, self.K = fmt, int(N), int(K)
+        self.data = self.absmax = self.absmax_q = self.absmax_scale = None
+        self._keepalive = keepalive
+        self.desc = WeightDesc(FMT[fmt], int(dq_group), self.N, self.K, data or None, absmax or None,
+                               absmax_q or None, absmax_scale or None)
+        return self
+
     def nbytes(self) -> int:
         n = 0
         for t in (self.data, self.absmax, self.absmax_q, self.absmax_scale):
@@ -241,6 +253,77 @@ def linear_bwd(w: DeviceWeight, X, A, B, T, dY, alpha: float, dX=None, dA=None, 
     return dX, dA, dB
 
 
+# ---------------------------------------------------------------------------
+# grouped (mixture-of-experts)
+# ---------------------------------------------------------------------------
+def _grouped_args(weights: Sequence[DeviceWeight], offsets):
+    E = len(weights)
+    descs = (WeightDesc * E)(*[w.desc for w in weights])
+    off = np.ascontiguousarray(offsets, dtype=np.int32)
+    assert off.size == E + 1
+    off_c = (ctypes.c_int32 * (E + 1))(*off.tolist())
+    return E, descs, off_c, int(off[-1])
+
+
+def grouped_workspace_bytes(weights: Sequence[DeviceWeight], offsets, rank: int) -> int:
+    E, descs, off_c, _ = _grouped_args(weights, offsets)
+    return int(load().qlora_grouped_workspace_bytes(descs, E, off_c, int(rank)))
+
+
+def grouped_fwd(weights: Sequence[DeviceWeight], offsets, X, A, B, alpha: float, Y=None, T=None, workspace=None,
+                stream=None):
+    """Rows of X sorted by expert; A [E, r, K], B [E, N, r].  Returns (Y, T_save)."""
+    torch = _torch()
+    E, descs, off_c, M = _grouped_args(weights, offsets)
+    r, N = A.shape[1], weights[0].N
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    if T is None:
+        T = torch.empty((M, r), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(grouped_workspace_bytes(weights, offsets, r), X.device)
+    st = load().grouped_moe_qlora_fwd(descs, E, off_c, r, float(alpha), _ptr(X), _ptr(A), _ptr(B), _ptr(Y), _ptr(T),
+                                      _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check("grouped_moe_qlora_fwd", st)
+    return Y, T
+
+
+def grouped_bwd(weights: Sequence[DeviceWeight], offsets, X, A, B, T, dY, alpha: float, dX=None, dA=None, dB=None,
+                workspace=None, stream=None, want_dx: bool = True):
+    """Returns (dX, dA [E, r, K], dB [E, N, r])."""
+    torch = _torch()
+    E, descs, off_c, M = _grouped_args(weights, offsets)
+    r, N, K = A.shape[1], weights[0].N, weights[0].K
+    if dX is None and want_dx:
+        dX = torch.empty((M, K), dtype=torch.bfloat16, device=X.device)
+    if dA is None:
+        dA = torch.empty((E, r, K), dtype=torch.float32, device=X.device)
+    if dB is None:
+        dB = torch.empty((E, N, r), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(grouped_workspace_bytes(weights, offsets, r), X.device)
+    st = load().grouped_moe_qlora_bwd(descs, E, off_c, r, float(alpha), _ptr(X), _ptr(A), _ptr(B), _ptr(T), _ptr(dY),
+                                      _ptr(dX), _ptr(dA), _ptr(dB), _ptr(workspace), workspace.numel(),
+                                      _stream_ptr(stream))
+    _check("grouped_moe_qlora_bwd", st)
+    return dX, dA, dB
+
+
+def stack_bf16_weights(weights: Sequence[Dict], device="cuda") -> List[DeviceWeight]:
+    """bf16 expert bases must live in one [E][N][K] array (grouped calls read
+    them through one 3-D tensor map); returns per-expert views of it."""
+    torch = _torch()
+    E = len(weights)
+    N, K = weights[0]["N"], weights[0]["K"]
+    big = torch.from_numpy(np.stack([np.asarray(w["data"], np.uint16).reshape(N, K) for w in weights])
+                           .view(np.int16)).to(device)
+    out = []
+    for e in range(E):
+        out.append(DeviceWeight("bf16", N, K, big[e]))
+    out[0]._stack = big
+    return out
+
+
 def device_error(clear: bool = True) -> int:
     return int(load().qlora_device_error(1 if clear else 0))
 
@@ -264,6 +347,28 @@ def profile_gemm_read() -> Tuple[float, int, float]:
 # ---------------------------------------------------------------------------
 # layer streaming
 # ---------------------------------------------------------------------------
+def pack_weight_blob(p: Dict) -> Tuple[np.ndarray, Dict[str, int]]:
+    """One contiguous byte blob per packed base weight (sections 256-byte
+    aligned): the unit the streaming pool copies.  Returns (blob, offsets)."""
+    parts = [("data", np.ascontiguousarray(p["data"]).view(np.uint8).reshape(-1))]
+    for k in ("absmax", "absmax_q", "absmax_scale"):
+        if k in p and p[k] is not None:
+            parts.append((k, np.ascontiguousarray(p[k]).view(np.uint8).reshape(-1)))
+    offs, o = {}, 0
+    for k, a in parts:
+        offs[k] = o
+        o = (o + a.nbytes + 255) // 256 * 256
+    blob = np.zeros(o, dtype=np.uint8)
+    for k, a in parts:
+        blob[offs[k]:offs[k] + a.nbytes] = a
+    return blob, offs
+
+
+def weight_in_slot(p: Dict, offs: Dict[str, int], base: int) -> DeviceWeight:
+    """Descriptor of a packed weight whose blob sits at device address base."""
+    g = lambda k: (base + offs[k]) if k in offs else 0  # noqa: E731
+    return DeviceWeight.from_pointers(p["fmt"], p["N"], p["K"], g("data"), g("absmax"), g("absmax_q"),
+                                      g("absmax_scale"), p.get("dq_group", 0))
 class LayerStream:
     """Pool of device slots fed from pinned host memory one layer ahead."""
 

@@ -10,6 +10,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -252,6 +253,155 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
   return gemm_launch(w->fmt, dx, pair, maps, a, st);
 }
 
+
+// ------------------------------------------------------------- grouped ------
+// Schedules for the grouped (mixture-of-experts) call, built on the host from
+// the host-side offsets and copied into the workspace with one copy.
+struct GroupedPlan {
+  int E = 0, r = 0;
+  int64_t M = 0, N = 0, K = 0;
+  std::vector<WeightView> table;
+  std::vector<int4> gf, gd, rr, cr;  // GEMM fwd / dX tiles, row tiles, row chunks
+  std::vector<int> cf;               // chunk_first[E+1]
+  SplitPlan t, u;
+  size_t off_table = 0, off_gf = 0, off_gd = 0, off_rr = 0, off_cr = 0, off_cf = 0, sched_bytes = 0;
+  size_t off_act = 0, off_u = 0, off_part = 0, total = 0;
+};
+
+static int validate_grouped(const qlora_weight_desc* ex, int E, const int32_t* off, int r) {
+  if (!ex || !off || E <= 0 || E > kMaxGroups) return QLORA_ERR_INVALID;
+  int v = validate_rank(r);
+  if (v != QLORA_OK) return v;
+  for (int e = 0; e < E; ++e) {
+    if ((v = validate_weight(&ex[e])) != QLORA_OK) return v;
+    if (ex[e].fmt != ex[0].fmt || ex[e].N != ex[0].N || ex[e].K != ex[0].K) return QLORA_ERR_INVALID;
+  }
+  if (off[0] != 0) return QLORA_ERR_INVALID;
+  for (int e = 0; e < E; ++e)
+    if (off[e + 1] < off[e]) return QLORA_ERR_INVALID;
+  if (off[E] > (1 << 30)) return QLORA_ERR_UNSUPPORTED;
+  return QLORA_OK;
+}
+
+static void build_grouped_plan(const qlora_weight_desc* ex, int E, const int32_t* off, int r, GroupedPlan& P) {
+  P.E = E;
+  P.r = r;
+  P.M = off[E];
+  P.N = ex[0].N;
+  P.K = ex[0].K;
+  const int nb_f = (int)((P.N + kBN - 1) / kBN), nb_d = (int)((P.K + kBN - 1) / kBN);
+  constexpr int kChunkRows = 256;
+  P.table.resize(E);
+  P.cf.resize(E + 1);
+  for (int e = 0; e < E; ++e) {
+    P.table[e] = view_of(&ex[e]);
+    const int lo = off[e], c = off[e + 1] - off[e];
+    // GEMM tiles of one expert are consecutive (its weights stay in L2), row
+    // blocks fastest
+    for (int nb = 0; nb < nb_f; ++nb)
+      for (int i = 0; i < c; i += kBM) P.gf.push_back(make_int4(e, lo + i, std::min(kBM, c - i), nb));
+    for (int nb = 0; nb < nb_d; ++nb)
+      for (int i = 0; i < c; i += kBM) P.gd.push_back(make_int4(e, lo + i, std::min(kBM, c - i), nb));
+    for (int i = 0; i < c; i += 64) P.rr.push_back(make_int4(e, lo + i, std::min(64, c - i), 0));
+    P.cf[e] = (int)P.cr.size();
+    for (int i = 0; i < c; i += kChunkRows) P.cr.push_back(make_int4(e, lo + i, lo + std::min(c, i + kChunkRows), 0));
+  }
+  P.cf[E] = (int)P.cr.size();
+  P.t = plan_split((int64_t)std::max<size_t>(P.rr.size(), 1), P.K);
+  P.u = plan_split((int64_t)std::max<size_t>(P.rr.size(), 1), P.N);
+  size_t o = 0;
+  P.off_table = o;
+  o = round256(o + sizeof(WeightView) * E);
+  P.off_gf = o;
+  o = round256(o + sizeof(int4) * P.gf.size());
+  P.off_gd = o;
+  o = round256(o + sizeof(int4) * P.gd.size());
+  P.off_rr = o;
+  o = round256(o + sizeof(int4) * P.rr.size());
+  P.off_cr = o;
+  o = round256(o + sizeof(int4) * P.cr.size());
+  P.off_cf = o;
+  o = round256(o + sizeof(int) * P.cf.size());
+  P.sched_bytes = o;
+  P.off_act = o;
+  o = round256(o + (size_t)P.M * r * 2);
+  P.off_u = o;
+  o = round256(o + (size_t)P.M * r * 4);
+  size_t part = (size_t)P.t.splits * P.M * r;
+  part = std::max(part, (size_t)P.u.splits * P.M * r);
+  part = std::max(part, P.cr.size() * (size_t)P.N * r * 2);
+  part = std::max(part, P.cr.size() * (size_t)P.K * r * 2);
+  P.off_part = o;
+  o = round256(o + std::max<size_t>(part, 1) * 4);
+  P.total = o;
+}
+
+static cudaError_t upload_grouped_plan(const GroupedPlan& P, uint8_t* ws, cudaStream_t st) {
+  std::vector<uint8_t> h(P.sched_bytes, 0);
+  std::memcpy(h.data() + P.off_table, P.table.data(), sizeof(WeightView) * P.table.size());
+  if (!P.gf.empty()) std::memcpy(h.data() + P.off_gf, P.gf.data(), sizeof(int4) * P.gf.size());
+  if (!P.gd.empty()) std::memcpy(h.data() + P.off_gd, P.gd.data(), sizeof(int4) * P.gd.size());
+  if (!P.rr.empty()) std::memcpy(h.data() + P.off_rr, P.rr.data(), sizeof(int4) * P.rr.size());
+  if (!P.cr.empty()) std::memcpy(h.data() + P.off_cr, P.cr.data(), sizeof(int4) * P.cr.size());
+  std::memcpy(h.data() + P.off_cf, P.cf.data(), sizeof(int) * P.cf.size());
+  // pageable source: the copy is staged before this call returns
+  return cudaMemcpyAsync(ws, h.data(), h.size(), cudaMemcpyHostToDevice, st);
+}
+
+// bf16 [E][mid][inner] as a 3-D tensor (innermost first), box {64, rows, 1}
+static bool map3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t E, uint32_t box_inner,
+                  uint32_t box_rows) {
+  const uint64_t dims[3] = {inner, mid, E};
+  const uint64_t strides[2] = {inner * 2, inner * mid * 2};
+  const uint32_t box[3] = {box_inner, box_rows, 1};
+  return make_map(m, base, 3, dims, strides, box);
+}
+
+// bf16 expert weights must be one array [E][N][K] for the 3-D map
+static bool map3d_weights(CUtensorMap* m, const qlora_weight_desc* ex, int E, int64_t K, int64_t N,
+                          uint32_t box_rows) {
+  const uint8_t* b0 = static_cast<const uint8_t*>(ex[0].data);
+  for (int e = 1; e < E; ++e)
+    if (static_cast<const uint8_t*>(ex[e].data) != b0 + (size_t)e * N * K * 2) return false;
+  return map3d(m, b0, K, N, E, 64, box_rows);
+}
+
+static GemmArgs grouped_args(const GroupedPlan& P, bool dx, int rank, void* out, uint8_t* ws) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.M = (int)P.M;
+  a.n_out = (int)(dx ? P.K : P.N);
+  a.k_red = (int)(dx ? P.N : P.K);
+  a.rank = rank;
+  a.num_n_blk = (a.n_out + kBN - 1) / kBN;
+  a.num_tiles = (int)(dx ? P.gd.size() : P.gf.size());
+  a.w_lines_per_row = P.K / 64;
+  a.w_rows = P.N;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.tile_sched = reinterpret_cast<const int4*>(ws + (dx ? P.off_gd : P.off_gf));
+  a.num_groups = P.E;
+  a.groups = reinterpret_cast<const GroupTable*>(ws + P.off_table);
+  a.err = device_error_word();
+  return a;
+}
+
+static cudaError_t gemm_launch_grouped(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& a, cudaStream_t st) {
+  std::unique_lock<std::mutex> g(g_prof_mu);
+  if (!g_prof_on) {
+    g.unlock();
+    return launch_qgemm(fmt, dx, true, maps, a, sm_count(), st);
+  }
+  GemmRec r;
+  r.a = prof_event();
+  r.b = prof_event();
+  r.flops = 2.0 * (double)a.M * (double)a.n_out * (double)(a.k_red + a.rank);
+  cudaEventRecord(r.a, st);
+  cudaError_t e = launch_qgemm(fmt, dx, true, maps, a, sm_count(), st);
+  cudaEventRecord(r.b, st);
+  g_prof_recs.push_back(r);
+  return e;
+}
+
 }  // namespace qlora
 
 using namespace qlora;
@@ -421,22 +571,112 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
 
 size_t qlora_grouped_workspace_bytes(const qlora_weight_desc* experts, int32_t E, const int32_t* offsets,
                                      int32_t rank) {
-  (void)experts;
-  (void)E;
-  (void)offsets;
-  (void)rank;
-  return 0;
+  if (validate_grouped(experts, E, offsets, rank) != QLORA_OK) return 0;
+  GroupedPlan P;
+  build_grouped_plan(experts, E, offsets, rank, P);
+  return P.total;
 }
 
-int32_t grouped_moe_qlora_fwd(const qlora_weight_desc*, int32_t, const int32_t*, int32_t, float, const void*,
-                              const void*, const void*, void*, float*, void*, size_t, void*) {
-  return QLORA_ERR_UNSUPPORTED;
+int32_t grouped_moe_qlora_fwd(const qlora_weight_desc* experts, int32_t E, const int32_t* offsets, int32_t rank,
+                              float alpha, const void* X, const void* A, const void* B, void* Y, float* T_save,
+                              void* workspace, size_t ws_bytes, void* stream) {
+  int v = validate_grouped(experts, E, offsets, rank);
+  if (v != QLORA_OK) return v;
+  if (!std::isfinite(alpha)) return QLORA_ERR_INVALID;
+  const int64_t M = offsets[E];
+  if (M == 0) return QLORA_OK;
+  if (!X || !A || !B || !Y || !T_save) return QLORA_ERR_INVALID;
+  if (!aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(Y) || !aligned16(T_save)) return QLORA_ERR_ALIGN;
+  GroupedPlan P;
+  build_grouped_plan(experts, E, offsets, rank, P);
+  if (!workspace || ws_bytes < P.total) return QLORA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (upload_grouped_plan(P, ws, st) != cudaSuccess) return QLORA_ERR_CUDA;
+  const int64_t N = P.N, K = P.K;
+  const float s = alpha / (float)rank;
+  __nv_bfloat16* sT = reinterpret_cast<__nv_bfloat16*>(ws + P.off_act);
+  float* part = reinterpret_cast<float*>(ws + P.off_part);
+
+  // 1) T = X A_e^T per expert's rows, T_save = T, sT = bf16(s T)
+  cudaError_t e = launch_row_reduce(static_cast<const __nv_bfloat16*>(X), M, K, static_cast<const __nv_bfloat16*>(A),
+                                    rank, true, part, P.t, st, reinterpret_cast<const int4*>(ws + P.off_rr),
+                                    (int)P.rr.size(), (int64_t)rank * K);
+  if (e == cudaSuccess) e = launch_fin_rows(part, P.t.splits, M, rank, s, T_save, sT, st);
+  if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  // 2) Y = X deq(W_e)^T + sT B_e^T
+  GemmMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  bool ok = map2d(&maps.a, X, K, M, 64, 128) && map2d(&maps.la, sT, rank, M, 64, 128) &&
+            map3d(&maps.lb, B, rank, N, E, 64, 256);
+  if (experts[0].fmt == QLORA_FMT_BF16) ok = ok && map3d_weights(&maps.w, experts, E, K, N, 256);
+  if (!ok) return QLORA_ERR_CUDA;
+  GemmArgs a = grouped_args(P, false, rank, Y, ws);
+  return cuda_status(gemm_launch_grouped(experts[0].fmt, false, maps, a, st));
 }
 
-int32_t grouped_moe_qlora_bwd(const qlora_weight_desc*, int32_t, const int32_t*, int32_t, float, const void*,
-                              const void*, const void*, const float*, const void*, void*, float*, float*, void*,
-                              size_t, void*) {
-  return QLORA_ERR_UNSUPPORTED;
+int32_t grouped_moe_qlora_bwd(const qlora_weight_desc* experts, int32_t E, const int32_t* offsets, int32_t rank,
+                              float alpha, const void* X, const void* A, const void* B, const float* T_save,
+                              const void* dY, void* dX, float* dA, float* dB, void* workspace, size_t ws_bytes,
+                              void* stream) {
+  int v = validate_grouped(experts, E, offsets, rank);
+  if (v != QLORA_OK) return v;
+  if (!std::isfinite(alpha)) return QLORA_ERR_INVALID;
+  if (!dA || !dB) return QLORA_ERR_INVALID;
+  const int64_t M = offsets[E];
+  const int64_t N = experts[0].N, K = experts[0].K;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    if (cudaMemsetAsync(dA, 0, (size_t)E * rank * K * 4, st) != cudaSuccess) return QLORA_ERR_CUDA;
+    return cuda_status(cudaMemsetAsync(dB, 0, (size_t)E * N * rank * 4, st));
+  }
+  if (!X || !A || !B || !T_save || !dY) return QLORA_ERR_INVALID;
+  if (!aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(T_save) || !aligned16(dY) || !aligned16(dA) ||
+      !aligned16(dB) || (dX && !aligned16(dX)))
+    return QLORA_ERR_ALIGN;
+  GroupedPlan P;
+  build_grouped_plan(experts, E, offsets, rank, P);
+  if (!workspace || ws_bytes < P.total) return QLORA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (upload_grouped_plan(P, ws, st) != cudaSuccess) return QLORA_ERR_CUDA;
+  const float s = alpha / (float)rank;
+  __nv_bfloat16* sU = reinterpret_cast<__nv_bfloat16*>(ws + P.off_act);
+  float* U = reinterpret_cast<float*>(ws + P.off_u);
+  float* part = reinterpret_cast<float*>(ws + P.off_part);
+  const __nv_bfloat16* dYb = static_cast<const __nv_bfloat16*>(dY);
+  const int4* chunks = reinterpret_cast<const int4*>(ws + P.off_cr);
+  const int* chunk_first = reinterpret_cast<const int*>(ws + P.off_cf);
+
+  // 1) U = dY B_e per expert's rows: U fp32, sU = bf16(s U)
+  cudaError_t e = launch_row_reduce(dYb, M, N, static_cast<const __nv_bfloat16*>(B), rank, false, part, P.u, st,
+                                    reinterpret_cast<const int4*>(ws + P.off_rr), (int)P.rr.size(),
+                                    (int64_t)N * rank);
+  if (e == cudaSuccess) e = launch_fin_rows(part, P.u.splits, M, rank, s, U, sU, st);
+  // 2) dB_e = s dY_e^T T_e
+  SplitPlan cp;
+  cp.splits = (int)P.cr.size();
+  cp.chunk = 0;
+  if (e == cudaSuccess) e = launch_col_reduce(dYb, M, N, T_save, rank, part, cp, st, chunks);
+  if (e == cudaSuccess) e = launch_fin_cols_grouped(part, chunk_first, E, N, rank, s, dB, false, st);
+  if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  // 3) dX = dY deq(W_e) + sU A_e
+  if (dX) {
+    GemmMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    bool ok = map2d(&maps.a, dY, N, M, 64, 128) && map2d(&maps.la, sU, rank, M, 64, 128) &&
+              map3d(&maps.lb, A, K, rank, E, 64, 64);
+    if (experts[0].fmt == QLORA_FMT_BF16) ok = ok && map3d_weights(&maps.w, experts, E, K, N, 64);
+    if (!ok) return QLORA_ERR_CUDA;
+    GemmArgs a = grouped_args(P, true, rank, dX, ws);
+    e = gemm_launch_grouped(experts[0].fmt, true, maps, a, st);
+    if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  }
+  // 4) dA_e = s U_e^T X_e
+  e = launch_col_reduce(static_cast<const __nv_bfloat16*>(X), M, K, U, rank, part, cp, st, chunks);
+  if (e == cudaSuccess) e = launch_fin_cols_grouped(part, chunk_first, E, K, rank, s, dA, true, st);
+  return cuda_status(e);
 }
 
 }  // extern "C"

@@ -39,10 +39,14 @@ inline SplitPlan plan_split(int64_t outer_tiles, int64_t red_len) {
   return p;
 }
 
+// tiles / chunks: optional grouped-row lists (see skinny.cu); null for dense.
 cudaError_t launch_row_reduce(const __nv_bfloat16* L, int64_t P, int64_t J, const __nv_bfloat16* S, int Q,
-                              bool s_qj, float* partial, const SplitPlan& sp, cudaStream_t st);
+                              bool s_qj, float* partial, const SplitPlan& sp, cudaStream_t st,
+                              const int4* tiles = nullptr, int ntiles = 0, int64_t s_stride = 0);
 cudaError_t launch_col_reduce(const __nv_bfloat16* L, int64_t P, int64_t J, const float* S, int Q,
-                              float* partial, const SplitPlan& sp, cudaStream_t st);
+                              float* partial, const SplitPlan& sp, cudaStream_t st, const int4* chunks = nullptr);
+cudaError_t launch_fin_cols_grouped(const float* partial, const int* chunk_first, int groups, int64_t J, int Q,
+                                    float scale, float* out, bool transposed, cudaStream_t st);
 cudaError_t launch_fin_rows(const float* partial, int splits, int64_t P, int Q, float scale, float* out_f32,
                             __nv_bfloat16* out_scaled, cudaStream_t st);
 cudaError_t launch_fin_cols(const float* partial, int splits, int64_t J, int Q, float scale, float* out,

@@ -70,18 +70,26 @@ __device__ __forceinline__ uint32_t s_addr(const void* p) { return (uint32_t)__c
 //   S_QJ = true : S given as [Q x J] (j contiguous), e.g. A [r x K]
 //   S_QJ = false: S given as [J x Q] (q contiguous), e.g. B [N x r]
 // partial: fp32 [splits][P][Q].
+// Grouped rows: with `tiles` non-null, CTA x handles tiles[x] = (group g,
+// first row, row count) and uses S + g * s_stride (the group's adapter).
 // ---------------------------------------------------------------------------
 template <int Q, bool S_QJ>
 __global__ void __launch_bounds__(NTHR) rr_kernel(const __nv_bfloat16* __restrict__ L, int64_t P, int64_t J,
                                                   const __nv_bfloat16* __restrict__ S, float* __restrict__ partial,
-                                                  int64_t jc) {
+                                                  int64_t jc, const int4* __restrict__ tiles, int64_t s_stride) {
   constexpr int SP = S_QJ ? LPITCH : (Q + 8);           // smem pitch of S tile
   constexpr int S_ELEMS = S_QJ ? Q * LPITCH : TJ * (Q + 8);
   __shared__ __align__(128) __nv_bfloat16 sL[2][TP * LPITCH];
   __shared__ __align__(128) __nv_bfloat16 sS[2][S_ELEMS];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t p0 = (int64_t)blockIdx.x * TP;
+  int64_t p0 = (int64_t)blockIdx.x * TP, p_lim = P;
+  if (tiles != nullptr) {
+    const int4 tl = tiles[blockIdx.x];
+    p0 = tl.y;
+    p_lim = (int64_t)tl.y + tl.z;
+    S += (int64_t)tl.x * s_stride;
+  }
   const int64_t j_begin = (int64_t)blockIdx.y * jc;
   const int64_t j_end = min(J, j_begin + jc);
   const int nchunks = (int)((j_end - j_begin + TJ - 1) / TJ);
@@ -92,7 +100,7 @@ __global__ void __launch_bounds__(NTHR) rr_kernel(const __nv_bfloat16* __restric
     for (int i = 0; i < 4; ++i) {
       const int piece = tid + i * NTHR;
       const int r = piece >> 3, c8 = (piece & 7) * 8;
-      const bool ok = (p0 + r) < P;
+      const bool ok = (p0 + r) < p_lim;
       const __nv_bfloat16* src = L + (ok ? (p0 + r) : 0) * J + j0 + c8;
       cp_async16(s_addr(&sL[buf][r * LPITCH + c8]), src, ok);
     }
@@ -169,8 +177,8 @@ __global__ void __launch_bounds__(NTHR) rr_kernel(const __nv_bfloat16* __restric
   for (int nt = 0; nt < Q / 8; ++nt) {
     const int q = nt * 8 + 2 * t4;
     const int64_t r0 = p0 + warp * 16 + g, r1 = r0 + 8;
-    if (r0 < P) *reinterpret_cast<float2*>(out + r0 * Q + q) = make_float2(acc[nt][0], acc[nt][1]);
-    if (r1 < P) *reinterpret_cast<float2*>(out + r1 * Q + q) = make_float2(acc[nt][2], acc[nt][3]);
+    if (r0 < p_lim) *reinterpret_cast<float2*>(out + r0 * Q + q) = make_float2(acc[nt][0], acc[nt][1]);
+    if (r1 < p_lim) *reinterpret_cast<float2*>(out + r1 * Q + q) = make_float2(acc[nt][2], acc[nt][3]);
   }
 }
 
@@ -181,10 +189,12 @@ __global__ void __launch_bounds__(NTHR) rr_kernel(const __nv_bfloat16* __restric
 // side as a [P x 2Q] bf16 tile, so the tensor-core products keep ~16
 // significant bits of S.  partial: fp32 [splits][J][2Q] (hi half, lo half).
 // ---------------------------------------------------------------------------
+// Grouped rows: with `chunks` non-null, split y covers rows
+// [chunks[y].y, chunks[y].z) (one group's rows) instead of [y pc, (y+1) pc).
 template <int Q>
 __global__ void __launch_bounds__(NTHR) cr_kernel(const __nv_bfloat16* __restrict__ L, int64_t P, int64_t J,
                                                   const float* __restrict__ S, float* __restrict__ partial,
-                                                  int64_t pc) {
+                                                  int64_t pc, const int4* __restrict__ chunks) {
   constexpr int Q2 = 2 * Q;
   constexpr int SP = Q2 + 8;
   extern __shared__ __align__(128) uint8_t cr_smem[];
@@ -195,8 +205,13 @@ __global__ void __launch_bounds__(NTHR) cr_kernel(const __nv_bfloat16* __restric
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t j0 = (int64_t)blockIdx.x * TJ;
-  const int64_t p_begin = (int64_t)blockIdx.y * pc;
-  const int64_t p_end = min(P, p_begin + pc);
+  int64_t p_begin = (int64_t)blockIdx.y * pc;
+  int64_t p_end = min(P, p_begin + pc);
+  if (chunks != nullptr) {
+    const int4 ch = chunks[blockIdx.y];
+    p_begin = ch.y;
+    p_end = ch.z;
+  }
   const int nchunks = (int)((p_end - p_begin + TP - 1) / TP);
 
   auto load_chunk = [&](int buf, int64_t pp) {
@@ -313,18 +328,20 @@ __global__ void fin_cols_kernel(const float* __restrict__ partial, int splits, i
 // ---------------------------------------------------------------------------
 template <int Q>
 static cudaError_t launch_rr_q(const __nv_bfloat16* L, int64_t P, int64_t J, const __nv_bfloat16* S, bool s_qj,
-                               float* partial, const SplitPlan& sp, cudaStream_t st) {
-  dim3 grid((unsigned)((P + TP - 1) / TP), (unsigned)sp.splits);
+                               float* partial, const SplitPlan& sp, cudaStream_t st, const int4* tiles,
+                               int ntiles, int64_t s_stride) {
+  dim3 grid((unsigned)(tiles ? ntiles : (P + TP - 1) / TP), (unsigned)sp.splits);
+  if (grid.x == 0) return cudaSuccess;
   if (s_qj)
-    rr_kernel<Q, true><<<grid, NTHR, 0, st>>>(L, P, J, S, partial, sp.chunk);
+    rr_kernel<Q, true><<<grid, NTHR, 0, st>>>(L, P, J, S, partial, sp.chunk, tiles, s_stride);
   else
-    rr_kernel<Q, false><<<grid, NTHR, 0, st>>>(L, P, J, S, partial, sp.chunk);
+    rr_kernel<Q, false><<<grid, NTHR, 0, st>>>(L, P, J, S, partial, sp.chunk, tiles, s_stride);
   return cudaGetLastError();
 }
 
 template <int Q>
 static cudaError_t launch_cr_q(const __nv_bfloat16* L, int64_t P, int64_t J, const float* S, float* partial,
-                               const SplitPlan& sp, cudaStream_t st) {
+                               const SplitPlan& sp, cudaStream_t st, const int4* chunks) {
   constexpr size_t smem = 2 * sizeof(__nv_bfloat16) * (TP * LPITCH + TP * (2 * Q + 8));
   static bool attr = false;
   if (!attr) {
@@ -333,7 +350,8 @@ static cudaError_t launch_cr_q(const __nv_bfloat16* L, int64_t P, int64_t J, con
     attr = true;
   }
   dim3 grid((unsigned)(J / TJ), (unsigned)sp.splits);
-  cr_kernel<Q><<<grid, NTHR, smem, st>>>(L, P, J, S, partial, sp.chunk);
+  if (grid.y == 0) return cudaSuccess;
+  cr_kernel<Q><<<grid, NTHR, smem, st>>>(L, P, J, S, partial, sp.chunk, chunks);
   return cudaGetLastError();
 }
 
@@ -351,15 +369,51 @@ static cudaError_t launch_cr_q(const __nv_bfloat16* L, int64_t P, int64_t J, con
   }
 
 cudaError_t launch_row_reduce(const __nv_bfloat16* L, int64_t P, int64_t J, const __nv_bfloat16* S, int Q,
-                              bool s_qj, float* partial, const SplitPlan& sp, cudaStream_t st) {
+                              bool s_qj, float* partial, const SplitPlan& sp, cudaStream_t st, const int4* tiles,
+                              int ntiles, int64_t s_stride) {
   count_launch(1);
-  QLORA_RANK_DISPATCH(launch_rr_q, L, P, J, S, s_qj, partial, sp, st)
+  QLORA_RANK_DISPATCH(launch_rr_q, L, P, J, S, s_qj, partial, sp, st, tiles, ntiles, s_stride)
 }
 
 cudaError_t launch_col_reduce(const __nv_bfloat16* L, int64_t P, int64_t J, const float* S, int Q,
-                              float* partial, const SplitPlan& sp, cudaStream_t st) {
+                              float* partial, const SplitPlan& sp, cudaStream_t st, const int4* chunks) {
   count_launch(1);
-  QLORA_RANK_DISPATCH(launch_cr_q, L, P, J, S, partial, sp, st)
+  QLORA_RANK_DISPATCH(launch_cr_q, L, P, J, S, partial, sp, st, chunks)
+}
+
+// Grouped finalize: out[g] = scale * sum of the hi/lo partials of chunks
+// chunk_first[g] .. chunk_first[g+1]-1 (zero for a group without rows);
+// out[g] is [J x Q] at out + g * J * Q, or [Q x J] when transposed.
+__global__ void fin_cols_grouped_kernel(const float* __restrict__ partial, const int* __restrict__ chunk_first,
+                                        int64_t J, int Q, float scale, float* __restrict__ out, int transposed) {
+  const int g = blockIdx.y;
+  const int c0 = chunk_first[g], c1 = chunk_first[g + 1];
+  const int64_t JQ = J * Q, JQ2 = 2 * JQ;
+  float* og = out + (int64_t)g * JQ;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < JQ; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t j = i / Q, q = i % Q;
+    const int64_t o = j * 2 * Q + q;
+    float hi = 0.f, lo = 0.f;
+    for (int c = c0; c < c1; ++c) {
+      hi += partial[(int64_t)c * JQ2 + o];
+      lo += partial[(int64_t)c * JQ2 + o + Q];
+    }
+    const float v = (hi + lo) * scale;
+    if (transposed)
+      og[q * J + j] = v;
+    else
+      og[i] = v;
+  }
+}
+
+cudaError_t launch_fin_cols_grouped(const float* partial, const int* chunk_first, int groups, int64_t J, int Q,
+                                    float scale, float* out, bool transposed, cudaStream_t st) {
+  if (groups <= 0) return cudaSuccess;
+  count_launch(1);
+  int64_t b = (J * Q + 255) / 256;
+  dim3 grid((unsigned)(b < 64 ? b : 64), (unsigned)groups);
+  fin_cols_grouped_kernel<<<grid, 256, 0, st>>>(partial, chunk_first, J, Q, scale, out, transposed ? 1 : 0);
+  return cudaGetLastError();
 }
 
 static unsigned fin_grid(int64_t n) {

@@ -2,11 +2,15 @@
 // device slots, copied one layer ahead on a dedicated copy stream, ordered
 // against the compute stream with events.
 //
-// Each slot carries the layer id it holds.  acquire() checks the id, so a
-// slot that was refilled with another layer is never read as the old one (a
-// stale buffer is an error, not a silent wrong answer).  A layer that is
-// still resident is not copied again (the backward pass starts on the layers
-// the forward pass ended with).
+// Each slot carries the layer id it holds and a state: empty, pending (copied
+// or resident and announced by prefetch, not yet acquired), acquired, or
+// released (consumed, may be refilled).  acquire() checks the id, so a slot
+// that was refilled with another layer is never read as the old one (a stale
+// buffer is an error, not a silent wrong answer).  prefetch() only refills
+// empty or released slots, least recently used first; it never evicts a
+// pending layer, and fails with QLORA_ERR_STATE when no slot is free.  A layer
+// that is still resident is not copied again (the backward pass starts on the
+// layers the forward pass ended with).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -26,6 +30,7 @@ struct StreamPool {
   std::vector<cudaEvent_t> ready, freed;
   std::vector<int> layer;     // layer held by the slot, -1 = none
   std::vector<int> acquired;  // compute work holding the slot not yet released
+  std::vector<int> pending;   // announced by prefetch, not yet acquired
   std::vector<int> freed_valid;
   std::vector<uint64_t> last_use;
   uint64_t clock = 0;
@@ -61,6 +66,7 @@ int32_t qlora_stream_create(int32_t slots, size_t slot_bytes, void** handle) {
   }
   p->layer.assign(slots, -1);
   p->acquired.assign(slots, 0);
+  p->pending.assign(slots, 0);
   p->freed_valid.assign(slots, 0);
   p->last_use.assign(slots, 0);
   *handle = p;
@@ -74,15 +80,16 @@ int32_t qlora_stream_prefetch(void* handle, int32_t layer, const void* host_src,
   std::lock_guard<std::mutex> g(p->mu);
   for (int i = 0; i < p->slots; ++i)
     if (p->layer[i] == layer) {  // already resident
+      p->pending[i] = 1;
       p->last_use[i] = ++p->clock;
       return QLORA_OK;
     }
   int victim = -1;
   for (int i = 0; i < p->slots; ++i) {
-    if (p->acquired[i]) continue;
+    if (p->acquired[i] || p->pending[i]) continue;
     if (victim < 0 || p->last_use[i] < p->last_use[victim]) victim = i;
   }
-  if (victim < 0) return QLORA_ERR_STATE;  // every slot is in use
+  if (victim < 0) return QLORA_ERR_STATE;  // every slot is in use or pending
   if (p->freed_valid[victim] && cudaStreamWaitEvent(p->copy, p->freed[victim], 0) != cudaSuccess)
     return QLORA_ERR_CUDA;
   p->layer[victim] = -1;
@@ -91,6 +98,7 @@ int32_t qlora_stream_prefetch(void* handle, int32_t layer, const void* host_src,
     return QLORA_ERR_CUDA;
   if (cudaEventRecord(p->ready[victim], p->copy) != cudaSuccess) return QLORA_ERR_CUDA;
   p->layer[victim] = layer;
+  p->pending[victim] = 1;
   p->last_use[victim] = ++p->clock;
   return QLORA_OK;
 }
@@ -104,6 +112,7 @@ int32_t qlora_stream_acquire(void* handle, int32_t layer, void* compute_stream, 
     if (cudaStreamWaitEvent(static_cast<cudaStream_t>(compute_stream), p->ready[i], 0) != cudaSuccess)
       return QLORA_ERR_CUDA;
     p->acquired[i] += 1;
+    p->pending[i] = 0;
     p->last_use[i] = ++p->clock;
     *dev_ptr = p->dev + (size_t)i * p->slot_bytes;
     return QLORA_OK;
