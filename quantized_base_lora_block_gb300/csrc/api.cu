@@ -221,8 +221,10 @@ static cudaError_t gemm_launch(int fmt, bool dx, bool pair, const GemmMaps& maps
 static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M, int rank, const void* a_op,
                                   const void* la, const void* lb, void* out, cudaStream_t st) {
   const int64_t N = w->N, K = w->K;
-  const bool pair = M > kBM;  // 256-row tiles on a CTA pair; short problems use one CTA per tile
-  const uint32_t brows = pair ? 128 : 256;
+  const bool pair = M > kBM;  // pair tiles on an SM pair; short problems use one CTA per 128 x 256 tile
+  const int tile_rows = pair ? pair_tile_rows(w->fmt) : kBM;
+  const int tile_cols = pair ? pair_tile_cols(w->fmt) : kBN;
+  const uint32_t brows = pair ? (uint32_t)(tile_cols / 2) : 256;
   GemmMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   bool ok;
@@ -242,9 +244,8 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
   a.n_out = (int)(dx ? K : N);
   a.k_red = (int)(dx ? N : K);
   a.rank = rank;
-  a.num_n_blk = (a.n_out + kBN - 1) / kBN;
-  const int64_t row_tile = pair ? 256 : kBM;
-  a.num_tiles = (int)(((M + row_tile - 1) / row_tile) * a.num_n_blk);
+  a.num_n_blk = (a.n_out + tile_cols - 1) / tile_cols;
+  a.num_tiles = (int)(((M + tile_rows - 1) / tile_rows) * a.num_n_blk);
   a.w_lines_per_row = K / 64;
   a.w_rows = N;
   a.out = static_cast<__nv_bfloat16*>(out);

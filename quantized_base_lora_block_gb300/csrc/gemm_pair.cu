@@ -33,29 +33,48 @@ namespace qlora {
 
 namespace {
 
-constexpr int P_STAGES = 6;
-constexpr int P_A_BYTES = 128 * kBK * 2;  // this CTA's 128 A rows x 64
-constexpr int P_B_BYTES = 128 * kBK * 2;  // this CTA's half of B: 128 x 64
-constexpr int P_DQ_GROUPS = 3;            // groups of 4 decode warps, rotating over stages
-constexpr int P_DQ_WARPS = 4 * P_DQ_GROUPS;
-static_assert(P_STAGES % P_DQ_GROUPS == 0, "a stage must always be decoded by the same group");
 constexpr int P_TMEM_COLS = 512;
 
+// Tile shape of the pair, by the number of accumulators NACC:
+//   NACC = 1: 256 x 256 (one M256 x N256 accumulator per buffer);
+//   NACC = 2: 512 x 128 (two M256 x N128 accumulators per buffer sharing
+//             every decoded B tile, which halves the decode work per flop).
+// Either way a buffer is 256 TMEM columns and two buffers fill TMEM.
+template <int NACC>
+struct PairCfg {
+  static constexpr int TM = 256 * NACC;                 // output rows per pair tile
+  static constexpr int TN = NACC == 1 ? 256 : 128;      // output columns per pair tile
+  static constexpr int HALF_N = TN / 2;                 // B rows (or columns) per CTA
+  static constexpr int A_BYTES = NACC * 128 * kBK * 2;  // this CTA's A rows
+  static constexpr int B_BYTES = HALF_N * kBK * 2;      // this CTA's half of B
+  static constexpr int STAGES = NACC == 1 ? 6 : 5;
+  static constexpr int LINES = HALF_N;                  // decoded 64-wide lines per stage per CTA
+  static constexpr int GROUP_WARPS = LINES / 32;        // one line per thread of a group
+  static constexpr int GROUPS = NACC == 1 ? 3 : 5;      // groups rotate over stages
+  static constexpr int DQ_WARPS = GROUP_WARPS * GROUPS;
+  static_assert(STAGES % GROUPS == 0, "a stage must always be decoded by the same group");
+};
+
+template <int NACC>
 struct __align__(8) PairBarriers {
-  uint64_t full[P_STAGES];    // CTA 0: bytes of both CTAs' copies (CTA 1: unused)
-  uint64_t bready[P_STAGES];  // CTA 0: decode warps of both CTAs
-  uint64_t empty[P_STAGES];   // both: MMA completion (multicast)
-  uint64_t acc_full[2];       // both: MMA completion (multicast)
-  uint64_t acc_empty[2];      // CTA 0: epilogue warps of both CTAs
+  uint64_t full[PairCfg<NACC>::STAGES];    // CTA 0: bytes of both CTAs' copies (CTA 1: unused)
+  uint64_t bready[PairCfg<NACC>::STAGES];  // CTA 0: decode warps of both CTAs
+  uint64_t empty[PairCfg<NACC>::STAGES];   // both: MMA completion (multicast)
+  uint64_t acc_full[2];                    // both: MMA completion (multicast)
+  uint64_t acc_empty[2];                   // CTA 0: epilogue warps of both CTAs
   uint32_t tmem_base;
   int abort;
 };
 
-constexpr size_t P_SMEM_BYTES = 1024 + (size_t)P_STAGES * (P_A_BYTES + P_B_BYTES) + sizeof(PairBarriers);
+template <int NACC>
+constexpr size_t p_smem_bytes() {
+  return 1024 + (size_t)PairCfg<NACC>::STAGES * (PairCfg<NACC>::A_BYTES + PairCfg<NACC>::B_BYTES) +
+         sizeof(PairBarriers<NACC>);
+}
 
-template <int FMT>
+template <int FMT, int NACC>
 constexpr int p_threads() {
-  return (FMT == FMT_BF16) ? 6 * 32 : (6 + P_DQ_WARPS) * 32;
+  return (FMT == FMT_BF16) ? 6 * 32 : (6 + PairCfg<NACC>::DQ_WARPS) * 32;
 }
 
 struct PairTile {
@@ -65,33 +84,37 @@ struct PairTile {
 // forward: row blocks fastest (the activation block stays in L2 while the
 // weight slab streams); dX: column blocks fastest (the dY row block stays in
 // L2 while every output column block of it runs).
-template <bool DX>
+template <bool DX, int NACC>
 __device__ __forceinline__ PairTile pair_tile(const GemmArgs& a, int t) {
-  const int num_m = (a.M + 255) / 256;
+  constexpr int TM = PairCfg<NACC>::TM, TN = PairCfg<NACC>::TN;
+  const int num_m = (a.M + TM - 1) / TM;
   const int num_n = a.num_n_blk;
   PairTile p;
   if (!DX) {
-    p.m0 = (t % num_m) * 256;
-    p.n0 = (t / num_m) * kBN;
+    p.m0 = (t % num_m) * TM;
+    p.n0 = (t / num_m) * TN;
   } else {
-    p.n0 = (t % num_n) * kBN;
-    p.m0 = (t / num_n) * 256;
+    p.n0 = (t % num_n) * TN;
+    p.m0 = (t / num_n) * TM;
   }
   return p;
 }
 
 }  // namespace
 
-template <int FMT, bool DX>
-__global__ void __launch_bounds__(p_threads<FMT>(), 1)
+template <int FMT, bool DX, int NACC>
+__global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
     qgemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_lb,
                       const GemmArgs args) {
+  using Cfg = PairCfg<NACC>;
+  constexpr int P_STAGES = Cfg::STAGES, P_A_BYTES = Cfg::A_BYTES, P_B_BYTES = Cfg::B_BYTES;
+  constexpr int TN = Cfg::TN, HALF_N = Cfg::HALF_N;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sA0 = smem_u32(smem);
   const uint32_t sB0 = sA0 + P_STAGES * P_A_BYTES;
-  PairBarriers* bars = reinterpret_cast<PairBarriers*>(smem + P_STAGES * (P_A_BYTES + P_B_BYTES));
+  PairBarriers<NACC>* bars = reinterpret_cast<PairBarriers<NACC>*>(smem + P_STAGES * (P_A_BYTES + P_B_BYTES));
   volatile int* abort = &bars->abort;
 
   const uint32_t rank = cluster_ctarank();
@@ -105,7 +128,7 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < P_STAGES; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
-      mbar_init(smem_u32(&bars->bready[s]), 2 * 4);  // 4 warps of one group, both CTAs
+      mbar_init(smem_u32(&bars->bready[s]), 2 * Cfg::GROUP_WARPS);  // one group's warps, both CTAs
       mbar_init(smem_u32(&bars->empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -135,9 +158,9 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
     if (lane == 0) {
       uint32_t it = 0;
       for (int lt = 0; lt < my_tiles; ++lt) {
-        const PairTile tc = pair_tile<DX>(args, pair + lt * num_pairs);
-        const int am = tc.m0 + 128 * (int)rank;  // this CTA's A rows
-        const int bn = tc.n0 + 128 * (int)rank;  // this CTA's half of B
+        const PairTile tc = pair_tile<DX, NACC>(args, pair + lt * num_pairs);
+        const int am = tc.m0 + 128 * (int)rank;     // this CTA's A rows (+256 per accumulator)
+        const int bn = tc.n0 + HALF_N * (int)rank;  // this CTA's half of B
         for (int kb = 0; kb < nkb_total; ++kb, ++it) {
           const int s = it % P_STAGES;
           const uint32_t ph = (it / P_STAGES) & 1;
@@ -149,22 +172,24 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(&bars->full[s]), 2 * bytes);
           const uint32_t fb = mapa_shared(smem_u32(&bars->full[s]), 0);
           if (!lora) {
-            tma_load_2d_pair(sa, &tm_a, fb, kb * kBK, am);
+#pragma unroll
+            for (int a = 0; a < NACC; ++a) tma_load_2d_pair(sa + a * 16384, &tm_a, fb, kb * kBK, am + 256 * a);
             if (FMT == FMT_BF16) {
               if (!DX) {
                 tma_load_2d_pair(sb, &tm_w, fb, kb * kBK, bn);
               } else {
-                tma_load_2d_pair(sb, &tm_w, fb, bn, kb * kBK);
-                tma_load_2d_pair(sb + 8192, &tm_w, fb, bn + 64, kb * kBK);
+#pragma unroll
+                for (int j = 0; j < HALF_N / 64; ++j) tma_load_2d_pair(sb + j * 8192, &tm_w, fb, bn + 64 * j, kb * kBK);
               }
             }
           } else {
-            tma_load_2d_pair(sa, &tm_la, fb, 0, am);
+#pragma unroll
+            for (int a = 0; a < NACC; ++a) tma_load_2d_pair(sa + a * 16384, &tm_la, fb, 0, am + 256 * a);
             if (!DX) {
               tma_load_2d_pair(sb, &tm_lb, fb, 0, bn);
             } else {
-              tma_load_2d_pair(sb, &tm_lb, fb, bn, 0);
-              tma_load_2d_pair(sb + 8192, &tm_lb, fb, bn + 64, 0);
+#pragma unroll
+              for (int j = 0; j < HALF_N / 64; ++j) tma_load_2d_pair(sb + j * 8192, &tm_lb, fb, bn + 64 * j, 0);
             }
           }
         }
@@ -179,13 +204,13 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(256, kBN, DX);
+      constexpr uint32_t idesc = idesc_bf16_f32(256, TN, DX);
       uint32_t it = 0;
       for (int lt = 0; lt < my_tiles; ++lt) {
         const uint32_t ab = lt & 1, aph = (lt >> 1) & 1;
         if (!mbar_wait_cluster(smem_u32(&bars->acc_empty[ab]), aph ^ 1, abort, args.err)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + ab * kBN;
+        const uint32_t d_tmem = tmem_base + ab * 256;  // NACC accumulators of TN columns
         bool ok = true;
         for (int kb = 0; kb < nkb_total; ++kb, ++it) {
           const int s = it % P_STAGES;
@@ -201,10 +226,13 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
           const int nk = lora ? (args.rank + 15) / 16 : kBK / 16;
           const uint32_t sa = sA0 + s * P_A_BYTES, sb = sB0 + s * P_B_BYTES;
           for (int kk = 0; kk < nk; ++kk) {
-            const uint64_t adesc = smem_desc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bdesc = DX ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
                                       : smem_desc_sw128(sb + kk * 32, 16, 1024);
-            tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int a = 0; a < NACC; ++a) {
+              const uint64_t adesc = smem_desc_sw128(sa + a * 16384 + kk * 32, 16, 1024);
+              tc_mma_bf16_pair(d_tmem + a * TN, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           tc_commit_pair_mc(smem_u32(&bars->empty[s]));
         }
@@ -217,31 +245,34 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
     for (int lt = 0; lt < my_tiles; ++lt) {
-      const PairTile tc = pair_tile<DX>(args, pair + lt * num_pairs);
+      const PairTile tc = pair_tile<DX, NACC>(args, pair + lt * num_pairs);
       const uint32_t ab = lt & 1, aph = (lt >> 1) & 1;
       bool ok = true;
       if (lane == 0) ok = mbar_wait_cluster(smem_u32(&bars->acc_full[ab]), aph, abort, args.err);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      const int row = tc.m0 + 128 * (int)rank + row_in_tile;
-      const bool row_ok = row < args.M;
-      __nv_bfloat16* orow = args.out + (int64_t)row * args.n_out + tc.n0;
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kBN + c * 32, v);
-        tc_wait_ld();
-        if (row_ok && tc.n0 + c * 32 < args.n_out) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+      for (int a = 0; a < NACC; ++a) {
+        const int row = tc.m0 + 256 * a + 128 * (int)rank + row_in_tile;
+        const bool row_ok = row < args.M;
+        __nv_bfloat16* orow = args.out + (int64_t)row * args.n_out + tc.n0;
+#pragma unroll 1
+        for (int c = 0; c < TN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * 256 + a * TN + c * 32, v);
+          tc_wait_ld();
+          if (row_ok && tc.n0 + c * 32 < args.n_out) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-            o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-            o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-            o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-            dst[q] = o;
+            for (int q = 0; q < 4; ++q) {
+              uint4 o;
+              o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+              o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+              o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+              o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+              dst[q] = o;
+            }
           }
         }
       }
@@ -251,11 +282,12 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
     }
   } else if (FMT != FMT_BF16) {
     // ------------------------------------------------------------ decode
-    // group g (4 warps) handles the items with it % P_DQ_GROUPS == g; thread
-    // d of the group decodes one 64-element line of this CTA's half of B per
-    // item, with the next item's bytes loaded while it decodes this one.
-    const int g = (warp - 6) >> 2;
-    const int d = ((warp - 6) & 3) * 32 + lane;  // 0..127
+    // group g (GROUP_WARPS warps) handles the items with it % GROUPS == g;
+    // thread d of the group decodes one 64-element line of this CTA's half
+    // of B per item.
+    constexpr int P_DQ_GROUPS = Cfg::GROUPS;
+    const int g = (warp - 6) / Cfg::GROUP_WARPS;
+    const int d = ((warp - 6) % Cfg::GROUP_WARPS) * 32 + lane;  // 0 .. LINES-1
     const int srow = DX ? (d & 63) : d;
     const uint32_t soff = DX ? (uint32_t)((d >> 6) * 8192 + srow * 128) : (uint32_t)(srow * 128);
     const int swz = srow & 7;
@@ -266,43 +298,42 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
       const int lt = (int)(it / (uint32_t)nkb_total), kb = (int)(it % (uint32_t)nkb_total);
       valid = false;
       if (kb >= nkb) return 0;  // adapter chunk: nothing to decode
-      const PairTile tc = pair_tile<DX>(args, pair + lt * num_pairs);
+      const PairTile tc = pair_tile<DX, NACC>(args, pair + lt * num_pairs);
       int64_t row, kl;
       if (!DX) {
-        row = tc.n0 + 128 * (int)rank + d;
+        row = tc.n0 + HALF_N * (int)rank + d;
         kl = kb;
       } else {
         row = (int64_t)kb * kBK + (d & 63);
-        kl = (tc.n0 + 128 * (int)rank) / 64 + (d >> 6);
+        kl = (tc.n0 + HALF_N * (int)rank) / 64 + (d >> 6);
       }
       valid = row < args.w_rows && kl < args.w_lines_per_row;
       return row * args.w_lines_per_row + kl;
     };
 
-    RawLine cur;
-    bool cur_valid = false;
-    if ((uint32_t)g < total) {
-      const int64_t ln = line_of((uint32_t)g, cur_valid);
-      if (cur_valid) load_line<FMT>(args.wv, ln, cur);
-    }
-    for (uint32_t it = (uint32_t)g; it < total; it += P_DQ_GROUPS) {
-      RawLine nxt;
-      bool nxt_valid = false;
-      if (it + P_DQ_GROUPS < total) {
-        const int64_t ln = line_of(it + P_DQ_GROUPS, nxt_valid);
-        if (nxt_valid) load_line<FMT>(args.wv, ln, nxt);
+    // Two raw lines in flight per thread: the bytes of item it + 2G are
+    // requested right after item it's stores are fenced and published (a
+    // proxy fence may wait for this thread's outstanding memory operations,
+    // so no load is in flight across it), and are decoded two items later.
+    auto fetch = [&](uint32_t it, RawLine& r) -> bool {
+      bool valid = false;
+      if (it < total) {
+        const int64_t ln = line_of(it, valid);
+        if (valid) load_line<FMT>(args.wv, ln, r);
       }
+      return valid;
+    };
+    auto process = [&](uint32_t it, const RawLine& r, bool valid) -> bool {
       const int s = it % P_STAGES;
       const uint32_t ph = (it / P_STAGES) & 1;
       bool ok = true;
       if (lane == 0) ok = mbar_wait_cluster(smem_u32(&bars->empty[s]), ph ^ 1, abort, args.err);
-      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) break;
-      const bool decode_item = (int)(it % (uint32_t)nkb_total) < nkb;
-      if (decode_item) {
+      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) return false;
+      if ((int)(it % (uint32_t)nkb_total) < nkb) {
         const uint32_t dst = sB0 + s * P_B_BYTES + soff;
-        if (cur_valid) {
+        if (valid) {
           uint4 out[8];
-          decode_line<FMT>(cur, out);
+          decode_line<FMT>(r, out);
 #pragma unroll
           for (int c = 0; c < 8; ++c) sts_v4(dst + ((c ^ swz) << 4), out[c]);
         } else {
@@ -313,8 +344,19 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(bready0 + s * 8);
-      cur = nxt;
-      cur_valid = nxt_valid;
+      return true;
+    };
+
+    RawLine ra, rb;
+    bool va = fetch((uint32_t)g, ra);
+    bool vb = fetch((uint32_t)g + P_DQ_GROUPS, rb);
+    for (uint32_t it = (uint32_t)g; it < total; it += 2 * P_DQ_GROUPS) {
+      if (!process(it, ra, va)) break;
+      va = fetch(it + 2 * P_DQ_GROUPS, ra);
+      const uint32_t it2 = it + P_DQ_GROUPS;
+      if (it2 >= total) break;
+      if (!process(it2, rb, vb)) break;
+      vb = fetch(it2 + 2 * P_DQ_GROUPS, rb);
     }
   }
 
@@ -328,9 +370,10 @@ __global__ void __launch_bounds__(p_threads<FMT>(), 1)
 }
 
 // ---------------------------------------------------------------------------
-template <int FMT, bool DX>
+template <int FMT, bool DX, int NACC>
 static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, cudaStream_t st) {
-  auto kern = qgemm_pair_kernel<FMT, DX>;
+  auto kern = qgemm_pair_kernel<FMT, DX, NACC>;
+  constexpr size_t P_SMEM_BYTES = p_smem_bytes<NACC>();
   static int max_clusters = -1;  // per instantiation
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -338,7 +381,7 @@ static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, c
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(p_threads<FMT>());
+  cfg.blockDim = dim3(p_threads<FMT, NACC>());
   cfg.dynamicSmemBytes = P_SMEM_BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -358,13 +401,18 @@ static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, c
   return cudaLaunchKernelEx(&cfg, kern, maps.a, maps.w, maps.la, maps.lb, args);
 }
 
+int pair_tile_rows(int fmt) { return fmt == FMT_BF16 ? PairCfg<1>::TM : PairCfg<2>::TM; }
+int pair_tile_cols(int fmt) { return fmt == FMT_BF16 ? PairCfg<1>::TN : PairCfg<2>::TN; }
+
+// bf16 bases: 256 x 256 tiles; quantised bases: 512 x 128 tiles (two
+// accumulators share every decoded weight tile).
 cudaError_t launch_qgemm_pair(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args, cudaStream_t st) {
   count_launch(1);
   switch (fmt) {
-    case FMT_BF16: return dx ? launch_pair_one<FMT_BF16, true>(maps, args, st) : launch_pair_one<FMT_BF16, false>(maps, args, st);
-    case FMT_NF4: return dx ? launch_pair_one<FMT_NF4, true>(maps, args, st) : launch_pair_one<FMT_NF4, false>(maps, args, st);
-    case FMT_Q8_0: return dx ? launch_pair_one<FMT_Q8_0, true>(maps, args, st) : launch_pair_one<FMT_Q8_0, false>(maps, args, st);
-    case FMT_Q4_0: return dx ? launch_pair_one<FMT_Q4_0, true>(maps, args, st) : launch_pair_one<FMT_Q4_0, false>(maps, args, st);
+    case FMT_BF16: return dx ? launch_pair_one<FMT_BF16, true, 1>(maps, args, st) : launch_pair_one<FMT_BF16, false, 1>(maps, args, st);
+    case FMT_NF4: return dx ? launch_pair_one<FMT_NF4, true, 2>(maps, args, st) : launch_pair_one<FMT_NF4, false, 2>(maps, args, st);
+    case FMT_Q8_0: return dx ? launch_pair_one<FMT_Q8_0, true, 2>(maps, args, st) : launch_pair_one<FMT_Q8_0, false, 2>(maps, args, st);
+    case FMT_Q4_0: return dx ? launch_pair_one<FMT_Q4_0, true, 2>(maps, args, st) : launch_pair_one<FMT_Q4_0, false, 2>(maps, args, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -98,9 +98,14 @@ struct GemmMaps {
 cudaError_t launch_qgemm(int fmt, bool dx, bool grouped, const GemmMaps& maps, const GemmArgs& args,
                          int num_sms, cudaStream_t st);
 
-// CTA-pair variant (gemm_pair.cu): 256 x 256 tiles, dense problems only.
-// Tensor-map boxes: A / adapter-A [64 x 128]; bf16 W and adapter-B
-// [64 x 128] forward, [64 x 64] for dX.  args.num_tiles counts 256-row tiles.
+// CTA-pair variant (gemm_pair.cu), dense problems only.  Tensor-map boxes:
+// A / adapter-A [64 x 128]; bf16 W and adapter-B [64 x tile_cols/2] forward,
+// [64 x 64] for dX.  args.num_tiles / num_n_blk count pair tiles.
 cudaError_t launch_qgemm_pair(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args, cudaStream_t st);
+// Output tile of the pair kernel for a base format: 256 x 256 (bf16) or
+// 512 x 128 (quantised).  Forward bf16-W and adapter-B maps use boxes of
+// pair_tile_cols / 2 rows.
+int pair_tile_rows(int fmt);
+int pair_tile_cols(int fmt);
 
 }  // namespace qlora

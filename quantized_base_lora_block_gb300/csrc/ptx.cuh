@@ -15,10 +15,11 @@ constexpr int kErrTimeout = -5;
 // a wait still open after 4 s means a broken protocol.
 constexpr uint64_t kWaitNs = 4000000000ull;
 constexpr uint64_t kDrainNs = 100000000ull;
-// Polls before a wait starts reading the global timer (a timer read is slow
-// enough to matter on a pipeline's critical path; legal waits end well
-// within these polls).
-constexpr uint32_t kFastPolls = 4096;
+// Each poll may suspend the thread in hardware for up to this long; it wakes
+// as soon as the phase completes.  Suspended threads issue no instructions,
+// so long waits (a whole tile for the epilogue) do not steal issue slots
+// from the decode warps.
+constexpr uint32_t kSuspendHintNs = 1000000;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -52,9 +53,9 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -64,19 +65,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // *err, the device error word, and raising this CTA's abort flag), or as soon
 // as another role of this CTA has raised the abort flag.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* err) {
-  // fast path: plain polls, no timer read on the critical path of a pipeline
-#pragma unroll 1
-  for (uint32_t i = 0; i < kFastPolls; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023) == 0) {
-      if (*abort) return false;
-      const uint64_t dt = globaltimer_ns() - t0;
-      if (dt > kWaitNs) break;
-      if (dt > 100000ull) __nanosleep(256);
-    }
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitNs) break;
   }
   if (err) atomicExch(err, kErrTimeout);
   *abort = 1;
@@ -230,10 +224,10 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -241,18 +235,12 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // Bounded wait (as mbar_wait) with cluster-scope acquire, for barriers that
 // the peer CTA arrives on.
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort, int* err) {
-#pragma unroll 1
-  for (uint32_t i = 0; i < kFastPolls; ++i)
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+  if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
+  for (;;) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((i & 1023) == 0) {
-      if (*abort) return false;
-      const uint64_t dt = globaltimer_ns() - t0;
-      if (dt > kWaitNs) break;
-      if (dt > 100000ull) __nanosleep(256);
-    }
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitNs) break;
   }
   if (err) atomicExch(err, kErrTimeout);
   *abort = 1;
