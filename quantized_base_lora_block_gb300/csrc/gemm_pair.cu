@@ -294,51 +294,67 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
     const uint32_t total = (uint32_t)my_tiles * (uint32_t)nkb_total;
     const uint32_t bready0 = mapa_shared(smem_u32(&bars->bready[0]), 0);
 
-    auto line_of = [&](uint32_t it, bool& valid) -> int64_t {
-      const int lt = (int)(it / (uint32_t)nkb_total), kb = (int)(it % (uint32_t)nkb_total);
-      valid = false;
-      if (kb >= nkb) return 0;  // adapter chunk: nothing to decode
-      const PairTile tc = pair_tile<DX, NACC>(args, pair + lt * num_pairs);
-      int64_t row, kl;
-      if (!DX) {
-        row = tc.n0 + HALF_N * (int)rank + d;
-        kl = kb;
-      } else {
-        row = (int64_t)kb * kBK + (d & 63);
-        kl = (tc.n0 + HALF_N * (int)rank) / 64 + (d >> 6);
-      }
-      valid = row < args.w_rows && kl < args.w_lines_per_row;
-      return row * args.w_lines_per_row + kl;
+    // Item iterator without divisions: (local tile, k-block) advance by
+    // GROUPS items per step; the tile's line base is recomputed only when the
+    // tile changes.
+    struct Cursor {
+      uint32_t it;
+      int kb, lt;
+      int64_t base;  // forward: first line of this thread's row; dX: k-line
+      bool row_ok;   // forward: weight row in range; dX: k-line in range
     };
-
-    // Two raw lines in flight per thread: the bytes of item it + 2G are
-    // requested right after item it's stores are fenced and published (a
-    // proxy fence may wait for this thread's outstanding memory operations,
-    // so no load is in flight across it), and are decoded two items later.
-    auto fetch = [&](uint32_t it, RawLine& r) -> bool {
-      bool valid = false;
-      if (it < total) {
-        const int64_t ln = line_of(it, valid);
-        if (valid) load_line<FMT>(args.wv, ln, r);
+    auto set_tile = [&](Cursor& c) {
+      if (c.lt >= my_tiles) return;
+      const PairTile tc = pair_tile<DX, NACC>(args, pair + c.lt * num_pairs);
+      if (!DX) {
+        const int64_t row = tc.n0 + HALF_N * (int)rank + d;
+        c.row_ok = row < args.w_rows;
+        c.base = row * args.w_lines_per_row;
+      } else {
+        const int64_t kl = (tc.n0 + HALF_N * (int)rank) / 64 + (d >> 6);
+        c.row_ok = kl < args.w_lines_per_row;
+        c.base = kl;
       }
+    };
+    auto advance = [&](Cursor& c, int n) {
+      c.it += n;
+      c.kb += n;
+      bool moved = false;
+      while (c.kb >= nkb_total) {
+        c.kb -= nkb_total;
+        ++c.lt;
+        moved = true;
+      }
+      if (moved) set_tile(c);
+    };
+    // line index and validity of the cursor's item (adapter chunk: invalid)
+    auto line_at = [&](const Cursor& c, bool& valid) -> int64_t {
+      valid = c.it < total && c.kb < nkb && c.row_ok;
+      if (!DX) return c.base + c.kb;
+      return ((int64_t)c.kb * kBK + (d & 63)) * args.w_lines_per_row + c.base;
+    };
+    auto fetch = [&](const Cursor& c, RawLine& r) -> bool {
+      bool valid;
+      const int64_t ln = line_at(c, valid);
+      if (valid) load_line<FMT>(args.wv, ln, r);
       return valid;
     };
-    auto process = [&](uint32_t it, const RawLine& r, bool valid) -> bool {
-      const int s = it % P_STAGES;
-      const uint32_t ph = (it / P_STAGES) & 1;
+    auto process = [&](const Cursor& c, const RawLine& r, bool valid) -> bool {
+      const int s = c.it % P_STAGES;
+      const uint32_t ph = (c.it / P_STAGES) & 1;
       bool ok = true;
       if (lane == 0) ok = mbar_wait_cluster(smem_u32(&bars->empty[s]), ph ^ 1, abort, args.err);
       if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) return false;
-      if ((int)(it % (uint32_t)nkb_total) < nkb) {
+      if (c.kb < nkb) {
         const uint32_t dst = sB0 + s * P_B_BYTES + soff;
         if (valid) {
           uint4 out[8];
           decode_line<FMT>(r, out);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) sts_v4(dst + ((c ^ swz) << 4), out[c]);
+          for (int q = 0; q < 8; ++q) sts_v4(dst + ((q ^ swz) << 4), out[q]);
         } else {
 #pragma unroll
-          for (int c = 0; c < 8; ++c) sts_v4(dst + (c << 4), make_uint4(0, 0, 0, 0));
+          for (int q = 0; q < 8; ++q) sts_v4(dst + (q << 4), make_uint4(0, 0, 0, 0));
         }
       }
       fence_proxy_async_smem();
@@ -347,16 +363,27 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
       return true;
     };
 
+    // cur: the item being processed; pre: the item whose bytes are loaded
+    // next (two items ahead of cur, so two lines are in flight per thread)
+    Cursor cur{0, 0, 0, 0, false};
+    set_tile(cur);
+    advance(cur, g);
+    Cursor pre = cur;
+    advance(pre, P_DQ_GROUPS);
     RawLine ra, rb;
-    bool va = fetch((uint32_t)g, ra);
-    bool vb = fetch((uint32_t)g + P_DQ_GROUPS, rb);
-    for (uint32_t it = (uint32_t)g; it < total; it += 2 * P_DQ_GROUPS) {
-      if (!process(it, ra, va)) break;
-      va = fetch(it + 2 * P_DQ_GROUPS, ra);
-      const uint32_t it2 = it + P_DQ_GROUPS;
-      if (it2 >= total) break;
-      if (!process(it2, rb, vb)) break;
-      vb = fetch(it2 + 2 * P_DQ_GROUPS, rb);
+    bool va = fetch(cur, ra);
+    bool vb = fetch(pre, rb);
+    advance(pre, P_DQ_GROUPS);
+    while (cur.it < total) {
+      if (!process(cur, ra, va)) break;
+      va = fetch(pre, ra);
+      advance(pre, P_DQ_GROUPS);
+      advance(cur, P_DQ_GROUPS);
+      if (cur.it >= total) break;
+      if (!process(cur, rb, vb)) break;
+      vb = fetch(pre, rb);
+      advance(pre, P_DQ_GROUPS);
+      advance(cur, P_DQ_GROUPS);
     }
   }
 
