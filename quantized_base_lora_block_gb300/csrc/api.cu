@@ -251,6 +251,13 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
   a.out = static_cast<__nv_bfloat16*>(out);
   a.wv = view_of(w);
   a.err = device_error_word();
+  // Tile order.  Forward: row blocks fastest while the activation fits in L2
+  // next to the streamed weight slabs (measured: gate 133 MB of DRAM traffic
+  // this way vs 234 MB the other way); beyond ~64 MB (e.g. the 14336-wide
+  // down projection) column blocks fastest, so each activation row block is
+  // read once (543 -> 253 MB).  dX: column blocks fastest, so each dY row
+  // block is read once.
+  a.n_fastest = dx ? 1 : ((double)M * (double)a.k_red * 2.0 > 64e6 ? 1 : 0);
   return gemm_launch(w->fmt, dx, pair, maps, a, st);
 }
 

@@ -81,16 +81,17 @@ struct PairTile {
   int m0, n0;
 };
 
-// forward: row blocks fastest (the activation block stays in L2 while the
-// weight slab streams); dX: column blocks fastest (the dY row block stays in
-// L2 while every output column block of it runs).
+// Tile order (chosen on the host): row blocks fastest keeps the whole A
+// operand hot in L2 while weight slabs stream; column blocks fastest keeps
+// the weight hot while A row blocks stream.  The smaller operand is the one
+// kept, so the larger one is read from DRAM once.
 template <bool DX, int NACC>
 __device__ __forceinline__ PairTile pair_tile(const GemmArgs& a, int t) {
   constexpr int TM = PairCfg<NACC>::TM, TN = PairCfg<NACC>::TN;
   const int num_m = (a.M + TM - 1) / TM;
   const int num_n = a.num_n_blk;
   PairTile p;
-  if (!DX) {
+  if (!a.n_fastest) {
     p.m0 = (t % num_m) * TM;
     p.n0 = (t / num_m) * TN;
   } else {

@@ -85,6 +85,7 @@ struct GemmArgs {
   const GroupTable* groups;  // device copy (grouped); dense uses wv below
   WeightView wv;
   int* err;              // device error word
+  int n_fastest;         // pair kernel tile order: 1 = output column blocks fastest
 };
 
 // Tensor maps: A operand [M x k_red] (X or dY), bf16 W (format BF16 only),
