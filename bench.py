@@ -53,6 +53,24 @@ def parse_args():
     return p.parse_args()
 
 
+def captured_traffic(wl):
+    """DRAM bytes per fused-GEMM launch from the committed ncu capture, or
+    None when the kernel sources changed since it was taken (or for another
+    workload)."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "qgemm_traffic_llama8b_nf4dq.json")
+    if wl.name != "llama31_8b_nf4dq" or not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    h = hashlib.sha256()
+    for src in d["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return d["traffic_bytes_per_launch"] if h.hexdigest() == d["sources_sha256"] else None
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -422,7 +440,7 @@ def main():
     peaks = measured_peaks()
     ach = gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else 0.0
     roofline = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                "frac": ach / peaks["bf16_sustained"], "traffic": None,
+                "frac": ach / peaks["bf16_sustained"], "traffic": captured_traffic(wl),
                 "kernel": "qgemm_kernel (fused decode + tcgen05 GEMM + adapter chunk), fwd and dX launches",
                 "peak_kind": f"{peaks['source']} sustained bf16",
                 "frac_of_burst": ach / peaks["bf16"], "frac_of_nominal_2250": ach / NOMINAL_BF16_TFLOPS,
