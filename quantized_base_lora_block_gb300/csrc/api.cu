@@ -237,6 +237,7 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
          map2d(&maps.lb, lb, K, rank, 64, 64);
     if (w->fmt == QLORA_FMT_BF16) ok = ok && map2d(&maps.w, w->data, K, N, 64, 64);
   }
+  if (pair) ok = ok && map2d(&maps.out, out, dx ? K : N, M, 64, 128);
   if (!ok) return cudaErrorInvalidValue;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));

@@ -64,12 +64,17 @@ struct __align__(8) PairBarriers {
   uint64_t acc_empty[2];                   // CTA 0: epilogue warps of both CTAs
   uint32_t tmem_base;
   int abort;
+  int ep_ok;  // epilogue: result of the "accumulator full" wait, for all 4 warps
 };
+
+// epilogue staging: one 128-row x 64-column bf16 chunk (128B-swizzled),
+// written out with a TMA tensor store
+constexpr int P_STAGE_OUT_BYTES = 128 * 64 * 2;
 
 template <int NACC>
 constexpr size_t p_smem_bytes() {
   return 1024 + (size_t)PairCfg<NACC>::STAGES * (PairCfg<NACC>::A_BYTES + PairCfg<NACC>::B_BYTES) +
-         sizeof(PairBarriers<NACC>);
+         P_STAGE_OUT_BYTES + sizeof(PairBarriers<NACC>);
 }
 
 template <int FMT, int NACC>
@@ -107,7 +112,7 @@ template <int FMT, bool DX, int NACC>
 __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
     qgemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_lb,
-                      const GemmArgs args) {
+                      const __grid_constant__ CUtensorMap tm_out, const GemmArgs args) {
   using Cfg = PairCfg<NACC>;
   constexpr int P_STAGES = Cfg::STAGES, P_A_BYTES = Cfg::A_BYTES, P_B_BYTES = Cfg::B_BYTES;
   constexpr int TN = Cfg::TN, HALF_N = Cfg::HALF_N;
@@ -115,7 +120,9 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sA0 = smem_u32(smem);
   const uint32_t sB0 = sA0 + P_STAGES * P_A_BYTES;
-  PairBarriers<NACC>* bars = reinterpret_cast<PairBarriers<NACC>*>(smem + P_STAGES * (P_A_BYTES + P_B_BYTES));
+  const uint32_t sOut = sB0 + P_STAGES * P_B_BYTES;  // 1024-aligned (stage sizes are multiples of 8 KB)
+  PairBarriers<NACC>* bars =
+      reinterpret_cast<PairBarriers<NACC>*>(smem + P_STAGES * (P_A_BYTES + P_B_BYTES) + P_STAGE_OUT_BYTES);
   volatile int* abort = &bars->abort;
 
   const uint32_t rank = cluster_ctarank();
@@ -140,6 +147,7 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc_pair(smem_u32(&bars->tmem_base), P_TMEM_COLS);
+  if (warp == 2 && lane == 0) prefetch_tmap(&tm_out);
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_a);
     if (FMT == FMT_BF16) prefetch_tmap(&tm_w);
@@ -243,44 +251,64 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
+    // Per 64-column chunk: each thread loads its row's 64 fp32 values from
+    // TMEM, converts them to bf16 and writes one 128-byte row of a
+    // 128B-swizzled staging tile (conflict-free); one thread then stores the
+    // 128 x 64 tile with a TMA tensor store (rows beyond M are not written).
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
+    const int ep = (warp - 2) * 32 + lane;  // 0..127
+    const uint32_t srow = sOut + (uint32_t)row_in_tile * 128;
+    const int swz = row_in_tile & 7;
     for (int lt = 0; lt < my_tiles; ++lt) {
       const PairTile tc = pair_tile<DX, NACC>(args, pair + lt * num_pairs);
       const uint32_t ab = lt & 1, aph = (lt >> 1) & 1;
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait_cluster(smem_u32(&bars->acc_full[ab]), aph, abort, args.err);
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      // one thread waits; all four warps take the same decision (they meet
+      // at named barriers below, which must never be left half-entered)
+      if (ep == 0) bars->ep_ok = mbar_wait_cluster(smem_u32(&bars->acc_full[ab]), aph, abort, args.err) ? 1 : 0;
+      named_bar(1, 128);
+      const bool ok = *reinterpret_cast<volatile int*>(&bars->ep_ok) != 0;
+      named_bar(1, 128);  // everyone has read ep_ok before it is rewritten
       if (!ok) break;
       tc_fence_after();
 #pragma unroll 1
       for (int a = 0; a < NACC; ++a) {
-        const int row = tc.m0 + 256 * a + 128 * (int)rank + row_in_tile;
-        const bool row_ok = row < args.M;
-        __nv_bfloat16* orow = args.out + (int64_t)row * args.n_out + tc.n0;
+        const int row0 = tc.m0 + 256 * a + 128 * (int)rank;
 #pragma unroll 1
-        for (int c = 0; c < TN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * 256 + a * TN + c * 32, v);
+        for (int c = 0; c < TN / 64; ++c) {
+          uint32_t v0[32], v1[32];
+          const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * 256 + a * TN + c * 64;
+          tmem_ld_32x32b_x32(tcol, v0);
+          tmem_ld_32x32b_x32(tcol + 32, v1);
           tc_wait_ld();
-          if (row_ok && tc.n0 + c * 32 < args.n_out) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          if (a == NACC - 1 && c == TN / 64 - 1) {
+            // every TMEM value of this buffer is in registers: release it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[ab]), 0));
+          }
+          if (ep == 0) bulk_wait_read0();  // staging tile free again
+          named_bar(1, 128);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-              o.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-              o.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-              o.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-              dst[q] = o;
-            }
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t* v = q < 4 ? v0 + 8 * q : v1 + 8 * (q - 4);
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+            o.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+            o.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+            o.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+            sts_v4(srow + ((q ^ swz) << 4), o);
+          }
+          fence_proxy_async_smem();
+          named_bar(1, 128);
+          if (ep == 0 && row0 < args.M && tc.n0 + 64 * c < args.n_out) {
+            tma_store_2d(&tm_out, sOut, tc.n0 + 64 * c, row0);
+            bulk_commit();
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[ab]), 0));
     }
+    if (ep == 0) bulk_wait0();
   } else if (FMT != FMT_BF16) {
     // ------------------------------------------------------------ decode
     // group g (GROUP_WARPS warps) handles the items with it % GROUPS == g;
@@ -426,7 +454,7 @@ static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, c
   const int pairs = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
   if (pairs <= 0) return cudaSuccess;
   cfg.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&cfg, kern, maps.a, maps.w, maps.la, maps.lb, args);
+  return cudaLaunchKernelEx(&cfg, kern, maps.a, maps.w, maps.la, maps.lb, maps.out, args);
 }
 
 int pair_tile_rows(int fmt) { return fmt == FMT_BF16 ? PairCfg<1>::TM : PairCfg<2>::TM; }

@@ -94,6 +94,7 @@ struct GemmArgs {
 // index outermost.
 struct GemmMaps {
   CUtensorMap a, w, la, lb;
+  CUtensorMap out;  // pair kernel: bf16 output [M x n_out], box [64 x 128] (TMA stores)
 };
 
 cudaError_t launch_qgemm(int fmt, bool dx, bool grouped, const GemmMaps& maps, const GemmArgs& args,
