@@ -447,6 +447,11 @@ def main():
                 "launches": gemm_n, "share_of_step": gemm_ms / ms if ms > 0 else None}
 
     # --------------------------------------------------------- end to end
+    # Every step copies its X and dY (pinned host) in and its dA, dB out.  The
+    # copies run on a copy stream into two alternating sets of device
+    # buffers, and each linear's compute waits only for its own inputs, so
+    # copies overlap the computation of earlier linears and of the previous
+    # step.
     e2e = None
     if not args.no_e2e:
         hX = [torch.empty(d["X"].shape, dtype=torch.bfloat16).pin_memory() for d in L]
@@ -459,27 +464,52 @@ def main():
         hdB = [torch.empty(d["dB"].shape, dtype=torch.float32).pin_memory() for d in L]
         h2d = sum(h.numel() * 2 for h in hX + hdY)
         d2h = sum(h.numel() * 4 for h in hdA + hdB)
+        sets = [[{"X": torch.empty_like(d["X"]), "dY": torch.empty_like(d["dY"])} for d in L] for _ in range(2)]
+        copy_stream = torch.cuda.Stream(dev)
+        n = len(L)
+        ev_x = [[torch.cuda.Event() for _ in range(n)] for _ in range(2)]
+        ev_y = [[torch.cuda.Event() for _ in range(n)] for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_done_used = [False, False]
 
-        def e2e_step():
-            for d, hx, hy in zip(L, hX, hdY):
-                d["X"].copy_(hx, non_blocking=True)
-                d["dY"].copy_(hy, non_blocking=True)
-            step()
-            for d, ha, hb in zip(L, hdA, hdB):
-                ha.copy_(d["dA"], non_blocking=True)
-                hb.copy_(d["dB"], non_blocking=True)
+        def e2e_step(k):
+            b = k % 2
+            with torch.cuda.stream(copy_stream):
+                if ev_done_used[b]:
+                    copy_stream.wait_event(ev_done[b])  # step k-2 finished with this set
+                for i in range(n):
+                    sets[b][i]["X"].copy_(hX[i], non_blocking=True)
+                    ev_x[b][i].record(copy_stream)
+                for i in reversed(range(n)):
+                    sets[b][i]["dY"].copy_(hdY[i], non_blocking=True)
+                    ev_y[b][i].record(copy_stream)
+            for i, d in enumerate(L):
+                stream.wait_event(ev_x[b][i])
+                q.linear_fwd(d["W"], sets[b][i]["X"], d["A"], d["B"], alpha, Y=d["Y"], T=d["T"], workspace=ws,
+                             stream=stream)
+            for i in reversed(range(n)):
+                d = L[i]
+                stream.wait_event(ev_y[b][i])
+                q.linear_bwd(d["W"], sets[b][i]["X"], d["A"], d["B"], d["T"], sets[b][i]["dY"], alpha, dX=d["dX"],
+                             dA=d["dA"], dB=d["dB"], workspace=ws, stream=stream)
+                hdA[i].copy_(d["dA"], non_blocking=True)
+                hdB[i].copy_(d["dB"], non_blocking=True)
+            ev_done[b].record(stream)
+            ev_done_used[b] = True
 
-        e2e_step()
+        e2e_step(0)
+        e2e_step(1)
         torch.cuda.synchronize()
         barrier(world)
         t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
+        for k in range(args.steps):
+            e2e_step(k)
         torch.cuda.synchronize()
         t_e2e = max_over_ranks(time.perf_counter() - t0, world)
         e2e = {"value": world * M * args.steps / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h,
-               "note": "pinned host X and dY copied in, dA and dB copied out, every step, same stream"}
+               "note": "pinned host X and dY copied in on a copy stream (double-buffered, overlapped with "
+                       "compute), dA and dB copied out, every step; wall clock"}
 
     # --------------------------------------------------------- other legs
     stream_res = None

@@ -35,33 +35,40 @@ namespace {
 
 constexpr int P_TMEM_COLS = 512;
 
-// Tile shape of the pair, by the number of accumulators NACC:
-//   NACC = 1: 256 x 256 (one M256 x N256 accumulator per buffer);
-//   NACC = 2: 512 x 128 (two M256 x N128 accumulators per buffer sharing
-//             every decoded B tile, which halves the decode work per flop).
-// Either way a buffer is 256 TMEM columns and two buffers fill TMEM.
-template <int NACC>
+// Tile configurations of the pair (CFG):
+//   1: 256 x 256, one M256 x N256 accumulator, two TMEM buffers (bf16 bases);
+//   2: 512 x 128, two M256 x N128 accumulators sharing every decoded B tile,
+//      two TMEM buffers;
+//   3: 512 x 256, two M256 x N256 accumulators sharing every decoded B tile,
+//      one TMEM buffer (all 512 columns): each accumulator is released as
+//      soon as the epilogue holds its values, so the next tile's MMAs into
+//      it can start while the previous tile is still being stored.
+// Decoding one B tile for two accumulators halves the decode work per flop.
+template <int CFG>
 struct PairCfg {
-  static constexpr int TM = 256 * NACC;                 // output rows per pair tile
-  static constexpr int TN = NACC == 1 ? 256 : 128;      // output columns per pair tile
-  static constexpr int HALF_N = TN / 2;                 // B rows (or columns) per CTA
-  static constexpr int A_BYTES = NACC * 128 * kBK * 2;  // this CTA's A rows
-  static constexpr int B_BYTES = HALF_N * kBK * 2;      // this CTA's half of B
-  static constexpr int STAGES = NACC == 1 ? 6 : 5;
-  static constexpr int LINES = HALF_N;                  // decoded 64-wide lines per stage per CTA
-  static constexpr int GROUP_WARPS = LINES / 32;        // one line per thread of a group
-  static constexpr int GROUPS = NACC == 1 ? 3 : 5;      // groups rotate over stages
+  static constexpr int NACC = CFG == 1 ? 1 : 2;           // accumulators per tile
+  static constexpr int TM = 256 * NACC;                   // output rows per pair tile
+  static constexpr int TN = CFG == 2 ? 128 : 256;         // output columns per pair tile
+  static constexpr int NBUF = NACC * TN <= 256 ? 2 : 1;   // TMEM buffers of NACC accumulators
+  static constexpr int HALF_N = TN / 2;                   // B rows (or columns) per CTA
+  static constexpr int A_BYTES = NACC * 128 * kBK * 2;    // this CTA's A rows
+  static constexpr int B_BYTES = HALF_N * kBK * 2;        // this CTA's half of B
+  static constexpr int STAGES = CFG == 1 ? 6 : (CFG == 2 ? 5 : 4);
+  static constexpr int LINES = HALF_N;                    // decoded 64-wide lines per stage per CTA
+  static constexpr int GROUP_WARPS = LINES / 32;          // one line per thread of a group
+  static constexpr int GROUPS = CFG == 1 ? 3 : (CFG == 2 ? 5 : 2);  // groups rotate over stages
   static constexpr int DQ_WARPS = GROUP_WARPS * GROUPS;
   static_assert(STAGES % GROUPS == 0, "a stage must always be decoded by the same group");
+  static_assert(NBUF * NACC * TN == 512, "accumulators fill TMEM");
 };
 
-template <int NACC>
+template <int CFG>
 struct __align__(8) PairBarriers {
-  uint64_t full[PairCfg<NACC>::STAGES];    // CTA 0: bytes of both CTAs' copies (CTA 1: unused)
-  uint64_t bready[PairCfg<NACC>::STAGES];  // CTA 0: decode warps of both CTAs
-  uint64_t empty[PairCfg<NACC>::STAGES];   // both: MMA completion (multicast)
-  uint64_t acc_full[2];                    // both: MMA completion (multicast)
-  uint64_t acc_empty[2];                   // CTA 0: epilogue warps of both CTAs
+  uint64_t full[PairCfg<CFG>::STAGES];    // CTA 0: bytes of both CTAs' copies (CTA 1: unused)
+  uint64_t bready[PairCfg<CFG>::STAGES];  // CTA 0: decode warps of both CTAs
+  uint64_t empty[PairCfg<CFG>::STAGES];   // both: MMA completion (multicast)
+  uint64_t acc_full[4];                   // per (buffer, accumulator): MMA completion (multicast)
+  uint64_t acc_empty[4];                  // CTA 0, per (buffer, accumulator): epilogue warps of both CTAs
   uint32_t tmem_base;
   int abort;
   int ep_ok;  // epilogue: result of the "accumulator full" wait, for all 4 warps
@@ -71,15 +78,15 @@ struct __align__(8) PairBarriers {
 // written out with a TMA tensor store
 constexpr int P_STAGE_OUT_BYTES = 128 * 64 * 2;
 
-template <int NACC>
+template <int CFG>
 constexpr size_t p_smem_bytes() {
-  return 1024 + (size_t)PairCfg<NACC>::STAGES * (PairCfg<NACC>::A_BYTES + PairCfg<NACC>::B_BYTES) +
-         P_STAGE_OUT_BYTES + sizeof(PairBarriers<NACC>);
+  return 1024 + (size_t)PairCfg<CFG>::STAGES * (PairCfg<CFG>::A_BYTES + PairCfg<CFG>::B_BYTES) +
+         P_STAGE_OUT_BYTES + sizeof(PairBarriers<CFG>);
 }
 
-template <int FMT, int NACC>
+template <int FMT, int CFG>
 constexpr int p_threads() {
-  return (FMT == FMT_BF16) ? 6 * 32 : (6 + PairCfg<NACC>::DQ_WARPS) * 32;
+  return (FMT == FMT_BF16) ? 6 * 32 : (6 + PairCfg<CFG>::DQ_WARPS) * 32;
 }
 
 struct PairTile {
@@ -90,9 +97,9 @@ struct PairTile {
 // operand hot in L2 while weight slabs stream; column blocks fastest keeps
 // the weight hot while A row blocks stream.  The smaller operand is the one
 // kept, so the larger one is read from DRAM once.
-template <bool DX, int NACC>
+template <bool DX, int CFG>
 __device__ __forceinline__ PairTile pair_tile(const GemmArgs& a, int t) {
-  constexpr int TM = PairCfg<NACC>::TM, TN = PairCfg<NACC>::TN;
+  constexpr int TM = PairCfg<CFG>::TM, TN = PairCfg<CFG>::TN;
   const int num_m = (a.M + TM - 1) / TM;
   const int num_n = a.num_n_blk;
   PairTile p;
@@ -108,21 +115,21 @@ __device__ __forceinline__ PairTile pair_tile(const GemmArgs& a, int t) {
 
 }  // namespace
 
-template <int FMT, bool DX, int NACC>
-__global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
+template <int FMT, bool DX, int CFG>
+__global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     qgemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_lb,
                       const __grid_constant__ CUtensorMap tm_out, const GemmArgs args) {
-  using Cfg = PairCfg<NACC>;
+  using Cfg = PairCfg<CFG>;
   constexpr int P_STAGES = Cfg::STAGES, P_A_BYTES = Cfg::A_BYTES, P_B_BYTES = Cfg::B_BYTES;
-  constexpr int TN = Cfg::TN, HALF_N = Cfg::HALF_N;
+  constexpr int TN = Cfg::TN, HALF_N = Cfg::HALF_N, NACC = Cfg::NACC, NBUF = Cfg::NBUF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sA0 = smem_u32(smem);
   const uint32_t sB0 = sA0 + P_STAGES * P_A_BYTES;
   const uint32_t sOut = sB0 + P_STAGES * P_B_BYTES;  // 1024-aligned (stage sizes are multiples of 8 KB)
-  PairBarriers<NACC>* bars =
-      reinterpret_cast<PairBarriers<NACC>*>(smem + P_STAGES * (P_A_BYTES + P_B_BYTES) + P_STAGE_OUT_BYTES);
+  PairBarriers<CFG>* bars =
+      reinterpret_cast<PairBarriers<CFG>*>(smem + P_STAGES * (P_A_BYTES + P_B_BYTES) + P_STAGE_OUT_BYTES);
   volatile int* abort = &bars->abort;
 
   const uint32_t rank = cluster_ctarank();
@@ -139,7 +146,7 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
       mbar_init(smem_u32(&bars->bready[s]), 2 * Cfg::GROUP_WARPS);  // one group's warps, both CTAs
       mbar_init(smem_u32(&bars->empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 4; ++b) {
       mbar_init(smem_u32(&bars->acc_full[b]), 1);
       mbar_init(smem_u32(&bars->acc_empty[b]), 8);
     }
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
     if (lane == 0) {
       uint32_t it = 0;
       for (int lt = 0; lt < my_tiles; ++lt) {
-        const PairTile tc = pair_tile<DX, NACC>(args, pair + lt * num_pairs);
+        const PairTile tc = pair_tile<DX, CFG>(args, pair + lt * num_pairs);
         const int am = tc.m0 + 128 * (int)rank;     // this CTA's A rows (+256 per accumulator)
         const int bn = tc.n0 + HALF_N * (int)rank;  // this CTA's half of B
         for (int kb = 0; kb < nkb_total; ++kb, ++it) {
@@ -216,12 +223,10 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
       constexpr uint32_t idesc = idesc_bf16_f32(256, TN, DX);
       uint32_t it = 0;
       for (int lt = 0; lt < my_tiles; ++lt) {
-        const uint32_t ab = lt & 1, aph = (lt >> 1) & 1;
-        if (!mbar_wait_cluster(smem_u32(&bars->acc_empty[ab]), aph ^ 1, abort, args.err)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + ab * 256;  // NACC accumulators of TN columns
+        const int buf = lt % NBUF;
+        const uint32_t aph = (lt / NBUF) & 1;
         bool ok = true;
-        for (int kb = 0; kb < nkb_total; ++kb, ++it) {
+        for (int kb = 0; kb < nkb_total && ok; ++kb, ++it) {
           const int s = it % P_STAGES;
           const uint32_t ph = (it / P_STAGES) & 1;
           if (!mbar_wait_cluster(smem_u32(&bars->full[s]), ph, abort, args.err)) { ok = false; break; }
@@ -239,14 +244,26 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
                                       : smem_desc_sw128(sb + kk * 32, 16, 1024);
 #pragma unroll
             for (int a = 0; a < NACC; ++a) {
+              if (kb == 0 && kk == 0) {
+                // the epilogue must have taken this accumulator's values
+                if (!mbar_wait_cluster(smem_u32(&bars->acc_empty[buf * NACC + a]), aph ^ 1, abort, args.err)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+              }
               const uint64_t adesc = smem_desc_sw128(sa + a * 16384 + kk * 32, 16, 1024);
-              tc_mma_bf16_pair(d_tmem + a * TN, adesc, bdesc, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+              tc_mma_bf16_pair(tmem_base + buf * (NACC * TN) + a * TN, adesc, bdesc, idesc,
+                               (kb > 0 || kk > 0) ? 1u : 0u);
             }
+            if (!ok) break;
           }
+          if (!ok) break;
           tc_commit_pair_mc(smem_u32(&bars->empty[s]));
         }
         if (!ok) break;
-        tc_commit_pair_mc(smem_u32(&bars->acc_full[ab]));
+#pragma unroll
+        for (int a = 0; a < NACC; ++a) tc_commit_pair_mc(smem_u32(&bars->acc_full[buf * NACC + a]));
       }
     }
   } else if (warp < 6) {
@@ -261,31 +278,34 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
     const uint32_t srow = sOut + (uint32_t)row_in_tile * 128;
     const int swz = row_in_tile & 7;
     for (int lt = 0; lt < my_tiles; ++lt) {
-      const PairTile tc = pair_tile<DX, NACC>(args, pair + lt * num_pairs);
-      const uint32_t ab = lt & 1, aph = (lt >> 1) & 1;
-      // one thread waits; all four warps take the same decision (they meet
-      // at named barriers below, which must never be left half-entered)
-      if (ep == 0) bars->ep_ok = mbar_wait_cluster(smem_u32(&bars->acc_full[ab]), aph, abort, args.err) ? 1 : 0;
-      named_bar(1, 128);
-      const bool ok = *reinterpret_cast<volatile int*>(&bars->ep_ok) != 0;
-      named_bar(1, 128);  // everyone has read ep_ok before it is rewritten
-      if (!ok) break;
-      tc_fence_after();
+      const PairTile tc = pair_tile<DX, CFG>(args, pair + lt * num_pairs);
+      const int buf = lt % NBUF;
+      const uint32_t aph = (lt / NBUF) & 1;
+      bool ok = true;
 #pragma unroll 1
-      for (int a = 0; a < NACC; ++a) {
+      for (int a = 0; a < NACC && ok; ++a) {
+        const int slot = buf * NACC + a;
+        // one thread waits; all four warps take the same decision (they meet
+        // at named barriers below, which must never be left half-entered)
+        if (ep == 0) bars->ep_ok = mbar_wait_cluster(smem_u32(&bars->acc_full[slot]), aph, abort, args.err) ? 1 : 0;
+        named_bar(1, 128);
+        ok = *reinterpret_cast<volatile int*>(&bars->ep_ok) != 0;
+        named_bar(1, 128);  // everyone has read ep_ok before it is rewritten
+        if (!ok) break;
+        tc_fence_after();
         const int row0 = tc.m0 + 256 * a + 128 * (int)rank;
 #pragma unroll 1
         for (int c = 0; c < TN / 64; ++c) {
           uint32_t v0[32], v1[32];
-          const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * 256 + a * TN + c * 64;
+          const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * (NACC * TN) + a * TN + c * 64;
           tmem_ld_32x32b_x32(tcol, v0);
           tmem_ld_32x32b_x32(tcol + 32, v1);
           tc_wait_ld();
-          if (a == NACC - 1 && c == TN / 64 - 1) {
-            // every TMEM value of this buffer is in registers: release it
+          if (c == TN / 64 - 1) {
+            // every value of this accumulator is in registers: release it
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[ab]), 0));
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[slot]), 0));
           }
           if (ep == 0) bulk_wait_read0();  // staging tile free again
           named_bar(1, 128);
@@ -307,6 +327,7 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
           }
         }
       }
+      if (!ok) break;
     }
     if (ep == 0) bulk_wait0();
   } else if (FMT != FMT_BF16) {
@@ -334,7 +355,7 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
     };
     auto set_tile = [&](Cursor& c) {
       if (c.lt >= my_tiles) return;
-      const PairTile tc = pair_tile<DX, NACC>(args, pair + c.lt * num_pairs);
+      const PairTile tc = pair_tile<DX, CFG>(args, pair + c.lt * num_pairs);
       if (!DX) {
         const int64_t row = tc.n0 + HALF_N * (int)rank + d;
         c.row_ok = row < args.w_rows;
@@ -426,10 +447,10 @@ __global__ void __launch_bounds__(p_threads<FMT, NACC>(), 1)
 }
 
 // ---------------------------------------------------------------------------
-template <int FMT, bool DX, int NACC>
+template <int FMT, bool DX, int CFG>
 static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, cudaStream_t st) {
-  auto kern = qgemm_pair_kernel<FMT, DX, NACC>;
-  constexpr size_t P_SMEM_BYTES = p_smem_bytes<NACC>();
+  auto kern = qgemm_pair_kernel<FMT, DX, CFG>;
+  constexpr size_t P_SMEM_BYTES = p_smem_bytes<CFG>();
   static int max_clusters = -1;  // per instantiation
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -437,7 +458,7 @@ static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, c
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(p_threads<FMT, NACC>());
+  cfg.blockDim = dim3(p_threads<FMT, CFG>());
   cfg.dynamicSmemBytes = P_SMEM_BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -457,18 +478,24 @@ static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, c
   return cudaLaunchKernelEx(&cfg, kern, maps.a, maps.w, maps.la, maps.lb, maps.out, args);
 }
 
-int pair_tile_rows(int fmt) { return fmt == FMT_BF16 ? PairCfg<1>::TM : PairCfg<2>::TM; }
-int pair_tile_cols(int fmt) { return fmt == FMT_BF16 ? PairCfg<1>::TN : PairCfg<2>::TN; }
+#ifndef QLORA_PAIR_QCFG
+#define QLORA_PAIR_QCFG 3
+#endif
+constexpr int kQuantCfg = QLORA_PAIR_QCFG;  // tile configuration for quantised bases
 
-// bf16 bases: 256 x 256 tiles; quantised bases: 512 x 128 tiles (two
+int pair_tile_rows(int fmt) { return fmt == FMT_BF16 ? PairCfg<1>::TM : PairCfg<kQuantCfg>::TM; }
+int pair_tile_cols(int fmt) { return fmt == FMT_BF16 ? PairCfg<1>::TN : PairCfg<kQuantCfg>::TN; }
+
+// bf16 bases: 256 x 256 tiles; quantised bases: 512 x 256 tiles (two
 // accumulators share every decoded weight tile).
 cudaError_t launch_qgemm_pair(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args, cudaStream_t st) {
   count_launch(1);
+  constexpr int Q = kQuantCfg;
   switch (fmt) {
     case FMT_BF16: return dx ? launch_pair_one<FMT_BF16, true, 1>(maps, args, st) : launch_pair_one<FMT_BF16, false, 1>(maps, args, st);
-    case FMT_NF4: return dx ? launch_pair_one<FMT_NF4, true, 2>(maps, args, st) : launch_pair_one<FMT_NF4, false, 2>(maps, args, st);
-    case FMT_Q8_0: return dx ? launch_pair_one<FMT_Q8_0, true, 2>(maps, args, st) : launch_pair_one<FMT_Q8_0, false, 2>(maps, args, st);
-    case FMT_Q4_0: return dx ? launch_pair_one<FMT_Q4_0, true, 2>(maps, args, st) : launch_pair_one<FMT_Q4_0, false, 2>(maps, args, st);
+    case FMT_NF4: return dx ? launch_pair_one<FMT_NF4, true, Q>(maps, args, st) : launch_pair_one<FMT_NF4, false, Q>(maps, args, st);
+    case FMT_Q8_0: return dx ? launch_pair_one<FMT_Q8_0, true, Q>(maps, args, st) : launch_pair_one<FMT_Q8_0, false, Q>(maps, args, st);
+    case FMT_Q4_0: return dx ? launch_pair_one<FMT_Q4_0, true, Q>(maps, args, st) : launch_pair_one<FMT_Q4_0, false, Q>(maps, args, st);
     default: return cudaErrorInvalidValue;
   }
 }
