@@ -226,6 +226,16 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
         const int buf = lt % NBUF;
         const uint32_t aph = (lt / NBUF) & 1;
         bool ok = true;
+        // the epilogue must have taken the buffer's values (double-buffered:
+        // a tile ago; single buffer: the epilogue releases each accumulator
+        // as soon as its values are in registers).  Waiting here rather than
+        // right before each accumulator's first MMA measured the same for
+        // the single buffer and 20% faster for bf16 tiles.
+#pragma unroll
+        for (int a = 0; a < NACC; ++a)
+          ok = ok && mbar_wait_cluster(smem_u32(&bars->acc_empty[buf * NACC + a]), aph ^ 1, abort, args.err);
+        if (!ok) break;
+        tc_fence_after();
         for (int kb = 0; kb < nkb_total && ok; ++kb, ++it) {
           const int s = it % P_STAGES;
           const uint32_t ph = (it / P_STAGES) & 1;
@@ -244,21 +254,11 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
                                       : smem_desc_sw128(sb + kk * 32, 16, 1024);
 #pragma unroll
             for (int a = 0; a < NACC; ++a) {
-              if (kb == 0 && kk == 0) {
-                // the epilogue must have taken this accumulator's values
-                if (!mbar_wait_cluster(smem_u32(&bars->acc_empty[buf * NACC + a]), aph ^ 1, abort, args.err)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-              }
               const uint64_t adesc = smem_desc_sw128(sa + a * 16384 + kk * 32, 16, 1024);
               tc_mma_bf16_pair(tmem_base + buf * (NACC * TN) + a * TN, adesc, bdesc, idesc,
                                (kb > 0 || kk > 0) ? 1u : 0u);
             }
-            if (!ok) break;
           }
-          if (!ok) break;
           tc_commit_pair_mc(smem_u32(&bars->empty[s]));
         }
         if (!ok) break;
