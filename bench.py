@@ -272,12 +272,22 @@ def stream_leg(q, torch, inputs, L_dev, wl, n_layers, steps, stream, resident_ms
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
     pool.close()
+    # one layer's copy alone, for context
+    dst = torch.empty(layer_bytes, dtype=torch.uint8, device="cuda")
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for h in hosts[:4]:
+        dst.copy_(h, non_blocking=True)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    alone = 4 * layer_bytes / (c0.elapsed_time(c1) / 1e3) / 1e9
+    del dst
     # every layer is copied for the forward pass and again for the backward
     # pass, except the two the forward pass leaves resident
     h2d = (2 * n_layers - 2) * layer_bytes
     return {"layers": n_layers, "slots": 2, "layer_bytes": layer_bytes, "ms_per_pass": ms,
             "value": M / (ms / n_layers / 1e3), "unit": "tokens/s per layer (fwd+bwd)",
-            "h2d_bytes_per_pass": h2d, "h2d_GBps": h2d / (ms / 1e3) / 1e9,
+            "h2d_bytes_per_pass": h2d, "h2d_GBps": h2d / (ms / 1e3) / 1e9, "h2d_alone_GBps": alone,
             "streamed_over_resident": ms / (n_layers * resident_ms_per_layer),
             "note": "pinned host -> 2-slot device pool, one layer ahead on the library's copy stream; "
                     "fwd 0..L-1 then bwd L-1..0; each layer's 7 bases in one blob"}
@@ -466,9 +476,13 @@ def main():
         d2h = sum(h.numel() * 4 for h in hdA + hdB)
         sets = [[{"X": torch.empty_like(d["X"]), "dY": torch.empty_like(d["dY"])} for d in L] for _ in range(2)]
         copy_stream = torch.cuda.Stream(dev)
+        out_stream = torch.cuda.Stream(dev)
         n = len(L)
         ev_x = [[torch.cuda.Event() for _ in range(n)] for _ in range(2)]
         ev_y = [[torch.cuda.Event() for _ in range(n)] for _ in range(2)]
+        ev_g = [torch.cuda.Event() for _ in range(n)]     # gradients of linear i written
+        ev_out = [torch.cuda.Event() for _ in range(n)]   # gradients of linear i copied out
+        ev_out_used = [False] * n
         ev_done = [torch.cuda.Event() for _ in range(2)]
         ev_done_used = [False, False]
 
@@ -490,10 +504,17 @@ def main():
             for i in reversed(range(n)):
                 d = L[i]
                 stream.wait_event(ev_y[b][i])
+                if ev_out_used[i]:
+                    stream.wait_event(ev_out[i])  # the previous step's dA, dB of linear i are out
                 q.linear_bwd(d["W"], sets[b][i]["X"], d["A"], d["B"], d["T"], sets[b][i]["dY"], alpha, dX=d["dX"],
                              dA=d["dA"], dB=d["dB"], workspace=ws, stream=stream)
-                hdA[i].copy_(d["dA"], non_blocking=True)
-                hdB[i].copy_(d["dB"], non_blocking=True)
+                ev_g[i].record(stream)
+                with torch.cuda.stream(out_stream):
+                    out_stream.wait_event(ev_g[i])
+                    hdA[i].copy_(d["dA"], non_blocking=True)
+                    hdB[i].copy_(d["dB"], non_blocking=True)
+                    ev_out[i].record(out_stream)
+                    ev_out_used[i] = True
             ev_done[b].record(stream)
             ev_done_used[b] = True
 
@@ -506,10 +527,19 @@ def main():
             e2e_step(k)
         torch.cuda.synchronize()
         t_e2e = max_over_ranks(time.perf_counter() - t0, world)
+        # the host -> device copies of one step alone, for context
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(copy_stream):
+            c0.record(copy_stream)
+            for i in range(n):
+                sets[0][i]["X"].copy_(hX[i], non_blocking=True)
+                sets[0][i]["dY"].copy_(hdY[i], non_blocking=True)
+            c1.record(copy_stream)
+        torch.cuda.synchronize()
         e2e = {"value": world * M * args.steps / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h,
+               "d2h_bytes_per_step": d2h, "h2d_alone_GBps": h2d / (c0.elapsed_time(c1) / 1e3) / 1e9,
                "note": "pinned host X and dY copied in on a copy stream (double-buffered, overlapped with "
-                       "compute), dA and dB copied out, every step; wall clock"}
+                       "compute), dA and dB copied out on a third stream, every step; wall clock"}
 
     # --------------------------------------------------------- other legs
     stream_res = None

@@ -142,29 +142,24 @@ static WeightView view_of(const qlora_weight_desc* w) {
 struct DenseLayout {
   size_t act_off, act_bytes;  // sT or sU, bf16 [M x r]
   size_t u_off, u_bytes;      // U, fp32 [M x r] (backward)
-  size_t part_off, part_bytes;
-  SplitPlan t, u, db, da;
+  int64_t db_tiles, da_tiles;
+  SplitPlan t, u, c;          // T = X A^T, U = dY B, and dB / dA (one launch)
   size_t total;
 };
 
 static DenseLayout dense_layout(int64_t M, int64_t N, int64_t K, int r) {
   DenseLayout L;
-  const int64_t mt = (M + 63) / 64;
-  L.t = plan_split(mt, K);
-  L.u = plan_split(mt, N);
-  L.db = plan_split(N / 64, M);
-  L.da = plan_split(K / 64, M);
+  const int64_t row_tiles = (M + 63) / 64;
+  L.db_tiles = N / 64;
+  L.da_tiles = K / 64;
+  L.t = plan_split_fin(row_tiles, K);
+  L.u = plan_split_fin(row_tiles, N);
+  L.c = plan_split_fin(L.db_tiles + L.da_tiles, M);
   L.act_off = 0;
   L.act_bytes = round256((size_t)M * r * 2);
   L.u_off = L.act_off + L.act_bytes;
   L.u_bytes = round256((size_t)M * r * 4);
-  size_t p = (size_t)L.t.splits * M * r;
-  p = std::max(p, (size_t)L.u.splits * M * r);
-  p = std::max(p, (size_t)L.db.splits * N * r * 2);  // hi/lo halves
-  p = std::max(p, (size_t)L.da.splits * K * r * 2);
-  L.part_off = L.u_off + L.u_bytes;
-  L.part_bytes = round256(p * 4);
-  L.total = L.part_off + L.part_bytes;
+  L.total = L.u_off + L.u_bytes;
   return L;
 }
 
@@ -192,12 +187,13 @@ static cudaEvent_t prof_event() {
 }
 
 // Launch the fused GEMM, bracketed by events when instrumentation is on.
-static cudaError_t gemm_dispatch(int fmt, bool dx, bool pair, const GemmMaps& maps, const GemmArgs& a,
+// pair: 0 = one CTA per tile, else the pair kernel's tile configuration.
+static cudaError_t gemm_dispatch(int fmt, bool dx, int pair, const GemmMaps& maps, const GemmArgs& a,
                                 cudaStream_t st) {
-  return pair ? launch_qgemm_pair(fmt, dx, maps, a, st) : launch_qgemm(fmt, dx, false, maps, a, sm_count(), st);
+  return pair ? launch_qgemm_pair(fmt, dx, pair, maps, a, st) : launch_qgemm(fmt, dx, false, maps, a, sm_count(), st);
 }
 
-static cudaError_t gemm_launch(int fmt, bool dx, bool pair, const GemmMaps& maps, const GemmArgs& a,
+static cudaError_t gemm_launch(int fmt, bool dx, int pair, const GemmMaps& maps, const GemmArgs& a,
                                cudaStream_t st) {
   std::unique_lock<std::mutex> g(g_prof_mu);
   if (!g_prof_on) {
@@ -221,9 +217,10 @@ static cudaError_t gemm_launch(int fmt, bool dx, bool pair, const GemmMaps& maps
 static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M, int rank, const void* a_op,
                                   const void* la, const void* lb, void* out, cudaStream_t st) {
   const int64_t N = w->N, K = w->K;
-  const bool pair = M > kBM;  // pair tiles on an SM pair; short problems use one CTA per 128 x 256 tile
-  const int tile_rows = pair ? pair_tile_rows(w->fmt) : kBM;
-  const int tile_cols = pair ? pair_tile_cols(w->fmt) : kBN;
+  // pair tiles on an SM pair; short problems use one CTA per 128 x 256 tile
+  const int pair = M > kBM ? pair_cfg(w->fmt, M, dx ? K : N, sm_count()) : 0;
+  const int tile_rows = pair ? pair_tile_rows(pair) : kBM;
+  const int tile_cols = pair ? pair_tile_cols(pair) : kBN;
   const uint32_t brows = pair ? (uint32_t)(tile_cols / 2) : 256;
   GemmMaps maps;
   std::memset(&maps, 0, sizeof(maps));
@@ -316,8 +313,8 @@ static void build_grouped_plan(const qlora_weight_desc* ex, int E, const int32_t
     for (int i = 0; i < c; i += kChunkRows) P.cr.push_back(make_int4(e, lo + i, lo + std::min(c, i + kChunkRows), 0));
   }
   P.cf[E] = (int)P.cr.size();
-  P.t = plan_split((int64_t)std::max<size_t>(P.rr.size(), 1), P.K);
-  P.u = plan_split((int64_t)std::max<size_t>(P.rr.size(), 1), P.N);
+  P.t = plan_split_fin((int64_t)std::max<size_t>(P.rr.size(), 1), P.K);
+  P.u = plan_split_fin((int64_t)std::max<size_t>(P.rr.size(), 1), P.N);
   size_t o = 0;
   P.off_table = o;
   o = round256(o + sizeof(WeightView) * E);
@@ -513,15 +510,20 @@ int32_t qlora_linear_fwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   __nv_bfloat16* sT = reinterpret_cast<__nv_bfloat16*>(ws + L.act_off);
-  float* part = reinterpret_cast<float*>(ws + L.part_off);
   const float s = alpha / (float)rank;
 
-  // 1) T = X A^T (split over K), T_save = bf16(T), sT = bf16(s T)
-  cudaError_t e = launch_row_reduce(static_cast<const __nv_bfloat16*>(X), M, K,
-                                    static_cast<const __nv_bfloat16*>(A), rank, true, part, L.t, st);
-  if (e != cudaSuccess) return QLORA_ERR_CUDA;
-  e = launch_fin_rows(part, L.t.splits, M, rank, s, static_cast<float*>(T_save), sT, st);
-  if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  // 1) T = X A^T (split over K): T_save = T (fp32), sT = bf16(s T)
+  RowReduce rt;
+  rt.L = static_cast<const __nv_bfloat16*>(X);
+  rt.S = static_cast<const __nv_bfloat16*>(A);
+  rt.s_qj = 1;
+  rt.P = M;
+  rt.J = K;
+  rt.sp = L.t;
+  rt.scale = s;
+  rt.out_f32 = T_save;
+  rt.out_scaled = sT;
+  if (launch_row_reduce_fin(rt, rank, st) != cudaSuccess) return QLORA_ERR_CUDA;
 
   // 2) Y = X deq(W)^T + sT B^T
   return cuda_status(run_dense_gemm(w, false, M, rank, X, sT, B, Y, st));
@@ -552,30 +554,46 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   __nv_bfloat16* sU = reinterpret_cast<__nv_bfloat16*>(ws + L.act_off);
   float* U = reinterpret_cast<float*>(ws + L.u_off);
-  float* part = reinterpret_cast<float*>(ws + L.part_off);
   const float s = alpha / (float)rank;
   const __nv_bfloat16* Xb = static_cast<const __nv_bfloat16*>(X);
   const __nv_bfloat16* dYb = static_cast<const __nv_bfloat16*>(dY);
 
   // 1) U = dY B (split over N): U fp32, sU = bf16(s U)
-  cudaError_t e = launch_row_reduce(dYb, M, N, static_cast<const __nv_bfloat16*>(B), rank, false, part, L.u, st);
-  if (e == cudaSuccess) e = launch_fin_rows(part, L.u.splits, M, rank, s, U, sU, st);
-  // 2) dB = s dY^T T (split over M)
-  if (e == cudaSuccess)
-    e = launch_col_reduce(dYb, M, N, static_cast<const float*>(T_save), rank, part, L.db, st);
-  if (e == cudaSuccess) e = launch_fin_cols(part, L.db.splits, N, rank, s, dB, false, st);
-  if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  RowReduce ru;
+  ru.L = dYb;
+  ru.S = static_cast<const __nv_bfloat16*>(B);
+  ru.s_qj = 0;
+  ru.P = M;
+  ru.J = N;
+  ru.sp = L.u;
+  ru.scale = s;
+  ru.out_f32 = U;
+  ru.out_scaled = sU;
+  if (launch_row_reduce_fin(ru, rank, st) != cudaSuccess) return QLORA_ERR_CUDA;
 
-  // 3) dX = dY deq(W) + sU A
-  if (dX) {
-    e = run_dense_gemm(w, true, M, rank, dY, sU, A, dX, st);
-    if (e != cudaSuccess) return QLORA_ERR_CUDA;
-  }
+  // 2) dX = dY deq(W) + sU A
+  if (dX && run_dense_gemm(w, true, M, rank, dY, sU, A, dX, st) != cudaSuccess) return QLORA_ERR_CUDA;
 
-  // 4) dA = s U^T X (split over M), computed as dA^T [K x r] then transposed
-  e = launch_col_reduce(Xb, M, K, U, rank, part, L.da, st);
-  if (e == cudaSuccess) e = launch_fin_cols(part, L.da.splits, K, rank, s, dA, true, st);
-  return cuda_status(e);
+  // 3) dB = s dY^T T and dA = s U^T X (split over M, one launch); dA is
+  //    reduced as dA^T [K x r] and written transposed
+  ColReduce cb;
+  cb.L = dYb;
+  cb.S = T_save;
+  cb.P = M;
+  cb.J = N;
+  cb.sp = L.c;
+  cb.tiles = (int)L.db_tiles;
+  cb.scale = s;
+  cb.out = dB;
+  cb.transposed = 0;
+  ColReduce ca = cb;
+  ca.L = Xb;
+  ca.S = U;
+  ca.J = K;
+  ca.tiles = (int)L.da_tiles;
+  ca.out = dA;
+  ca.transposed = 1;
+  return cuda_status(launch_col_reduce_fin(cb, &ca, rank, st));
 }
 
 size_t qlora_grouped_workspace_bytes(const qlora_weight_desc* experts, int32_t E, const int32_t* offsets,

@@ -483,21 +483,46 @@ static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, c
 #endif
 constexpr int kQuantCfg = QLORA_PAIR_QCFG;  // tile configuration for quantised bases
 
-int pair_tile_rows(int fmt) { return fmt == FMT_BF16 ? PairCfg<1>::TM : PairCfg<kQuantCfg>::TM; }
-int pair_tile_cols(int fmt) { return fmt == FMT_BF16 ? PairCfg<1>::TN : PairCfg<kQuantCfg>::TN; }
+int pair_tile_rows(int cfg) { return cfg == 1 ? PairCfg<1>::TM : (cfg == 2 ? PairCfg<2>::TM : PairCfg<3>::TM); }
+int pair_tile_cols(int cfg) { return cfg == 1 ? PairCfg<1>::TN : (cfg == 2 ? PairCfg<2>::TN : PairCfg<3>::TN); }
 
-// bf16 bases: 256 x 256 tiles; quantised bases: 512 x 256 tiles (two
-// accumulators share every decoded weight tile).
-cudaError_t launch_qgemm_pair(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args, cudaStream_t st) {
-  count_launch(1);
-  constexpr int Q = kQuantCfg;
+// Quantised bases take 512 x 256 tiles (two accumulators share every decoded
+// weight tile) unless the launch has so few of them that the 512 x 128 tiling
+// finishes sooner: it has twice the tiles, each half the work, at ~0.8 of the
+// 512 x 256 tile's efficiency (measured on the Llama gate shape: 905 vs
+// 1104 TF/s).  Estimated time = waves of tiles x time of one tile.
+int pair_cfg(int fmt, int64_t M, int64_t n_out, int num_sms) {
+  if (fmt == FMT_BF16) return 1;
+  if (kQuantCfg != 3) return kQuantCfg;
+  const int64_t pairs = num_sms / 2 > 0 ? num_sms / 2 : 1;
+  const int64_t rows = (M + PairCfg<3>::TM - 1) / PairCfg<3>::TM;
+  const int64_t t3 = rows * ((n_out + PairCfg<3>::TN - 1) / PairCfg<3>::TN);
+  const int64_t t2 = rows * ((n_out + PairCfg<2>::TN - 1) / PairCfg<2>::TN);
+  const double cost3 = (double)((t3 + pairs - 1) / pairs);
+  const double cost2 = (double)((t2 + pairs - 1) / pairs) * 0.5 / 0.8;
+  return cost2 < 0.9 * cost3 ? 2 : 3;
+}
+
+template <int CFG>
+static cudaError_t launch_quant(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args, cudaStream_t st) {
   switch (fmt) {
-    case FMT_BF16: return dx ? launch_pair_one<FMT_BF16, true, 1>(maps, args, st) : launch_pair_one<FMT_BF16, false, 1>(maps, args, st);
-    case FMT_NF4: return dx ? launch_pair_one<FMT_NF4, true, Q>(maps, args, st) : launch_pair_one<FMT_NF4, false, Q>(maps, args, st);
-    case FMT_Q8_0: return dx ? launch_pair_one<FMT_Q8_0, true, Q>(maps, args, st) : launch_pair_one<FMT_Q8_0, false, Q>(maps, args, st);
-    case FMT_Q4_0: return dx ? launch_pair_one<FMT_Q4_0, true, Q>(maps, args, st) : launch_pair_one<FMT_Q4_0, false, Q>(maps, args, st);
+    case FMT_NF4: return dx ? launch_pair_one<FMT_NF4, true, CFG>(maps, args, st) : launch_pair_one<FMT_NF4, false, CFG>(maps, args, st);
+    case FMT_Q8_0: return dx ? launch_pair_one<FMT_Q8_0, true, CFG>(maps, args, st) : launch_pair_one<FMT_Q8_0, false, CFG>(maps, args, st);
+    case FMT_Q4_0: return dx ? launch_pair_one<FMT_Q4_0, true, CFG>(maps, args, st) : launch_pair_one<FMT_Q4_0, false, CFG>(maps, args, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_qgemm_pair(int fmt, bool dx, int cfg, const GemmMaps& maps, const GemmArgs& args,
+                              cudaStream_t st) {
+  count_launch(1);
+  if (fmt == FMT_BF16) {
+    if (cfg != 1) return cudaErrorInvalidValue;
+    return dx ? launch_pair_one<FMT_BF16, true, 1>(maps, args, st) : launch_pair_one<FMT_BF16, false, 1>(maps, args, st);
+  }
+  if (cfg == 2) return launch_quant<2>(fmt, dx, maps, args, st);
+  if (cfg == 3) return launch_quant<3>(fmt, dx, maps, args, st);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace qlora

@@ -39,6 +39,56 @@ inline SplitPlan plan_split(int64_t outer_tiles, int64_t red_len) {
   return p;
 }
 
+// Splits of the reductions that finish their sums in the kernel (reduce.cu):
+// the splits of one output tile form one thread-block cluster, so at most
+// kMaxClusterSplits; at most one wave of kSplitTargetCtas CTAs; at least two
+// 64-wide chunks per split.
+constexpr int kMaxClusterSplits = 8;
+inline SplitPlan plan_split_fin(int64_t outer_tiles, int64_t red_len) {
+  const int64_t red_tiles = (red_len + 63) / 64;
+  int64_t s = kSplitTargetCtas / (outer_tiles > 0 ? outer_tiles : 1);
+  if (s > red_tiles / 2) s = red_tiles / 2;
+  if (s > kMaxClusterSplits) s = kMaxClusterSplits;
+  if (s < 1) s = 1;
+  const int64_t per = (red_tiles + s - 1) / s;
+  SplitPlan p;
+  p.chunk = per * 64;
+  p.splits = (int)((red_tiles + per - 1) / per);
+  if (p.splits < 1) p.splits = 1;
+  return p;
+}
+
+// Row reduce out[p, q] = sum_j L[p, j] S(j, q), L [P x J] bf16, S [Q x J]
+// (s_qj) or [J x Q] bf16; out_f32 = v and / or out_scaled = bf16(scale v)
+// ([P x Q] each).
+struct RowReduce {
+  const __nv_bfloat16* L;
+  const __nv_bfloat16* S;
+  int s_qj;
+  int64_t P, J;
+  SplitPlan sp;
+  float scale;
+  float* out_f32;
+  __nv_bfloat16* out_scaled;
+};
+// Column reduce out[j, q] = scale sum_p L[p, j] S[p, q], L [P x J] bf16
+// (J a multiple of 64), S [P x Q] fp32; tiles = J / 64; out [J x Q], or
+// [Q x J] when transposed.
+struct ColReduce {
+  const __nv_bfloat16* L;
+  const float* S;
+  int64_t P, J;
+  SplitPlan sp;
+  int tiles;
+  float scale;
+  float* out;
+  int transposed;
+};
+cudaError_t launch_row_reduce_fin(const RowReduce& r, int Q, cudaStream_t st);
+// One launch for one or two column reductions with the same split plan (b
+// may be null).
+cudaError_t launch_col_reduce_fin(const ColReduce& a, const ColReduce* b, int Q, cudaStream_t st);
+
 // tiles / chunks: optional grouped-row lists (see skinny.cu); null for dense.
 cudaError_t launch_row_reduce(const __nv_bfloat16* L, int64_t P, int64_t J, const __nv_bfloat16* S, int Q,
                               bool s_qj, float* partial, const SplitPlan& sp, cudaStream_t st,
@@ -103,11 +153,15 @@ cudaError_t launch_qgemm(int fmt, bool dx, bool grouped, const GemmMaps& maps, c
 // CTA-pair variant (gemm_pair.cu), dense problems only.  Tensor-map boxes:
 // A / adapter-A [64 x 128]; bf16 W and adapter-B [64 x tile_cols/2] forward,
 // [64 x 64] for dX.  args.num_tiles / num_n_blk count pair tiles.
-cudaError_t launch_qgemm_pair(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args, cudaStream_t st);
-// Output tile of the pair kernel for a base format: 256 x 256 (bf16) or
-// 512 x 128 (quantised).  Forward bf16-W and adapter-B maps use boxes of
-// pair_tile_cols / 2 rows.
-int pair_tile_rows(int fmt);
-int pair_tile_cols(int fmt);
+// Tile configurations: 1 = 256 x 256 (bf16 bases), 3 = 512 x 256 (quantised
+// bases), 2 = 512 x 128 (quantised bases, for launches whose 512 x 256 tiles
+// would leave most SM pairs idle).
+int pair_cfg(int fmt, int64_t M, int64_t n_out, int num_sms);
+cudaError_t launch_qgemm_pair(int fmt, bool dx, int cfg, const GemmMaps& maps, const GemmArgs& args,
+                              cudaStream_t st);
+// Output tile of a configuration.  Forward bf16-W and adapter-B maps use
+// boxes of pair_tile_cols / 2 rows.
+int pair_tile_rows(int cfg);
+int pair_tile_cols(int cfg);
 
 }  // namespace qlora
