@@ -141,7 +141,8 @@ static WeightView view_of(const qlora_weight_desc* w) {
 // ------------------------------------------------------- workspace layout ---
 struct DenseLayout {
   size_t act_off, act_bytes;  // sT or sU, bf16 [M x r]
-  size_t u_off, u_bytes;      // U, fp32 [M x r] (backward)
+  size_t u_off, u_bytes;      // U as hi/lo bf16 [M x 2r] (backward)
+  size_t t_off, t_bytes;      // T as hi/lo bf16 [M x 2r] (backward)
   int64_t db_tiles, da_tiles;
   SplitPlan t, u, c;          // T = X A^T, U = dY B, and dB / dA (one launch)
   size_t total;
@@ -159,7 +160,9 @@ static DenseLayout dense_layout(int64_t M, int64_t N, int64_t K, int r) {
   L.act_bytes = round256((size_t)M * r * 2);
   L.u_off = L.act_off + L.act_bytes;
   L.u_bytes = round256((size_t)M * r * 4);
-  L.total = L.u_off + L.u_bytes;
+  L.t_off = L.u_off + L.u_bytes;
+  L.t_bytes = round256((size_t)M * r * 4);
+  L.total = L.t_off + L.t_bytes;
   return L;
 }
 
@@ -523,6 +526,9 @@ int32_t qlora_linear_fwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   rt.scale = s;
   rt.out_f32 = T_save;
   rt.out_scaled = sT;
+  rt.out_hilo = nullptr;
+  rt.aux_src = nullptr;
+  rt.aux_hilo = nullptr;
   if (launch_row_reduce_fin(rt, rank, st) != cudaSuccess) return QLORA_ERR_CUDA;
 
   // 2) Y = X deq(W)^T + sT B^T
@@ -553,12 +559,14 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   __nv_bfloat16* sU = reinterpret_cast<__nv_bfloat16*>(ws + L.act_off);
-  float* U = reinterpret_cast<float*>(ws + L.u_off);
+  __nv_bfloat16* U2 = reinterpret_cast<__nv_bfloat16*>(ws + L.u_off);
+  __nv_bfloat16* T2 = reinterpret_cast<__nv_bfloat16*>(ws + L.t_off);
   const float s = alpha / (float)rank;
   const __nv_bfloat16* Xb = static_cast<const __nv_bfloat16*>(X);
   const __nv_bfloat16* dYb = static_cast<const __nv_bfloat16*>(dY);
 
-  // 1) U = dY B (split over N): U fp32, sU = bf16(s U)
+  // 1) U = dY B (split over N): sU = bf16(s U) for the dX GEMM, U and T_save
+  //    as hi/lo bf16 pairs for the dA / dB reductions
   RowReduce ru;
   ru.L = dYb;
   ru.S = static_cast<const __nv_bfloat16*>(B);
@@ -567,8 +575,11 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   ru.J = N;
   ru.sp = L.u;
   ru.scale = s;
-  ru.out_f32 = U;
+  ru.out_f32 = nullptr;
   ru.out_scaled = sU;
+  ru.out_hilo = U2;
+  ru.aux_src = T_save;
+  ru.aux_hilo = T2;
   if (launch_row_reduce_fin(ru, rank, st) != cudaSuccess) return QLORA_ERR_CUDA;
 
   // 2) dX = dY deq(W) + sU A
@@ -578,7 +589,7 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   //    reduced as dA^T [K x r] and written transposed
   ColReduce cb;
   cb.L = dYb;
-  cb.S = T_save;
+  cb.S2 = T2;
   cb.P = M;
   cb.J = N;
   cb.sp = L.c;
@@ -588,7 +599,7 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   cb.transposed = 0;
   ColReduce ca = cb;
   ca.L = Xb;
-  ca.S = U;
+  ca.S2 = U2;
   ca.J = K;
   ca.tiles = (int)L.da_tiles;
   ca.out = dA;

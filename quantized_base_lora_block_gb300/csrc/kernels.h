@@ -59,8 +59,10 @@ inline SplitPlan plan_split_fin(int64_t outer_tiles, int64_t red_len) {
 }
 
 // Row reduce out[p, q] = sum_j L[p, j] S(j, q), L [P x J] bf16, S [Q x J]
-// (s_qj) or [J x Q] bf16; out_f32 = v and / or out_scaled = bf16(scale v)
-// ([P x Q] each).
+// (s_qj) or [J x Q] bf16.  Outputs (each optional): out_f32 = v [P x Q],
+// out_scaled = bf16(scale v) [P x Q], out_hilo = (bf16(v), bf16(v - bf16(v)))
+// side by side [P x 2Q]; and aux_hilo = the same split of aux_src [P x Q]
+// fp32, an independent array converted on the way.
 struct RowReduce {
   const __nv_bfloat16* L;
   const __nv_bfloat16* S;
@@ -70,13 +72,17 @@ struct RowReduce {
   float scale;
   float* out_f32;
   __nv_bfloat16* out_scaled;
+  __nv_bfloat16* out_hilo;
+  const float* aux_src;
+  __nv_bfloat16* aux_hilo;
 };
 // Column reduce out[j, q] = scale sum_p L[p, j] S[p, q], L [P x J] bf16
-// (J a multiple of 64), S [P x Q] fp32; tiles = J / 64; out [J x Q], or
-// [Q x J] when transposed.
+// (J a multiple of 64), S given as its hi/lo bf16 split [P x 2Q] (hi in
+// columns 0..Q-1, lo in Q..2Q-1); tiles = J / 64; out [J x Q], or [Q x J]
+// when transposed.
 struct ColReduce {
   const __nv_bfloat16* L;
-  const float* S;
+  const __nv_bfloat16* S2;
   int64_t P, J;
   SplitPlan sp;
   int tiles;

@@ -14,10 +14,10 @@
 // rank, so results are bitwise reproducible run to run, and nothing but the
 // result goes to global memory.
 //
-// The column reduction takes S in fp32 and splits it on the fly into
-// S_hi = bf16(S) and S_lo = bf16(S - S_hi) (side by side, a [64 x 2Q] bf16
-// tile), so the tensor-core products keep ~16 significant bits of S; the
-// finishing CTA adds the hi and lo sums.  One launch can carry two column
+// The column reduction takes S as S_hi = bf16(S) and S_lo = bf16(S - S_hi)
+// side by side ([P x 2Q] bf16, written by the row reduction that produces or
+// passes S), so the tensor-core products keep ~16 significant bits of S; the
+// finishing step adds the hi and lo sums.  One launch can carry two column
 // reductions (dB and dA of the same backward call).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -43,6 +43,22 @@ template <int Q>
 struct RowStages {
   static constexpr int NS = Q <= 32 ? 4 : 3;
 };
+
+// hi = bf16(v), lo = bf16(v - hi) of 4 consecutive values; hi at dst[0..3],
+// lo at dst[q_stride..q_stride+3]
+__device__ __forceinline__ void store_hilo(__nv_bfloat16* dst, float4 v, int q_stride) {
+  const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y);
+  const __nv_bfloat162 h23 = __floats2bfloat162_rn(v.z, v.w);
+  const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+  const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+  const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+  __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(dst);
+  __nv_bfloat162* l2 = reinterpret_cast<__nv_bfloat162*>(dst + q_stride);
+  h2[0] = h01;
+  h2[1] = h23;
+  l2[0] = l01;
+  l2[1] = l23;
+}
 
 // 16-byte load from the shared memory of CTA `rank` of the cluster, at the
 // offset of `local` in this CTA's shared memory.
@@ -205,6 +221,9 @@ __global__ void __launch_bounds__(NTHR) rr_fin_kernel(const RowReduce jb) {
       o2[0] = __floats2bfloat162_rn(v.x * jb.scale, v.y * jb.scale);
       o2[1] = __floats2bfloat162_rn(v.z * jb.scale, v.w * jb.scale);
     }
+    const int64_t h = (p0 + (it * 4) / Q) * (2 * Q) + (it * 4) % Q;  // [P x 2Q] position of the hi value
+    if (jb.out_hilo) store_hilo(jb.out_hilo + h, v, Q);
+    if (jb.aux_hilo) store_hilo(jb.aux_hilo + h, *reinterpret_cast<const float4*>(jb.aux_src + i), Q);
   }
   cluster_sync_all();  // no CTA leaves while its tile may still be read
 }
@@ -223,9 +242,8 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
   constexpr int Q2 = 2 * Q;
   constexpr int SP = Q2 + 8;
   extern __shared__ __align__(128) uint8_t cr_smem[];
-  __nv_bfloat16* sL = reinterpret_cast<__nv_bfloat16*>(cr_smem);                       // NS x [64 x 72]
-  float* sF = reinterpret_cast<float*>(cr_smem + NS * TP * LPITCH * 2);                 // NS x [64 x Q]
-  __nv_bfloat16* sS = reinterpret_cast<__nv_bfloat16*>(cr_smem + NS * TP * LPITCH * 2 + NS * TP * Q * 4);
+  __nv_bfloat16* sL = reinterpret_cast<__nv_bfloat16*>(cr_smem);  // NS x [64 x 72]
+  __nv_bfloat16* sS = sL + NS * TP * LPITCH;                         // NS x [64 x (2Q + 8)]
 
   const bool second = (int)blockIdx.x >= ja.tiles;
   ColReduce jb;
@@ -243,11 +261,11 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
   const int64_t p_end = min(P, p_begin + jb.sp.chunk);
   const int nchunks = p_end > p_begin ? (int)((p_end - p_begin + TP - 1) / TP) : 0;
   const __nv_bfloat16* __restrict__ L = jb.L;
-  const float* __restrict__ S = jb.S;
+  const __nv_bfloat16* __restrict__ S2 = jb.S2;
 
   auto load_chunk = [&](int buf, int64_t pp) {
     __nv_bfloat16* dL = sL + buf * TP * LPITCH;
-    float* dF = sF + buf * TP * Q;
+    __nv_bfloat16* dS = sS + buf * TP * SP;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int piece = tid + i * NTHR;
@@ -255,10 +273,10 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
       const bool ok = (pp + r) < p_end;
       cp_async16(s_addr(dL + r * LPITCH + c8), L + (ok ? (pp + r) : 0) * J + j0 + c8, ok);
     }
-    for (int piece = tid; piece < TP * (Q / 4); piece += NTHR) {  // 64 rows x Q fp32
-      const int r = piece / (Q / 4), c4 = (piece % (Q / 4)) * 4;
+    for (int piece = tid; piece < TP * (Q2 / 8); piece += NTHR) {  // 64 rows x 2Q bf16
+      const int r = piece / (Q2 / 8), c8 = (piece % (Q2 / 8)) * 8;
       const bool ok = (pp + r) < p_end;
-      cp_async16(s_addr(dF + r * Q + c4), S + (ok ? (pp + r) : 0) * Q + c4, ok);
+      cp_async16(s_addr(dS + r * SP + c8), S2 + (ok ? (pp + r) : 0) * Q2 + c8, ok);
     }
   };
 
@@ -273,25 +291,14 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
   }
   for (int ch = 0; ch < nchunks; ++ch) {
     cp_async_wait<NS - 2>();
-    __syncthreads();  // chunk ch landed for all; chunk ch-1's buffers and sS are free
-    const int buf = ch % NS;
-    {
-      const float* f = sF + buf * TP * Q;
-      for (int e = tid; e < TP * Q; e += NTHR) {
-        const int r = e / Q, q = e % Q;
-        const float v = f[e];
-        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-        sS[r * SP + q] = hi;
-        sS[r * SP + Q + q] = lo;
-      }
-    }
+    __syncthreads();  // chunk ch landed for all; chunk ch-1's buffers are free
     {
       const int nx = ch + NS - 1;
       if (nx < nchunks) load_chunk(nx % NS, p_begin + (int64_t)nx * TP);
       cp_async_commit();
     }
-    __syncthreads();  // sS complete
+    const int buf = ch % NS;
+    const __nv_bfloat16* tS = sS + buf * TP * SP;
     const __nv_bfloat16* tL = sL + buf * TP * LPITCH;
 #pragma unroll
     for (int kk = 0; kk < TP / 16; ++kk) {
@@ -308,7 +315,7 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
         const int i = lane >> 3;
         const int p = kk * 16 + (i & 1) * 8 + (lane & 7);
         const int q = nt * 8 + (i >> 1) * 8;
-        ldsm_x4_t(s_addr(sS + p * SP + q), b0, b1, b2, b3);
+        ldsm_x4_t(s_addr(tS + p * SP + q), b0, b1, b2, b3);
         mma_bf16_16816(acc[nt], a, b0, b1);
         mma_bf16_16816(acc[nt + 1], a, b2, b3);
       }
@@ -418,7 +425,7 @@ static cudaError_t launch_rr_fin_q(const RowReduce& r, cudaStream_t st) {
 template <int Q>
 static cudaError_t launch_cr_fin_q(const ColReduce& a, const ColReduce& b, cudaStream_t st) {
   constexpr int NS = kColStages;
-  constexpr size_t smem = (size_t)NS * TP * LPITCH * 2 + (size_t)NS * TP * Q * 4 + (size_t)TP * (2 * Q + 8) * 2;
+  constexpr size_t smem = (size_t)NS * 2 * (TP * LPITCH + TP * (2 * Q + 8));
   const dim3 grid((unsigned)(a.tiles + b.tiles), (unsigned)a.sp.splits);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   if (a.sp.splits > kMaxClusterSplits || (b.tiles > 0 && b.sp.splits != a.sp.splits)) return cudaErrorInvalidValue;
