@@ -134,6 +134,9 @@ static WeightView view_of(const qlora_weight_desc* w) {
   v.absmax_q = w->absmax_q;
   v.absmax_scale = w->absmax_scale;
   v.dq_group = w->dq_group > 0 ? w->dq_group : 1;
+  v.dq_shift = -1;
+  for (int b = 0; b < 31; ++b)
+    if (v.dq_group == (1 << b)) v.dq_shift = b;
   v.fmt = w->fmt;
   return v;
 }

@@ -194,15 +194,25 @@ struct WeightView {
   const int8_t* absmax_q;
   const float* absmax_scale;
   int dq_group;
+  int dq_shift;  // log2(dq_group) when it is a power of two, else -1
   int fmt;
 };
 
 // Raw bytes of one line, kept in registers between load and decode so the
-// loads of the next line can be in flight while this one is decoded.
+// loads of later lines can be in flight while this one is decoded.  Nothing
+// here depends on a loaded value: the NF4 absmax' = q * scale2 product is
+// formed at decode time, so issuing the loads never waits for them.
+constexpr int32_t kNoDq = 0x7fffffff;
 struct RawLine {
   uint32_t w[17];
-  float scale;  // NF4 absmax' (unused otherwise)
+  float scale;  // NF4: absmax (fp32 absmax) or the group's scale2 (double quantised)
+  int32_t q;    // NF4: the int8 absmax code (double quantised), else kNoDq
 };
+
+// NF4 absmax of the line: the fp32 absmax, or RN_f32(f32(q8) * scale2)
+__device__ __forceinline__ float nf4_line_scale(const RawLine& r) {
+  return r.q == kNoDq ? r.scale : __fmul_rn((float)r.q, r.scale);
+}
 
 enum { FMT_BF16 = 0, FMT_NF4 = 1, FMT_Q8_0 = 2, FMT_Q4_0 = 3 };
 
@@ -215,9 +225,11 @@ __device__ __forceinline__ void load_line(const WeightView& v, int64_t line, Raw
     r.w[4] = b.x; r.w[5] = b.y; r.w[6] = b.z; r.w[7] = b.w;
     if (v.absmax != nullptr) {
       r.scale = __ldg(v.absmax + line);
+      r.q = kNoDq;
     } else {
-      const float q = (float)__ldg(v.absmax_q + line);
-      r.scale = __fmul_rn(q, __ldg(v.absmax_scale + line / v.dq_group));
+      r.q = (int32_t)__ldg(v.absmax_q + line);
+      const int64_t grp = v.dq_shift >= 0 ? (line >> v.dq_shift) : line / v.dq_group;
+      r.scale = __ldg(v.absmax_scale + grp);
     }
   } else if constexpr (FMT == FMT_Q8_0) {
     const uint8_t* p = v.data + line * 68;
@@ -242,7 +254,7 @@ template <int FMT>
 __device__ __forceinline__ void decode_line(const RawLine& r, uint4 (&out)[8]) {
   if constexpr (FMT == FMT_NF4) {
     decode_nf4_line(make_uint4(r.w[0], r.w[1], r.w[2], r.w[3]), make_uint4(r.w[4], r.w[5], r.w[6], r.w[7]),
-                    r.scale, out);
+                    nf4_line_scale(r), out);
   } else if constexpr (FMT == FMT_Q8_0) {
     uint32_t W[17];
 #pragma unroll

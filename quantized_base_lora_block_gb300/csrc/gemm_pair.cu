@@ -57,6 +57,11 @@ struct PairCfg {
   static constexpr int LINES = HALF_N;                    // decoded 64-wide lines per stage per CTA
   static constexpr int GROUP_WARPS = LINES / 32;          // one line per thread of a group
   static constexpr int GROUPS = CFG == 1 ? 3 : (CFG == 2 ? 5 : 2);  // groups rotate over stages
+#ifndef QLORA_OUT_BUFS
+  static constexpr int OUT_BUFS = CFG == 2 ? 1 : 2;       // epilogue staging tiles (2: store overlaps next chunk)
+#else
+  static constexpr int OUT_BUFS = QLORA_OUT_BUFS;
+#endif
   static constexpr int DQ_WARPS = GROUP_WARPS * GROUPS;
   static_assert(STAGES % GROUPS == 0, "a stage must always be decoded by the same group");
   static_assert(NBUF * NACC * TN == 512, "accumulators fill TMEM");
@@ -74,14 +79,14 @@ struct __align__(8) PairBarriers {
   int ep_ok;  // epilogue: result of the "accumulator full" wait, for all 4 warps
 };
 
-// epilogue staging: one 128-row x 64-column bf16 chunk (128B-swizzled),
+// epilogue staging: 128-row x 64-column bf16 chunks (128B-swizzled), each
 // written out with a TMA tensor store
 constexpr int P_STAGE_OUT_BYTES = 128 * 64 * 2;
 
 template <int CFG>
 constexpr size_t p_smem_bytes() {
   return 1024 + (size_t)PairCfg<CFG>::STAGES * (PairCfg<CFG>::A_BYTES + PairCfg<CFG>::B_BYTES) +
-         P_STAGE_OUT_BYTES + sizeof(PairBarriers<CFG>);
+         (size_t)PairCfg<CFG>::OUT_BUFS * P_STAGE_OUT_BYTES + sizeof(PairBarriers<CFG>);
 }
 
 template <int FMT, int CFG>
@@ -92,6 +97,7 @@ constexpr int p_threads() {
 struct PairTile {
   int m0, n0;
 };
+
 
 // Tile order (chosen on the host): row blocks fastest keeps the whole A
 // operand hot in L2 while weight slabs stream; column blocks fastest keeps
@@ -129,7 +135,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
   const uint32_t sB0 = sA0 + P_STAGES * P_A_BYTES;
   const uint32_t sOut = sB0 + P_STAGES * P_B_BYTES;  // 1024-aligned (stage sizes are multiples of 8 KB)
   PairBarriers<CFG>* bars =
-      reinterpret_cast<PairBarriers<CFG>*>(smem + P_STAGES * (P_A_BYTES + P_B_BYTES) + P_STAGE_OUT_BYTES);
+      reinterpret_cast<PairBarriers<CFG>*>(smem + P_STAGES * (P_A_BYTES + P_B_BYTES) + Cfg::OUT_BUFS * P_STAGE_OUT_BYTES);
   volatile int* abort = &bars->abort;
 
   const uint32_t rank = cluster_ctarank();
@@ -271,12 +277,14 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     // Per 64-column chunk: each thread loads its row's 64 fp32 values from
     // TMEM, converts them to bf16 and writes one 128-byte row of a
     // 128B-swizzled staging tile (conflict-free); one thread then stores the
-    // 128 x 64 tile with a TMA tensor store (rows beyond M are not written).
+    // 128 x 64 tile with a TMA tensor store.  With two staging tiles the
+    // store of one chunk overlaps the conversion of the next.  Chunks wholly
+    // outside the output are neither staged nor stored.
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
     const int ep = (warp - 2) * 32 + lane;  // 0..127
-    const uint32_t srow = sOut + (uint32_t)row_in_tile * 128;
     const int swz = row_in_tile & 7;
+    uint32_t nstored = 0;  // chunks stored so far (selects the staging tile)
     for (int lt = 0; lt < my_tiles; ++lt) {
       const PairTile tc = pair_tile<DX, CFG>(args, pair + lt * num_pairs);
       const int buf = lt % NBUF;
@@ -307,8 +315,18 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[slot]), 0));
           }
-          if (ep == 0) bulk_wait_read0();  // staging tile free again
+          // the same for all 128 threads
+          if (row0 >= args.M || tc.n0 + 64 * c >= args.n_out) continue;
+          const uint32_t stile = sOut + (nstored % Cfg::OUT_BUFS) * P_STAGE_OUT_BYTES;
+          ++nstored;
+          if (ep == 0) {  // the store that last read this staging tile is done with it
+            if (Cfg::OUT_BUFS == 2)
+              bulk_wait_read1();
+            else
+              bulk_wait_read0();
+          }
           named_bar(1, 128);
+          const uint32_t srow = stile + (uint32_t)row_in_tile * 128;
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const uint32_t* v = q < 4 ? v0 + 8 * q : v1 + 8 * (q - 4);
@@ -321,8 +339,8 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
           }
           fence_proxy_async_smem();
           named_bar(1, 128);
-          if (ep == 0 && row0 < args.M && tc.n0 + 64 * c < args.n_out) {
-            tma_store_2d(&tm_out, sOut, tc.n0 + 64 * c, row0);
+          if (ep == 0) {
+            tma_store_2d(&tm_out, stile, tc.n0 + 64 * c, row0);
             bulk_commit();
           }
         }
@@ -414,7 +432,9 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     };
 
     // cur: the item being processed; pre: the item whose bytes are loaded
-    // next (two items ahead of cur, so two lines are in flight per thread)
+    // next (two items ahead of cur, so two lines are in flight per thread;
+    // measured on the Llama gate shape, three or four lines in flight are
+    // slower)
     Cursor cur{0, 0, 0, 0, false};
     set_tile(cur);
     advance(cur, g);
