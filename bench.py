@@ -522,9 +522,13 @@ def main():
         e2e_step(1)
         torch.cuda.synchronize()
         barrier(world)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0 = time.perf_counter()
+        g0.record(stream)
         for k in range(args.steps):
             e2e_step(k)
+        g1.record(stream)
+        t_issue = time.perf_counter() - t0
         torch.cuda.synchronize()
         t_e2e = max_over_ranks(time.perf_counter() - t0, world)
         # the host -> device copies of one step alone, for context
@@ -538,6 +542,8 @@ def main():
         torch.cuda.synchronize()
         e2e = {"value": world * M * args.steps / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "h2d_alone_GBps": h2d / (c0.elapsed_time(c1) / 1e3) / 1e9,
+               "host_issue_ms_per_step": 1e3 * t_issue / args.steps,
+               "compute_stream_ms_per_step": g0.elapsed_time(g1) / args.steps,
                "note": "pinned host X and dY copied in on a copy stream (double-buffered, overlapped with "
                        "compute), dA and dB copied out on a third stream, every step; wall clock"}
 

@@ -96,6 +96,20 @@ static bool map2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
   return make_map(m, base, 2, dims, strides, box);
 }
 
+// Byte tensor [rows x row_bytes] (row_bytes a multiple of 16), no swizzle,
+// zero fill outside the tensor: NF4 code bytes, two codes per byte.
+static bool map2d_u8(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_bytes,
+                     uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[2] = {row_bytes, rows}, s[1] = {row_bytes};
+  cuuint32_t b[2] = {box_bytes, box_rows}, e[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), d, s, b, e,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static int validate_weight(const qlora_weight_desc* w) {
@@ -241,6 +255,11 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
     if (w->fmt == QLORA_FMT_BF16) ok = ok && map2d(&maps.w, w->data, K, N, 64, 64);
   }
   if (pair) ok = ok && map2d(&maps.out, out, dx ? K : N, M, 64, 128);
+  // NF4 on 512 x 256 pair tiles: code bytes [N x K/2] through the raw ring,
+  // one box per item (forward: 128 weight rows x one 64-element block; dX:
+  // 64 weight rows x the CTA's two blocks)
+  if (pair == 3 && w->fmt == QLORA_FMT_NF4)
+    ok = ok && (dx ? map2d_u8(&maps.w, w->data, K / 2, N, 64, 64) : map2d_u8(&maps.w, w->data, K / 2, N, 32, 128));
   if (!ok) return cudaErrorInvalidValue;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));

@@ -249,6 +249,18 @@ __device__ __forceinline__ void load_line(const WeightView& v, int64_t line, Raw
   }
 }
 
+// NF4: the line's absmax fields only (its code bytes arrive another way).
+__device__ __forceinline__ void load_nf4_scale(const WeightView& v, int64_t line, RawLine& r) {
+  if (v.absmax != nullptr) {
+    r.scale = __ldg(v.absmax + line);
+    r.q = kNoDq;
+  } else {
+    r.q = (int32_t)__ldg(v.absmax_q + line);
+    const int64_t grp = v.dq_shift >= 0 ? (line >> v.dq_shift) : line / v.dq_group;
+    r.scale = __ldg(v.absmax_scale + grp);
+  }
+}
+
 // Only for the quantised formats.
 template <int FMT>
 __device__ __forceinline__ void decode_line(const RawLine& r, uint4 (&out)[8]) {

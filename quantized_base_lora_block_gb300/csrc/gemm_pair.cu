@@ -57,14 +57,23 @@ struct PairCfg {
   static constexpr int LINES = HALF_N;                    // decoded 64-wide lines per stage per CTA
   static constexpr int GROUP_WARPS = LINES / 32;          // one line per thread of a group
   static constexpr int GROUPS = CFG == 1 ? 3 : (CFG == 2 ? 5 : 2);  // groups rotate over stages
-#ifndef QLORA_OUT_BUFS
-  static constexpr int OUT_BUFS = CFG == 2 ? 1 : 2;       // epilogue staging tiles (2: store overlaps next chunk)
-#else
-  static constexpr int OUT_BUFS = QLORA_OUT_BUFS;
-#endif
   static constexpr int DQ_WARPS = GROUP_WARPS * GROUPS;
   static_assert(STAGES % GROUPS == 0, "a stage must always be decoded by the same group");
   static_assert(NBUF * NACC * TN == 512, "accumulators fill TMEM");
+};
+
+// NF4 bases on 512 x 256 tiles take their code bytes through a TMA ring
+// ("raw" ring, RAW_STAGES items deep, filled by a warp of its own) instead of
+// per-thread global loads: each stage's codes are one 2-D box (forward: 128
+// rows x 32 bytes; dX: 64 rows x 64 bytes), and the decode warps read them
+// from shared memory.  Their shared memory comes from the second epilogue
+// staging tile.
+template <int FMT, int CFG>
+struct PairRaw {
+  static constexpr bool ON = FMT == FMT_NF4 && CFG == 3;
+  static constexpr int STAGES = 4;
+  static constexpr int BYTES = ON ? 32 * PairCfg<CFG>::HALF_N : 0;  // code bytes of one item for this CTA
+  static constexpr int OUT_BUFS = (CFG == 2 || ON) ? 1 : 2;        // epilogue staging tiles
 };
 
 template <int CFG>
@@ -74,6 +83,8 @@ struct __align__(8) PairBarriers {
   uint64_t empty[PairCfg<CFG>::STAGES];   // both: MMA completion (multicast)
   uint64_t acc_full[4];                   // per (buffer, accumulator): MMA completion (multicast)
   uint64_t acc_empty[4];                  // CTA 0, per (buffer, accumulator): epilogue warps of both CTAs
+  uint64_t raw_full[4];                   // raw ring: code bytes landed (TMA, this CTA)
+  uint64_t raw_empty[4];                  // raw ring: the decode group has read them (this CTA)
   uint32_t tmem_base;
   int abort;
   int ep_ok;  // epilogue: result of the "accumulator full" wait, for all 4 warps
@@ -83,15 +94,21 @@ struct __align__(8) PairBarriers {
 // written out with a TMA tensor store
 constexpr int P_STAGE_OUT_BYTES = 128 * 64 * 2;
 
-template <int CFG>
+template <int FMT, int CFG>
 constexpr size_t p_smem_bytes() {
   return 1024 + (size_t)PairCfg<CFG>::STAGES * (PairCfg<CFG>::A_BYTES + PairCfg<CFG>::B_BYTES) +
-         (size_t)PairCfg<CFG>::OUT_BUFS * P_STAGE_OUT_BYTES + sizeof(PairBarriers<CFG>);
+         (size_t)PairRaw<FMT, CFG>::OUT_BUFS * P_STAGE_OUT_BYTES +
+         (size_t)PairRaw<FMT, CFG>::STAGES * PairRaw<FMT, CFG>::BYTES + sizeof(PairBarriers<CFG>);
 }
+static_assert(p_smem_bytes<FMT_NF4, 3>() <= 232448 && p_smem_bytes<FMT_Q8_0, 3>() <= 232448 &&
+                  p_smem_bytes<FMT_NF4, 2>() <= 232448 && p_smem_bytes<FMT_BF16, 1>() <= 232448,
+              "shared memory per CTA");
 
+// warps: 0 TMA producer, 1 TMEM / MMA issuer, 2-5 epilogue, then the decode
+// warps, then (raw ring) the code-byte producer
 template <int FMT, int CFG>
 constexpr int p_threads() {
-  return (FMT == FMT_BF16) ? 6 * 32 : (6 + PairCfg<CFG>::DQ_WARPS) * 32;
+  return (FMT == FMT_BF16) ? 6 * 32 : (6 + PairCfg<CFG>::DQ_WARPS + (PairRaw<FMT, CFG>::ON ? 1 : 0)) * 32;
 }
 
 struct PairTile {
@@ -127,6 +144,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
                       const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_lb,
                       const __grid_constant__ CUtensorMap tm_out, const GemmArgs args) {
   using Cfg = PairCfg<CFG>;
+  using Raw = PairRaw<FMT, CFG>;
   constexpr int P_STAGES = Cfg::STAGES, P_A_BYTES = Cfg::A_BYTES, P_B_BYTES = Cfg::B_BYTES;
   constexpr int TN = Cfg::TN, HALF_N = Cfg::HALF_N, NACC = Cfg::NACC, NBUF = Cfg::NBUF;
   extern __shared__ uint8_t smem_raw[];
@@ -134,8 +152,9 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
   const uint32_t sA0 = smem_u32(smem);
   const uint32_t sB0 = sA0 + P_STAGES * P_A_BYTES;
   const uint32_t sOut = sB0 + P_STAGES * P_B_BYTES;  // 1024-aligned (stage sizes are multiples of 8 KB)
-  PairBarriers<CFG>* bars =
-      reinterpret_cast<PairBarriers<CFG>*>(smem + P_STAGES * (P_A_BYTES + P_B_BYTES) + Cfg::OUT_BUFS * P_STAGE_OUT_BYTES);
+  const uint32_t sRaw = sOut + Raw::OUT_BUFS * P_STAGE_OUT_BYTES;
+  PairBarriers<CFG>* bars = reinterpret_cast<PairBarriers<CFG>*>(
+      smem + P_STAGES * (P_A_BYTES + P_B_BYTES) + Raw::OUT_BUFS * P_STAGE_OUT_BYTES + Raw::STAGES * Raw::BYTES);
   volatile int* abort = &bars->abort;
 
   const uint32_t rank = cluster_ctarank();
@@ -155,6 +174,8 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     for (int b = 0; b < 4; ++b) {
       mbar_init(smem_u32(&bars->acc_full[b]), 1);
       mbar_init(smem_u32(&bars->acc_empty[b]), 8);
+      mbar_init(smem_u32(&bars->raw_full[b]), 1);
+      mbar_init(smem_u32(&bars->raw_empty[b]), Cfg::GROUP_WARPS);
     }
     bars->abort = 0;
     fence_mbar_init();
@@ -163,7 +184,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
   if (warp == 2 && lane == 0) prefetch_tmap(&tm_out);
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_a);
-    if (FMT == FMT_BF16) prefetch_tmap(&tm_w);
+    if (FMT == FMT_BF16 || Raw::ON) prefetch_tmap(&tm_w);
     if (has_lora) {
       prefetch_tmap(&tm_la);
       prefetch_tmap(&tm_lb);
@@ -317,10 +338,10 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
           }
           // the same for all 128 threads
           if (row0 >= args.M || tc.n0 + 64 * c >= args.n_out) continue;
-          const uint32_t stile = sOut + (nstored % Cfg::OUT_BUFS) * P_STAGE_OUT_BYTES;
+          const uint32_t stile = sOut + (nstored % Raw::OUT_BUFS) * P_STAGE_OUT_BYTES;
           ++nstored;
           if (ep == 0) {  // the store that last read this staging tile is done with it
-            if (Cfg::OUT_BUFS == 2)
+            if (Raw::OUT_BUFS == 2)
               bulk_wait_read1();
             else
               bulk_wait_read0();
@@ -348,7 +369,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       if (!ok) break;
     }
     if (ep == 0) bulk_wait0();
-  } else if (FMT != FMT_BF16) {
+  } else if (FMT != FMT_BF16 && warp < 6 + Cfg::DQ_WARPS) {
     // ------------------------------------------------------------ decode
     // group g (GROUP_WARPS warps) handles the items with it % GROUPS == g;
     // thread d of the group decodes one 64-element line of this CTA's half
@@ -404,13 +425,33 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     auto fetch = [&](const Cursor& c, RawLine& r) -> bool {
       bool valid;
       const int64_t ln = line_at(c, valid);
-      if (valid) load_line<FMT>(args.wv, ln, r);
+      if (valid) {
+        if (Raw::ON)
+          load_nf4_scale(args.wv, ln, r);  // the code bytes come through the raw ring
+        else
+          load_line<FMT>(args.wv, ln, r);
+      }
       return valid;
     };
-    auto process = [&](const Cursor& c, const RawLine& r, bool valid) -> bool {
+    auto process = [&](const Cursor& c, RawLine& r, bool valid) -> bool {
       const int s = c.it % P_STAGES;
       const uint32_t ph = (c.it / P_STAGES) & 1;
       bool ok = true;
+      if (Raw::ON) {
+        // this item's code bytes: wait for them (every lane, for its own
+        // acquire), copy them to registers, hand the slot back
+        const uint32_t rs = c.it % Raw::STAGES;
+        ok = mbar_wait(smem_u32(&bars->raw_full[rs]), (c.it / Raw::STAGES) & 1, abort, args.err);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        if (valid) {
+          const uint32_t src = sRaw + rs * Raw::BYTES + (DX ? (uint32_t)((d & 63) * 64 + (d >> 6) * 32) : (uint32_t)(d * 32));
+          const uint4 a = lds_v4(src), b = lds_v4(src + 16);
+          r.w[0] = a.x; r.w[1] = a.y; r.w[2] = a.z; r.w[3] = a.w;
+          r.w[4] = b.x; r.w[5] = b.y; r.w[6] = b.z; r.w[7] = b.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->raw_empty[rs]));
+      }
       if (lane == 0) ok = mbar_wait_cluster(smem_u32(&bars->empty[s]), ph ^ 1, abort, args.err);
       if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) return false;
       if (c.kb < nkb) {
@@ -457,6 +498,38 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     }
   }
 
+  if (Raw::ON && warp == 6 + Cfg::DQ_WARPS && lane == 0) {
+    // ---------------------------------------------------- raw code producer
+    // the same item sequence as the decode warps: every (tile, k-block) of
+    // this pair, the adapter chunk included (no bytes: a plain arrive)
+    uint32_t it = 0;
+    bool ok = true;
+    for (int lt = 0; lt < my_tiles && ok; ++lt) {
+      const PairTile tc = pair_tile<DX, CFG>(args, pair + lt * num_pairs);
+      const int ncol = tc.n0 + HALF_N * (int)rank;  // forward: first weight row; dX: first output column
+      for (int kb = 0; kb < nkb_total; ++kb, ++it) {
+        const uint32_t rs = it % Raw::STAGES;
+        if (!mbar_wait(smem_u32(&bars->raw_empty[rs]), ((it / Raw::STAGES) & 1) ^ 1, abort, args.err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bar = smem_u32(&bars->raw_full[rs]);
+        if (kb < nkb) {
+          mbar_arrive_expect_tx(bar, Raw::BYTES);
+          if (!DX)
+            tma_load_2d(sRaw + rs * Raw::BYTES, &tm_w, bar, kb * 32, ncol);
+          else
+            tma_load_2d(sRaw + rs * Raw::BYTES, &tm_w, bar, ncol / 2, kb * kBK);
+        } else {
+          mbar_arrive(bar);
+        }
+      }
+    }
+    // copies still in flight land before the CTA may leave
+    for (uint32_t k = (it >= (uint32_t)Raw::STAGES ? it - Raw::STAGES : 0); k < it; ++k)
+      mbar_drain(smem_u32(&bars->raw_full[k % Raw::STAGES]), (k / Raw::STAGES) & 1);
+  }
+
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // no CTA leaves while its peer may still signal it
@@ -470,7 +543,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
 template <int FMT, bool DX, int CFG>
 static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, cudaStream_t st) {
   auto kern = qgemm_pair_kernel<FMT, DX, CFG>;
-  constexpr size_t P_SMEM_BYTES = p_smem_bytes<CFG>();
+  constexpr size_t P_SMEM_BYTES = p_smem_bytes<FMT, CFG>();
   static int max_clusters = -1;  // per instantiation
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
