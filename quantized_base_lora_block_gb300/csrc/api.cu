@@ -185,6 +185,36 @@ static DenseLayout dense_layout(int64_t M, int64_t N, int64_t K, int r) {
 
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA; }
 
+// ------------------------------------------------------------ side stream ---
+// A second stream per device for work of a call that may run beside the
+// call's main kernels: the backward call's adapter-gradient reduction runs
+// beside its dX GEMM, whose last partial wave of tiles leaves SMs idle.  The
+// call forks the side stream from the caller's stream and joins it back with
+// events before returning, so all of the call's work stays ordered on the
+// caller's stream.  The fork / launch / join sequence of one call is done
+// under a lock, so calls from several host threads do not interleave it.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ok = false;
+};
+static std::mutex g_side_mu;
+static SideStream g_side[64];
+
+static SideStream* side_stream_locked() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  SideStream& ss = g_side[dev];
+  if (!ss.ok) {
+    if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+    ss.ok = true;
+  }
+  return &ss;
+}
+
 // ------------------------------------------------ GEMM instrumentation ------
 struct GemmRec {
   cudaEvent_t a, b;
@@ -604,10 +634,7 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   ru.aux_hilo = T2;
   if (launch_row_reduce_fin(ru, rank, st) != cudaSuccess) return QLORA_ERR_CUDA;
 
-  // 2) dX = dY deq(W) + sU A
-  if (dX && run_dense_gemm(w, true, M, rank, dY, sU, A, dX, st) != cudaSuccess) return QLORA_ERR_CUDA;
-
-  // 3) dB = s dY^T T and dA = s U^T X (split over M, one launch); dA is
+  // 2) dB = s dY^T T and dA = s U^T X (split over M, one launch); dA is
   //    reduced as dA^T [K x r] and written transposed
   ColReduce cb;
   cb.L = dYb;
@@ -626,7 +653,23 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   ca.tiles = (int)L.da_tiles;
   ca.out = dA;
   ca.transposed = 1;
-  return cuda_status(launch_col_reduce_fin(cb, &ca, rank, st));
+  if (!dX) return cuda_status(launch_col_reduce_fin(cb, &ca, rank, st));
+
+  // 3) dX = dY deq(W) + sU A on the caller's stream, with step 2 beside it on
+  //    the side stream (both only read what step 1 wrote)
+  std::lock_guard<std::mutex> g(g_side_mu);
+  SideStream* ss = side_stream_locked();
+  if (!ss) {
+    if (run_dense_gemm(w, true, M, rank, dY, sU, A, dX, st) != cudaSuccess) return QLORA_ERR_CUDA;
+    return cuda_status(launch_col_reduce_fin(cb, &ca, rank, st));
+  }
+  cudaError_t e = cudaEventRecord(ss->fork, st);
+  if (e == cudaSuccess) e = run_dense_gemm(w, true, M, rank, dY, sU, A, dX, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
+  if (e == cudaSuccess) e = launch_col_reduce_fin(cb, &ca, rank, ss->s);
+  if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss->join, 0);
+  return cuda_status(e);
 }
 
 size_t qlora_grouped_workspace_bytes(const qlora_weight_desc* experts, int32_t E, const int32_t* offsets,
