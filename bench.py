@@ -425,7 +425,6 @@ def main():
     torch.cuda.synchronize()
     if clocks:
         clocks.mark("t0")
-    q.profile_gemm(True)
     n0 = q.launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -433,12 +432,24 @@ def main():
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    launches = q.launch_count() - n0
+    ms = e0.elapsed_time(e1)
+    # The same K steps again with CUDA events around every fused-GEMM launch
+    # (on the stream it is launched on) for the kernel's own time.  Those
+    # events lengthen a step by ~3.6%, so the headline pass above runs
+    # without them.
+    q.profile_gemm(True)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(args.steps):
+        step()
+    p1.record(stream)
+    torch.cuda.synchronize()
+    q.profile_gemm(False)
+    ms_prof = p0.elapsed_time(p1)
     if clocks:
         clocks.mark("t1")
-    launches = q.launch_count() - n0
-    q.profile_gemm(False)
     barrier(world)
-    ms = e0.elapsed_time(e1)
     clk = clocks.stop() if clocks else None
     gemm_ms, gemm_n, gemm_flops = q.profile_gemm_read()
     assert q.device_error() == 0, "device error in the timed region"
@@ -451,10 +462,12 @@ def main():
     ach = gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else 0.0
     roofline = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                 "frac": ach / peaks["bf16_sustained"], "traffic": captured_traffic(wl),
-                "kernel": "qgemm_kernel (fused decode + tcgen05 GEMM + adapter chunk), fwd and dX launches",
+                "kernel": "qgemm_pair_kernel (fused decode + tcgen05 cta_group::2 GEMM + adapter chunk), fwd and dX "
+                          "launches",
                 "peak_kind": f"{peaks['source']} sustained bf16",
                 "frac_of_burst": ach / peaks["bf16"], "frac_of_nominal_2250": ach / NOMINAL_BF16_TFLOPS,
-                "launches": gemm_n, "share_of_step": gemm_ms / ms if ms > 0 else None}
+                "launches": gemm_n, "share_of_step": gemm_ms / ms_prof if ms_prof > 0 else None,
+                "measured": "CUDA events around each fused-GEMM launch over a second pass of the same K steps"}
 
     # --------------------------------------------------------- end to end
     # Every step copies its X and dY (pinned host) in and its dA, dB out.  The
