@@ -148,6 +148,7 @@ static WeightView view_of(const qlora_weight_desc* w) {
   v.absmax_q = w->absmax_q;
   v.absmax_scale = w->absmax_scale;
   v.dq_group = w->dq_group > 0 ? w->dq_group : 1;
+  v.aq_align8 = (reinterpret_cast<uintptr_t>(w->absmax_q) & 7u) == 0 ? 1 : 0;
   v.dq_shift = -1;
   for (int b = 0; b < 31; ++b)
     if (v.dq_group == (1 << b)) v.dq_shift = b;

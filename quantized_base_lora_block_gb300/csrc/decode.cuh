@@ -194,7 +194,8 @@ struct WeightView {
   const int8_t* absmax_q;
   const float* absmax_scale;
   int dq_group;
-  int dq_shift;  // log2(dq_group) when it is a power of two, else -1
+  int dq_shift;   // log2(dq_group) when it is a power of two, else -1
+  int aq_align8;  // absmax_q is 8-byte aligned
   int fmt;
 };
 

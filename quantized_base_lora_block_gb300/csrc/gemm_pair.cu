@@ -422,16 +422,61 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       if (!DX) return c.base + c.kb;
       return ((int64_t)c.kb * kBK + (d & 63)) * args.w_lines_per_row + c.base;
     };
+    // Forward, double-quantised NF4 through the raw ring: a thread's lines
+    // are blocks kb, kb + GROUPS, ... of one weight row, so its absmax codes
+    // come 8 at a time (one aligned word) and its group scale changes at
+    // most once or twice per row.  Each is loaded when a line first needs a
+    // new one and kept with the one before it; a line records which word
+    // and group it needs (low 32 bits of their indices) and picks them at
+    // decode time, when the load issued for it has had an item to land.
+    const bool dq_cache = Raw::ON && !DX && args.wv.absmax == nullptr && args.wv.aq_align8;
+    int64_t aq_base = -1, sc_grp = -1;
+    uint32_t aq_new_lo = 0, aq_new_hi = 0, aq_old_lo = 0, aq_old_hi = 0, aq_old_base = 0xffffffffu;
+    float sc_new = 0.f, sc_old = 0.f;
+    uint32_t sc_old_grp = 0xffffffffu;
     auto fetch = [&](const Cursor& c, RawLine& r) -> bool {
       bool valid;
       const int64_t ln = line_at(c, valid);
       if (valid) {
-        if (Raw::ON)
+        if (dq_cache) {
+          const int64_t wb = ln & ~int64_t(7);
+          if (wb != aq_base) {
+            aq_old_lo = aq_new_lo;
+            aq_old_hi = aq_new_hi;
+            aq_old_base = (uint32_t)aq_base;
+            const uint2 w2 = ldg_nc_v2(args.wv.absmax_q + wb);
+            aq_new_lo = w2.x;
+            aq_new_hi = w2.y;
+            aq_base = wb;
+          }
+          const int64_t grp = args.wv.dq_shift >= 0 ? (ln >> args.wv.dq_shift) : ln / args.wv.dq_group;
+          if (grp != sc_grp) {
+            sc_old = sc_new;
+            sc_old_grp = (uint32_t)sc_grp;
+            sc_new = __ldg(args.wv.absmax_scale + grp);
+            sc_grp = grp;
+          }
+          r.w[8] = (uint32_t)wb;
+          r.w[9] = (uint32_t)grp;
+          r.q = (int32_t)(ln & 7);
+        } else if (Raw::ON) {
           load_nf4_scale(args.wv, ln, r);  // the code bytes come through the raw ring
-        else
+        } else {
           load_line<FMT>(args.wv, ln, r);
+        }
       }
       return valid;
+    };
+    // the line's absmax code and group scale from the two cached entries
+    auto resolve_dq = [&](RawLine& r) {
+      const bool wnew = r.w[8] == (uint32_t)aq_base;
+      const uint32_t lo = wnew ? aq_new_lo : aq_old_lo, hi = wnew ? aq_new_hi : aq_old_hi;
+      const uint32_t word = (r.q & 4) ? hi : lo;
+      const int32_t q = (int32_t)(int8_t)(uint8_t)(word >> (8 * (r.q & 3)));
+      r.scale = (r.w[9] == (uint32_t)sc_grp) ? sc_new : sc_old;
+      r.q = q;
+      (void)aq_old_base;
+      (void)sc_old_grp;
     };
     auto process = [&](const Cursor& c, RawLine& r, bool valid) -> bool {
       const int s = c.it % P_STAGES;
@@ -457,6 +502,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       if (c.kb < nkb) {
         const uint32_t dst = sB0 + s * P_B_BYTES + soff;
         if (valid) {
+          if (dq_cache) resolve_dq(r);
           uint4 out[8];
           decode_line<FMT>(r, out);
 #pragma unroll

@@ -325,6 +325,12 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   return r;
 }
 
+__device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t ldg_nc_u32(const void* p) {
   uint32_t r;
   asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
