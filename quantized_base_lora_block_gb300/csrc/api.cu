@@ -291,6 +291,20 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
   // 64 weight rows x the CTA's two blocks)
   if (pair == 3 && w->fmt == QLORA_FMT_NF4)
     ok = ok && (dx ? map2d_u8(&maps.w, w->data, K / 2, N, 64, 64) : map2d_u8(&maps.w, w->data, K / 2, N, 32, 128));
+  // dX with a double-quantised absmax: the int8 codes [N x K/64] and the
+  // group scales also through the raw ring, where the layout allows: 16-byte
+  // aligned arrays, code rows a multiple of 16 bytes, power-of-two groups, a
+  // scale array of whole 16-byte pieces, and an item's scales within the
+  // ring slot's 64 (at most ((63 K/64 + 1) >> log2 group) + 8 of them)
+  int raw_dq = 0;
+  if (ok && pair == 3 && dx && w->fmt == QLORA_FMT_NF4 && !w->absmax) {
+    const int64_t lpr = K / 64;
+    const WeightView v = view_of(w);
+    const int64_t groups = (N * lpr + v.dq_group - 1) / v.dq_group;
+    if (lpr % 16 == 0 && aligned16(w->absmax_q) && aligned16(w->absmax_scale) && v.dq_shift >= 0 &&
+        groups % 4 == 0 && ((63 * lpr + 1) >> v.dq_shift) + 8 <= 64)
+      raw_dq = map2d_u8(&maps.aq, w->absmax_q, lpr, N, 16, 64) ? 1 : 0;
+  }
   if (!ok) return cudaErrorInvalidValue;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -305,6 +319,7 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
   a.out = static_cast<__nv_bfloat16*>(out);
   a.wv = view_of(w);
   a.err = device_error_word();
+  a.raw_dq = raw_dq;
   // Tile order.  Forward: row blocks fastest while the activation fits in L2
   // next to the streamed weight slabs (measured: gate 133 MB of DRAM traffic
   // this way vs 234 MB the other way); beyond ~64 MB (e.g. the 14336-wide

@@ -63,17 +63,24 @@ struct PairCfg {
 };
 
 // NF4 bases on 512 x 256 tiles take their code bytes through a TMA ring
-// ("raw" ring, RAW_STAGES items deep, filled by a warp of its own) instead of
-// per-thread global loads: each stage's codes are one 2-D box (forward: 128
-// rows x 32 bytes; dX: 64 rows x 64 bytes), and the decode warps read them
-// from shared memory.  Their shared memory comes from the second epilogue
-// staging tile.
-template <int FMT, int CFG>
+// ("raw" ring, filled by a warp of its own) instead of per-thread global
+// loads: each item's codes are one 2-D box (forward: 128 rows x 32 bytes; dX:
+// 64 rows x 64 bytes), and the decode warps read them from shared memory.
+// In dX the slot also holds the item's int8 absmax codes (a 16-byte wide box
+// of the 64 rows, x rounded down to 16 bytes) and the range of group scales
+// its lines use (a 1-D bulk copy), when the host finds the layout allows it
+// (GemmArgs::raw_dq).  The ring's shared memory comes from the second
+// epilogue staging tile.
+template <int FMT, int CFG, bool DX>
 struct PairRaw {
   static constexpr bool ON = FMT == FMT_NF4 && CFG == 3;
-  static constexpr int STAGES = 4;
-  static constexpr int BYTES = ON ? 32 * PairCfg<CFG>::HALF_N : 0;  // code bytes of one item for this CTA
-  static constexpr int OUT_BUFS = (CFG == 2 || ON) ? 1 : 2;        // epilogue staging tiles
+  static constexpr int STAGES = DX ? 3 : 4;
+  static constexpr int CODE_BYTES = 32 * PairCfg<CFG>::HALF_N;  // code bytes of one item for this CTA
+  static constexpr int AQ_OFF = CODE_BYTES;                     // dX: [64 rows x 16] absmax codes
+  static constexpr int SC_OFF = CODE_BYTES + 1024;              // dX: group scales
+  static constexpr int SC_CAP = 64;                             // dX: group scales a slot holds
+  static constexpr int BYTES = !ON ? 0 : (DX ? SC_OFF + 4 * SC_CAP : CODE_BYTES);
+  static constexpr int OUT_BUFS = (CFG == 2 || ON) ? 1 : 2;     // epilogue staging tiles
 };
 
 template <int CFG>
@@ -94,21 +101,25 @@ struct __align__(8) PairBarriers {
 // written out with a TMA tensor store
 constexpr int P_STAGE_OUT_BYTES = 128 * 64 * 2;
 
-template <int FMT, int CFG>
+template <int FMT, int CFG, bool DX>
 constexpr size_t p_smem_bytes() {
+  using Raw = PairRaw<FMT, CFG, DX>;
   return 1024 + (size_t)PairCfg<CFG>::STAGES * (PairCfg<CFG>::A_BYTES + PairCfg<CFG>::B_BYTES) +
-         (size_t)PairRaw<FMT, CFG>::OUT_BUFS * P_STAGE_OUT_BYTES +
-         (size_t)PairRaw<FMT, CFG>::STAGES * PairRaw<FMT, CFG>::BYTES + sizeof(PairBarriers<CFG>);
+         (size_t)Raw::OUT_BUFS * P_STAGE_OUT_BYTES + (size_t)Raw::STAGES * Raw::BYTES + sizeof(PairBarriers<CFG>);
 }
-static_assert(p_smem_bytes<FMT_NF4, 3>() <= 232448 && p_smem_bytes<FMT_Q8_0, 3>() <= 232448 &&
-                  p_smem_bytes<FMT_NF4, 2>() <= 232448 && p_smem_bytes<FMT_BF16, 1>() <= 232448,
+static_assert(p_smem_bytes<FMT_NF4, 3, false>() <= 232448 && p_smem_bytes<FMT_NF4, 3, true>() <= 232448 &&
+                  p_smem_bytes<FMT_Q8_0, 3, true>() <= 232448 && p_smem_bytes<FMT_NF4, 2, true>() <= 232448 &&
+                  p_smem_bytes<FMT_BF16, 1, true>() <= 232448,
               "shared memory per CTA");
+static_assert(PairRaw<FMT_NF4, 3, true>::BYTES % 128 == 0 && PairRaw<FMT_NF4, 3, true>::AQ_OFF % 128 == 0 &&
+                  PairRaw<FMT_NF4, 3, true>::SC_OFF % 128 == 0,
+              "raw ring slots keep TMA destinations 128-byte aligned");
 
 // warps: 0 TMA producer, 1 TMEM / MMA issuer, 2-5 epilogue, then the decode
 // warps, then (raw ring) the code-byte producer
 template <int FMT, int CFG>
 constexpr int p_threads() {
-  return (FMT == FMT_BF16) ? 6 * 32 : (6 + PairCfg<CFG>::DQ_WARPS + (PairRaw<FMT, CFG>::ON ? 1 : 0)) * 32;
+  return (FMT == FMT_BF16) ? 6 * 32 : (6 + PairCfg<CFG>::DQ_WARPS + (PairRaw<FMT, CFG, false>::ON ? 1 : 0)) * 32;
 }
 
 struct PairTile {
@@ -142,9 +153,10 @@ template <int FMT, bool DX, int CFG>
 __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     qgemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_lb,
-                      const __grid_constant__ CUtensorMap tm_out, const GemmArgs args) {
+                      const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_aq,
+                      const GemmArgs args) {
   using Cfg = PairCfg<CFG>;
-  using Raw = PairRaw<FMT, CFG>;
+  using Raw = PairRaw<FMT, CFG, DX>;
   constexpr int P_STAGES = Cfg::STAGES, P_A_BYTES = Cfg::A_BYTES, P_B_BYTES = Cfg::B_BYTES;
   constexpr int TN = Cfg::TN, HALF_N = Cfg::HALF_N, NACC = Cfg::NACC, NBUF = Cfg::NBUF;
   extern __shared__ uint8_t smem_raw[];
@@ -185,6 +197,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_a);
     if (FMT == FMT_BF16 || Raw::ON) prefetch_tmap(&tm_w);
+    if (Raw::ON && DX && args.raw_dq) prefetch_tmap(&tm_aq);
     if (has_lora) {
       prefetch_tmap(&tm_la);
       prefetch_tmap(&tm_lb);
@@ -459,6 +472,8 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
           r.w[8] = (uint32_t)wb;
           r.w[9] = (uint32_t)grp;
           r.q = (int32_t)(ln & 7);
+        } else if (Raw::ON && DX && args.raw_dq) {
+          // everything this line needs arrives through the raw ring
         } else if (Raw::ON) {
           load_nf4_scale(args.wv, ln, r);  // the code bytes come through the raw ring
         } else {
@@ -489,10 +504,23 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
         ok = mbar_wait(smem_u32(&bars->raw_full[rs]), (c.it / Raw::STAGES) & 1, abort, args.err);
         if (!__all_sync(0xffffffffu, ok)) return false;
         if (valid) {
-          const uint32_t src = sRaw + rs * Raw::BYTES + (DX ? (uint32_t)((d & 63) * 64 + (d >> 6) * 32) : (uint32_t)(d * 32));
+          const uint32_t slot = sRaw + rs * Raw::BYTES;
+          const uint32_t src = slot + (DX ? (uint32_t)((d & 63) * 64 + (d >> 6) * 32) : (uint32_t)(d * 32));
           const uint4 a = lds_v4(src), b = lds_v4(src + 16);
           r.w[0] = a.x; r.w[1] = a.y; r.w[2] = a.z; r.w[3] = a.w;
           r.w[4] = b.x; r.w[5] = b.y; r.w[6] = b.z; r.w[7] = b.w;
+          if (DX && args.raw_dq) {
+            // absmax code of (row, block) and the group scale of its line
+            const int kblk = (int)c.base;  // this thread's k-block
+            const int kblk0 = kblk - (d >> 6);
+            const uint32_t qb = lds_u8(slot + Raw::AQ_OFF + (uint32_t)((d & 63) * 16 + (kblk & 15)));
+            const int64_t row0 = (int64_t)c.kb * kBK;
+            const int64_t g_lo = (row0 * args.w_lines_per_row + kblk0) >> args.wv.dq_shift;
+            const int64_t ln = (row0 + (d & 63)) * args.w_lines_per_row + kblk;
+            const int64_t gi = (ln >> args.wv.dq_shift) - (g_lo & ~int64_t(3));
+            r.q = (int32_t)(int8_t)(uint8_t)qb;
+            r.scale = lds_f32(slot + Raw::SC_OFF + (uint32_t)gi * 4);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->raw_empty[rs]));
@@ -560,12 +588,30 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
           break;
         }
         const uint32_t bar = smem_u32(&bars->raw_full[rs]);
+        const uint32_t slot = sRaw + rs * Raw::BYTES;
         if (kb < nkb) {
-          mbar_arrive_expect_tx(bar, Raw::BYTES);
-          if (!DX)
-            tma_load_2d(sRaw + rs * Raw::BYTES, &tm_w, bar, kb * 32, ncol);
-          else
-            tma_load_2d(sRaw + rs * Raw::BYTES, &tm_w, bar, ncol / 2, kb * kBK);
+          if (!DX) {
+            mbar_arrive_expect_tx(bar, Raw::CODE_BYTES);
+            tma_load_2d(slot, &tm_w, bar, kb * 32, ncol);
+          } else if (!args.raw_dq) {
+            mbar_arrive_expect_tx(bar, Raw::CODE_BYTES);
+            tma_load_2d(slot, &tm_w, bar, ncol / 2, kb * kBK);
+          } else {
+            // codes, the 64 rows' absmax codes from block (kblk0 & ~15) on,
+            // and the group scales from (g_lo & ~3) to g_hi rounded up to
+            // whole 16-byte pieces (the host checked that the array is a
+            // whole number of them and that the range fits SC_CAP)
+            const int kblk0 = ncol / 64;
+            const int64_t row0 = (int64_t)kb * kBK;
+            const int64_t g_lo = (row0 * args.w_lines_per_row + kblk0) >> args.wv.dq_shift;
+            const int64_t g_hi = ((row0 + 63) * args.w_lines_per_row + kblk0 + 1) >> args.wv.dq_shift;
+            const int64_t g0 = g_lo & ~int64_t(3);
+            const uint32_t sc_bytes = (uint32_t)(((g_hi - g0 + 1) + 3) & ~int64_t(3)) * 4;
+            mbar_arrive_expect_tx(bar, Raw::CODE_BYTES + 1024 + sc_bytes);
+            tma_load_2d(slot, &tm_w, bar, ncol / 2, kb * kBK);
+            tma_load_2d(slot + Raw::AQ_OFF, &tm_aq, bar, kblk0 & ~15, kb * kBK);
+            bulk_load_1d(slot + Raw::SC_OFF, args.wv.absmax_scale + g0, sc_bytes, bar);
+          }
         } else {
           mbar_arrive(bar);
         }
@@ -589,7 +635,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
 template <int FMT, bool DX, int CFG>
 static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, cudaStream_t st) {
   auto kern = qgemm_pair_kernel<FMT, DX, CFG>;
-  constexpr size_t P_SMEM_BYTES = p_smem_bytes<FMT, CFG>();
+  constexpr size_t P_SMEM_BYTES = p_smem_bytes<FMT, CFG, DX>();
   static int max_clusters = -1;  // per instantiation
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -614,7 +660,7 @@ static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, c
   const int pairs = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
   if (pairs <= 0) return cudaSuccess;
   cfg.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&cfg, kern, maps.a, maps.w, maps.la, maps.lb, maps.out, args);
+  return cudaLaunchKernelEx(&cfg, kern, maps.a, maps.w, maps.la, maps.lb, maps.out, maps.aq, args);
 }
 
 #ifndef QLORA_PAIR_QCFG

@@ -142,6 +142,7 @@ struct GemmArgs {
   WeightView wv;
   int* err;              // device error word
   int n_fastest;         // pair kernel tile order: 1 = output column blocks fastest
+  int raw_dq;            // pair kernel, NF4 dX: absmax codes and group scales through the raw ring
 };
 
 // Tensor maps: A operand [M x k_red] (X or dY), bf16 W (format BF16 only),
@@ -151,6 +152,7 @@ struct GemmArgs {
 struct GemmMaps {
   CUtensorMap a, w, la, lb;
   CUtensorMap out;  // pair kernel: bf16 output [M x n_out], box [64 x 128] (TMA stores)
+  CUtensorMap aq;   // pair kernel, NF4 dX with raw_dq: int8 absmax codes [N x K/64], box [16 x 64]
 };
 
 cudaError_t launch_qgemm(int fmt, bool dx, bool grouped, const GemmMaps& maps, const GemmArgs& args,

@@ -54,6 +54,17 @@ def test_formats_and_shapes(lib, fmt, dq, shape):
     check_all(inp, run_layer(inp), oracle_layer(inp))
 
 
+# Shapes with enough 512 x 256 pair tiles that the launches take them (the
+# NF4 code-byte ring, the forward absmax cache, and in the second case the dX
+# absmax / group-scale ring with groups spanning weight rows), ragged in M and
+# in the last column block.
+@pytest.mark.parametrize("shape", [(600, 1024, 10048, 16), (600, 10240, 1088, 16)], ids=["fwd_wide", "dx_wide"])
+def test_nf4dq_wide_tiles(lib, shape):
+    M, K, N, r = shape
+    inp = make(M, K, N, r, "nf4", True, seed=M + K + N)
+    check_all(inp, run_layer(inp), oracle_layer(inp))
+
+
 def test_b_zero_gives_base_product_and_zero_dA(lib):
     inp = make(160, 512, 256, 16, "nf4", b_std=0.0)
     assert np.all(syn.bf16_bits_to_f32(inp["B"]) == 0.0)  # +0 and -0 entries
