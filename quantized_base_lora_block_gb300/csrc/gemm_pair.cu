@@ -522,6 +522,10 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
             r.scale = lds_f32(slot + Raw::SC_OFF + (uint32_t)gi * 4);
           }
         }
+        // the slot is refilled by TMA (async proxy): order this warp's reads
+        // of it (generic proxy) before that write, or a refill can land
+        // before a read and the line decodes the next item's bytes
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&bars->raw_empty[rs]));
       }

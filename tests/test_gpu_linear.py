@@ -54,11 +54,15 @@ def test_formats_and_shapes(lib, fmt, dq, shape):
     check_all(inp, run_layer(inp), oracle_layer(inp))
 
 
-# Shapes with enough 512 x 256 pair tiles that the launches take them (the
-# NF4 code-byte ring, the forward absmax cache, and in the second case the dX
-# absmax / group-scale ring with groups spanning weight rows), ragged in M and
-# in the last column block.
-@pytest.mark.parametrize("shape", [(600, 1024, 10048, 16), (600, 10240, 1088, 16)], ids=["fwd_wide", "dx_wide"])
+# Shapes whose launches take the 512 x 256 pair tiles (the NF4 code-byte ring
+# and the forward absmax cache): forward with a ragged last column block
+# (10048 = 39 x 256 + 64, one CTA of the pair without weight rows), forward
+# with whole blocks, and dX with the absmax / group-scale ring (groups
+# spanning weight rows); all ragged in M.  The last case also has a long
+# reduction (K = 14336, as the down projection) with a ragged column block.
+@pytest.mark.parametrize("shape", [(600, 1024, 10048, 16), (600, 1024, 9728, 16), (600, 10240, 1088, 16),
+                                   (1100, 14336, 4160, 16)],
+                         ids=["fwd_ragged", "fwd", "dx", "fwd_long_ragged"])
 def test_nf4dq_wide_tiles(lib, shape):
     M, K, N, r = shape
     inp = make(M, K, N, r, "nf4", True, seed=M + K + N)
