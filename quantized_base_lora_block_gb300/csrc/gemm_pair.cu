@@ -499,7 +499,8 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       bool ok = true;
       if (Raw::ON) {
         // this item's code bytes: wait for them (every lane, for its own
-        // acquire), copy them to registers, hand the slot back
+        // acquire) and copy them to registers; the slot is handed back after
+        // the line's stores (below)
         const uint32_t rs = c.it % Raw::STAGES;
         ok = mbar_wait(smem_u32(&bars->raw_full[rs]), (c.it / Raw::STAGES) & 1, abort, args.err);
         if (!__all_sync(0xffffffffu, ok)) return false;
@@ -522,12 +523,6 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
             r.scale = lds_f32(slot + Raw::SC_OFF + (uint32_t)gi * 4);
           }
         }
-        // the slot is refilled by TMA (async proxy): order this warp's reads
-        // of it (generic proxy) before that write, or a refill can land
-        // before a read and the line decodes the next item's bytes
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->raw_empty[rs]));
       }
       if (lane == 0) ok = mbar_wait_cluster(smem_u32(&bars->empty[s]), ph ^ 1, abort, args.err);
       if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) return false;
@@ -544,9 +539,17 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
           for (int q = 0; q < 8; ++q) sts_v4(dst + (q << 4), make_uint4(0, 0, 0, 0));
         }
       }
+      // one proxy fence orders both this warp's stores of B (read by the
+      // MMA) and, with the raw ring, its reads of the raw slot before the
+      // slot's TMA refill (async proxy; without it a refill could land before
+      // a read and a line decode the next item's bytes), so the slot is
+      // handed back only after it
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(bready0 + s * 8);
+      if (lane == 0) {
+        mbar_arrive_cluster(bready0 + s * 8);
+        if (Raw::ON) mbar_arrive(smem_u32(&bars->raw_empty[c.it % Raw::STAGES]));
+      }
       return true;
     };
 
