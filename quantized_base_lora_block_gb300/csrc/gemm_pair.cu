@@ -208,6 +208,11 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
   cluster_sync_all();  // peer barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
+  // launched with programmatic stream serialisation: the set-up above
+  // overlaps the previous kernel's tail; nothing global is touched before it
+  // has finished, and the next kernel may start its own set-up
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -645,16 +650,18 @@ static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, c
   constexpr size_t P_SMEM_BYTES = p_smem_bytes<FMT, CFG, DX>();
   static int max_clusters = -1;  // per instantiation
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(p_threads<FMT, CFG>());
   cfg.dynamicSmemBytes = P_SMEM_BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // occupancy query without the launch-order attribute
   if (max_clusters < 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P_SMEM_BYTES);
     if (e != cudaSuccess) return e;
@@ -667,6 +674,7 @@ static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, c
   const int pairs = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
   if (pairs <= 0) return cudaSuccess;
   cfg.gridDim = dim3(2 * pairs);
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, maps.a, maps.w, maps.la, maps.lb, maps.out, maps.aq, args);
 }
 

@@ -99,6 +99,8 @@ __global__ void __launch_bounds__(NTHR) rr_fin_kernel(const RowReduce jb) {
   const int nchunks = j_end > j_begin ? (int)((j_end - j_begin + TJ - 1) / TJ) : 0;
   const __nv_bfloat16* __restrict__ L = jb.L;
   const __nv_bfloat16* __restrict__ S = jb.S;
+  griddep_wait();
+  griddep_launch_dependents();
 
   auto load_chunk = [&](int buf, int64_t j0) {
     __nv_bfloat16* dL = sL + buf * TP * LPITCH;
@@ -262,6 +264,8 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
   const int nchunks = p_end > p_begin ? (int)((p_end - p_begin + TP - 1) / TP) : 0;
   const __nv_bfloat16* __restrict__ L = jb.L;
   const __nv_bfloat16* __restrict__ S2 = jb.S2;
+  griddep_wait();
+  griddep_launch_dependents();
 
   auto load_chunk = [&](int buf, int64_t pp) {
     __nv_bfloat16* dL = sL + buf * TP * LPITCH;
@@ -383,8 +387,10 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// Launch with clusters of (1, splits, 1); the first launch of an
-// instantiation raises its shared-memory limit.
+// Launch with clusters of (1, splits, 1) and programmatic stream
+// serialisation (the kernels wait for the previous grid before touching
+// global memory); the first launch of an instantiation raises its
+// shared-memory limit.
 template <typename... Args>
 static cudaError_t launch_clustered(void (*kern)(Args...), dim3 grid, size_t smem, int splits, cudaStream_t st,
                                     bool& attr_done, Args... args) {
@@ -396,17 +402,19 @@ static cudaError_t launch_clustered(void (*kern)(Args...), dim3 grid, size_t sme
     attr_done = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = (unsigned)splits;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = grid;
   cfg.blockDim = dim3(NTHR);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
