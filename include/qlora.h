@@ -39,6 +39,10 @@
  *     dA and dB are overwritten (not accumulated).
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
  *     only enqueues work on it and returns; nothing synchronises.
+ *     qlora_linear_bwd also runs part of its work on a per-device stream of
+ *     the library's own, forked from `stream` and joined back into it with
+ *     events inside the call, so all of a call's work is still ordered on
+ *     `stream`.
  *   - Arguments are validated before anything is launched; a rejected call
  *     launches nothing and returns a negative qlora_status.
  *   - A kernel whose internal wait runs out (it never should) records
@@ -99,8 +103,10 @@ int32_t qlora_version(void);
 
 /* Bytes of device workspace that qlora_linear_fwd and qlora_linear_bwd need
  * for this weight shape, M and rank (the larger of the two).  0 on invalid
- * arguments.  The workspace holds the scaled adapter activations s*T, s*U
- * (bf16) and fp32 partial sums of the split reductions. */
+ * arguments.  The workspace holds the scaled adapter activation s*T or s*U
+ * (bf16) and, for the backward pass, U = dY B and T_save as bf16 hi / lo
+ * pairs.  Its contents need no initialisation and are not kept between
+ * calls; calls that may overlap on the GPU need separate workspaces. */
 size_t qlora_workspace_bytes(const qlora_weight_desc* w, int64_t M, int32_t rank);
 
 /* Decode the whole base weight to bf16: W_bf16[N*K] (device, caller-owned)
@@ -123,8 +129,9 @@ int32_t qlora_linear_fwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
 /* Backward: dX[M x K] = dY deq(Wq) + s (dY B) A;  dA[rank x K] (fp32) =
  * s (dY B)^T X;  dB[N x rank] (fp32) = s dY^T T_save.  dX may be NULL (then
  * only dA and dB are produced).  T_save is the forward's fp32 output.  U = dY B
- * is kept in fp32 for dA; the adapter term of dX enters through bf16(s U).
- * The base is never written. */
+ * and T_save enter dA and dB as bf16 hi / lo pairs (~16 significant bits);
+ * the adapter term of dX enters through bf16(s U).  The base is never
+ * written. */
 int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha,
                          const void* X, const void* A, const void* B,
                          const float* T_save, const void* dY,
