@@ -189,7 +189,9 @@ int32_t grouped_moe_qlora_bwd(const qlora_weight_desc* experts, int32_t E,
  * decoder layer at a time, prefetched one ahead on a dedicated CUDA stream").
  *
  * qlora_stream_create: allocates `slots` device buffers of `slot_bytes` each
- *   (the only memory this library allocates), a copy stream and events.
+ *   (the only device memory this library allocates at run time; the
+ *   no-alloc forward's scratch is a fixed array in the library's image), a
+ *   copy stream and events.
  * qlora_stream_prefetch: announce that `layer` is needed next.  If it is
  *   still resident nothing is copied; otherwise enqueue the host->device copy
  *   of `bytes` bytes at `host_src` (pinned host memory, valid until the copy
