@@ -232,14 +232,29 @@ __device__ __forceinline__ void load_line(const WeightView& v, int64_t line, Raw
       const int64_t grp = v.dq_shift >= 0 ? (line >> v.dq_shift) : line / v.dq_group;
       r.scale = __ldg(v.absmax_scale + grp);
     }
-  } else if constexpr (FMT == FMT_Q8_0) {
-    const uint8_t* p = v.data + line * 68;
+  } else if constexpr (FMT == FMT_Q8_0 || FMT == FMT_Q4_0) {
+    // 68- or 36-byte lines of a 16-byte aligned array: a line starts 8-byte
+    // aligned when its index is even and is 8-byte aligned from its second
+    // word otherwise, so it takes 8-byte loads and one 4-byte load
+    constexpr int WORDS = FMT == FMT_Q8_0 ? 17 : 9;
+    const uint8_t* p = v.data + line * (4 * WORDS);
+    if ((line & 1) == 0) {
 #pragma unroll
-    for (int i = 0; i < 17; ++i) r.w[i] = ldg_nc_u32(p + 4 * i);
-  } else if constexpr (FMT == FMT_Q4_0) {
-    const uint8_t* p = v.data + line * 36;
+      for (int i = 0; i < WORDS / 2; ++i) {
+        const uint2 w = ldg_nc_v2(p + 8 * i);
+        r.w[2 * i] = w.x;
+        r.w[2 * i + 1] = w.y;
+      }
+      r.w[WORDS - 1] = ldg_nc_u32(p + 4 * (WORDS - 1));
+    } else {
+      r.w[0] = ldg_nc_u32(p);
 #pragma unroll
-    for (int i = 0; i < 9; ++i) r.w[i] = ldg_nc_u32(p + 4 * i);
+      for (int i = 0; i < WORDS / 2; ++i) {
+        const uint2 w = ldg_nc_v2(p + 4 + 8 * i);
+        r.w[1 + 2 * i] = w.x;
+        r.w[2 + 2 * i] = w.y;
+      }
+    }
   } else {  // BF16: 128 bytes
     const uint4* p = reinterpret_cast<const uint4*>(v.data + line * 128);
 #pragma unroll
