@@ -316,3 +316,77 @@ def test_grouped_reduces_to_dense():
     assert np.allclose(g3["dA"].sum(0), gd["dA"], rtol=1e-12, atol=1e-12)
     assert np.allclose(g3["dB"].sum(0), gd["dB"], rtol=1e-12, atol=1e-12)
     assert np.all(g3["dA"][1] == 0) and np.all(g3["dB"][1] == 0)
+
+
+def _expert_of_row(offsets, m):
+    """Expert that owns sorted row m: the e with offsets[e] <= m < offsets[e + 1]."""
+    for e in range(len(offsets) - 1):
+        if offsets[e] <= m < offsets[e + 1]:
+            return e
+    raise AssertionError(m)
+
+
+def test_grouped_distinct_experts_against_row_loops():
+    # every expert has its own W, A and B; expert 1 (in the middle) and the
+    # last expert own no rows.  Each row is recomputed with plain loops from
+    # the tensors of the expert that owns it; every expert's dA / dB is the
+    # sum over exactly its own rows (zero for the empty ones).
+    rng = np.random.default_rng(21)
+    M, K, N, r, E = 9, 5, 4, 2, 5
+    off = [0, 3, 3, 7, 9, 9]
+    X = rng.standard_normal((M, K))
+    dY = rng.standard_normal((M, N))
+    Ws = [rng.standard_normal((N, K)) * (e + 1) for e in range(E)]
+    A = rng.standard_normal((E, r, K))
+    B = rng.standard_normal((E, N, r))
+    alpha = 3.0
+    s = alpha / r
+    Y, T = oracle.grouped_fwd(X, Ws, A, B, off, alpha)
+    g = oracle.grouped_bwd(X, Ws, A, B, dY, off, alpha)
+    dA_ref = np.zeros((E, r, K))
+    dB_ref = np.zeros((E, N, r))
+    for m in range(M):
+        e = _expert_of_row(off, m)
+        W, Ae, Be = Ws[e], A[e], B[e]
+        t = [sum(X[m, k] * Ae[q, k] for k in range(K)) for q in range(r)]
+        u = [sum(dY[m, n] * Be[n, q] for n in range(N)) for q in range(r)]
+        for q in range(r):
+            assert math.isclose(T[m, q], t[q], rel_tol=1e-12, abs_tol=1e-12)
+        for n in range(N):
+            y = sum(X[m, k] * W[n, k] for k in range(K)) + s * sum(t[q] * Be[n, q] for q in range(r))
+            assert math.isclose(Y[m, n], y, rel_tol=1e-12, abs_tol=1e-12), (m, n)
+        for k in range(K):
+            dx = sum(dY[m, n] * W[n, k] for n in range(N)) + s * sum(u[q] * Ae[q, k] for q in range(r))
+            assert math.isclose(g["dX"][m, k], dx, rel_tol=1e-12, abs_tol=1e-12), (m, k)
+        for q in range(r):
+            for k in range(K):
+                dA_ref[e, q, k] += s * u[q] * X[m, k]
+            for n in range(N):
+                dB_ref[e, n, q] += s * dY[m, n] * t[q]
+    assert np.allclose(g["dA"], dA_ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(g["dB"], dB_ref, rtol=1e-12, atol=1e-12)
+    for e in (1, 4):
+        assert np.all(g["dA"][e] == 0) and np.all(g["dB"][e] == 0)
+
+
+def test_grouped_hand_worked_two_experts():
+    # K = N = 1, r = 1, alpha = 1 (s = 1).  Expert 0: W = 2, A = 1, B = 3 owns
+    # row 0 (x = 1, dy = 1); expert 1: W = -1, A = 2, B = 0.5 owns rows 1, 2
+    # (x = 1, 2; dy = 2, -1).
+    #   row 0: T = 1,  Y = 2 + 1*3 = 5,        U = 3,   dX = 2 + 3*1 = 5
+    #   row 1: T = 2,  Y = -1 + 2*0.5 = 0,     U = 1,   dX = -2 + 1*2 = 0
+    #   row 2: T = 4,  Y = -2 + 4*0.5 = 0,     U = -0.5, dX = 1 - 0.5*2 = 0
+    #   dA0 = 3*1 = 3, dB0 = 1*1 = 1;  dA1 = 1*1 - 0.5*2 = 0, dB1 = 2*2 - 1*4 = 0
+    X = np.array([[1.0], [1.0], [2.0]])
+    dY = np.array([[1.0], [2.0], [-1.0]])
+    Ws = [np.array([[2.0]]), np.array([[-1.0]])]
+    A = np.array([[[1.0]], [[2.0]]])
+    B = np.array([[[3.0]], [[0.5]]])
+    off = [0, 1, 3]
+    Y, T = oracle.grouped_fwd(X, Ws, A, B, off, 1.0)
+    g = oracle.grouped_bwd(X, Ws, A, B, dY, off, 1.0)
+    assert np.array_equal(T.reshape(-1), [1.0, 2.0, 4.0])
+    assert np.array_equal(Y.reshape(-1), [5.0, 0.0, 0.0])
+    assert np.array_equal(g["dX"].reshape(-1), [5.0, 0.0, 0.0])
+    assert np.array_equal(g["dA"].reshape(-1), [3.0, 0.0])
+    assert np.array_equal(g["dB"].reshape(-1), [1.0, 0.0])
