@@ -197,14 +197,17 @@ int32_t grouped_moe_qlora_bwd(const qlora_weight_desc* experts, int32_t E,
  *   of `bytes` bytes at `host_src` (pinned host memory, valid until the copy
  *   ran) into the least recently used slot that is neither acquired nor
  *   holding an announced, not yet acquired layer, tagged with `layer`.  The
- *   copy waits until every earlier compute-stream use of that slot was
- *   released.  QLORA_ERR_STATE if no slot is free (prefetching too far ahead),
+ *   copy waits for the work enqueued before every release of that slot since
+ *   it was last filled, on whichever streams those releases named (a layer
+ *   acquired on several unordered streams is overwritten only after all of
+ *   them).  QLORA_ERR_STATE if no slot is free (prefetching too far ahead),
  *   QLORA_ERR_INVALID if `bytes` exceeds the slot size.
  * qlora_stream_acquire: make `compute_stream` wait for the copy of `layer`
  *   and return the slot's device address in *dev_ptr.  QLORA_ERR_STATE if no
  *   slot holds `layer` (never prefetched, or already overwritten).
  * qlora_stream_release: record on `compute_stream` that work reading `layer`
- *   has been enqueued; the slot may be refilled after that work.
+ *   has been enqueued (one release per acquire); the slot may be refilled
+ *   after that work and the work of the slot's other releases.
  * qlora_stream_destroy: synchronise and free everything. */
 int32_t qlora_stream_create(int32_t slots, size_t slot_bytes, void** handle);
 int32_t qlora_stream_prefetch(void* handle, int32_t layer, const void* host_src, size_t bytes);
@@ -216,6 +219,26 @@ int32_t qlora_stream_destroy(void* handle);
  * Call after synchronising the streams the library used.  clear != 0 resets
  * it.  This call synchronises the device. */
 int32_t qlora_device_error(int32_t clear);
+
+/* Stream-ordered read of the same word (the call list's
+ * qlora_last_device_error): enqueues a device->host copy of the word on
+ * `stream`, waits for that stream only (no device-wide synchronisation) and
+ * returns the value, i.e. any error recorded by work enqueued on `stream`
+ * before this call (including the backward call's side-stream work, which is
+ * joined back into the caller's stream).  The word is shared by all streams
+ * of the device, so an error recorded by another stream's finished work is
+ * reported too.  clear != 0 resets the word (stream-ordered) when it was
+ * set. */
+int32_t qlora_last_device_error(void* stream, int32_t clear);
+
+/* Diagnostic of the bounded-wait error path: launches on `stream` one warp
+ * that waits, for at most limit_ns nanoseconds (1 .. 1e9), on an mbarrier
+ * phase that nothing completes.  The wait runs out, records
+ * QLORA_ERR_TIMEOUT in the device error word and the kernel returns; the
+ * context stays usable.  Returns QLORA_OK once launched, QLORA_ERR_INVALID for
+ * a limit outside the range.  No counterpart on the pages: it exists so a
+ * test can check that a device wait that runs out ends as an error status. */
+int32_t qlora_selftest_bounded_wait(int64_t limit_ns, void* stream);
 
 /* Number of this library's kernels launched since load (host-side count). */
 int64_t qlora_launch_count(void);

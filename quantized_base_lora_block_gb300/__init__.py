@@ -71,6 +71,8 @@ SIGNATURES = {
     "qlora_stream_release": (_I32, [_P, _I32, _P]),
     "qlora_stream_destroy": (_I32, [_P]),
     "qlora_device_error": (_I32, [_I32]),
+    "qlora_last_device_error": (_I32, [_P, _I32]),
+    "qlora_selftest_bounded_wait": (_I32, [_I64, _P]),
     "qlora_launch_count": (_I64, []),
     "qlora_linear_fwd_noalloc": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P]),
     "qlora_noalloc_scratch_bytes": (_SZ, []),
@@ -326,6 +328,17 @@ def stack_bf16_weights(weights: Sequence[Dict], device="cuda") -> List[DeviceWei
 
 def device_error(clear: bool = True) -> int:
     return int(load().qlora_device_error(1 if clear else 0))
+
+
+def last_device_error(stream=None, clear: bool = True) -> int:
+    """The device error word as of the end of `stream`'s enqueued work (waits
+    for that stream only)."""
+    return int(load().qlora_last_device_error(_stream_ptr(stream), 1 if clear else 0))
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Launch the diagnostic wait that runs out after limit_ns (see qlora.h)."""
+    _check("qlora_selftest_bounded_wait", load().qlora_selftest_bounded_wait(int(limit_ns), _stream_ptr(stream)))
 
 
 def launch_count() -> int:

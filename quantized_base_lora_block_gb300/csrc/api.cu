@@ -544,6 +544,22 @@ int32_t qlora_device_error(int32_t clear) {
   return v;
 }
 
+int32_t qlora_last_device_error(void* stream, int32_t clear) {
+  // stream-ordered read: the copy runs after the stream's earlier work, and
+  // only this stream is waited for
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* word = device_error_word();
+  if (!word) return QLORA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyAsync(&v, word, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return QLORA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return QLORA_ERR_CUDA;
+  if (clear && v != 0) {
+    if (cudaMemsetAsync(word, 0, sizeof(int), st) != cudaSuccess) return QLORA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return QLORA_ERR_CUDA;
+  }
+  return v;
+}
+
 size_t qlora_workspace_bytes(const qlora_weight_desc* w, int64_t M, int32_t rank) {
   if (validate_weight(w) != QLORA_OK || validate_rank(rank) != QLORA_OK || M < 0) return 0;
   if (M == 0) return 256;

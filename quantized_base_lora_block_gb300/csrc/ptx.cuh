@@ -64,17 +64,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // false if it has not completed after kWaitNs (recording QLORA_ERR_TIMEOUT in
 // *err, the device error word, and raising this CTA's abort flag), or as soon
 // as another role of this CTA has raised the abort flag.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* err) {
+// The limit is a parameter so that a diagnostic kernel can run a wait with a
+// short limit out on purpose; every other wait passes kWaitNs.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, volatile int* abort, int* err,
+                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitNs) break;
+    if (globaltimer_ns() - t0 > limit_ns) break;
   }
   if (err) atomicExch(err, kErrTimeout);
   *abort = 1;
   return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* err) {
+  return mbar_wait_for(bar, parity, abort, err, kWaitNs);
 }
 
 // Bounded wait used only while retiring: waits for in-flight copies even if

@@ -27,11 +27,14 @@ struct StreamPool {
   size_t slot_bytes = 0;
   uint8_t* dev = nullptr;
   cudaStream_t copy = nullptr;
-  std::vector<cudaEvent_t> ready, freed;
+  std::vector<cudaEvent_t> ready;
+  // one event per release since the slot was last filled: a slot acquired on
+  // several unordered streams is refilled only after every one of them
+  std::vector<std::vector<cudaEvent_t>> released;
+  std::vector<cudaEvent_t> spare;  // recycled release events
   std::vector<int> layer;     // layer held by the slot, -1 = none
   std::vector<int> acquired;  // compute work holding the slot not yet released
   std::vector<int> pending;   // announced by prefetch, not yet acquired
-  std::vector<int> freed_valid;
   std::vector<uint64_t> last_use;
   uint64_t clock = 0;
   std::mutex mu;
@@ -59,15 +62,11 @@ int32_t qlora_stream_create(int32_t slots, size_t slot_bytes, void** handle) {
     return QLORA_ERR_CUDA;
   }
   p->ready.resize(slots);
-  p->freed.resize(slots);
-  for (int i = 0; i < slots; ++i) {
-    cudaEventCreateWithFlags(&p->ready[i], cudaEventDisableTiming);
-    cudaEventCreateWithFlags(&p->freed[i], cudaEventDisableTiming);
-  }
+  p->released.resize(slots);
+  for (int i = 0; i < slots; ++i) cudaEventCreateWithFlags(&p->ready[i], cudaEventDisableTiming);
   p->layer.assign(slots, -1);
   p->acquired.assign(slots, 0);
   p->pending.assign(slots, 0);
-  p->freed_valid.assign(slots, 0);
   p->last_use.assign(slots, 0);
   *handle = p;
   return QLORA_OK;
@@ -90,8 +89,12 @@ int32_t qlora_stream_prefetch(void* handle, int32_t layer, const void* host_src,
     if (victim < 0 || p->last_use[i] < p->last_use[victim]) victim = i;
   }
   if (victim < 0) return QLORA_ERR_STATE;  // every slot is in use or pending
-  if (p->freed_valid[victim] && cudaStreamWaitEvent(p->copy, p->freed[victim], 0) != cudaSuccess)
-    return QLORA_ERR_CUDA;
+  // the refill waits for every use of the slot released since its last fill
+  for (cudaEvent_t e : p->released[victim])
+    if (cudaStreamWaitEvent(p->copy, e, 0) != cudaSuccess) return QLORA_ERR_CUDA;
+  // the copy stream now holds the waits: the events may be recorded again
+  for (cudaEvent_t e : p->released[victim]) p->spare.push_back(e);
+  p->released[victim].clear();
   p->layer[victim] = -1;
   if (cudaMemcpyAsync(p->dev + (size_t)victim * p->slot_bytes, host_src, bytes, cudaMemcpyHostToDevice, p->copy) !=
       cudaSuccess)
@@ -127,9 +130,18 @@ int32_t qlora_stream_release(void* handle, int32_t layer, void* compute_stream) 
   std::lock_guard<std::mutex> g(p->mu);
   for (int i = 0; i < p->slots; ++i) {
     if (p->layer[i] != layer || p->acquired[i] == 0) continue;
-    if (cudaEventRecord(p->freed[i], static_cast<cudaStream_t>(compute_stream)) != cudaSuccess)
+    cudaEvent_t e = nullptr;
+    if (!p->spare.empty()) {
+      e = p->spare.back();
+      p->spare.pop_back();
+    } else if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
       return QLORA_ERR_CUDA;
-    p->freed_valid[i] = 1;
+    }
+    if (cudaEventRecord(e, static_cast<cudaStream_t>(compute_stream)) != cudaSuccess) {
+      p->spare.push_back(e);
+      return QLORA_ERR_CUDA;
+    }
+    p->released[i].push_back(e);
     p->acquired[i] -= 1;
     return QLORA_OK;
   }
@@ -141,10 +153,13 @@ int32_t qlora_stream_destroy(void* handle) {
   if (!p) return QLORA_ERR_INVALID;
   cudaStreamSynchronize(p->copy);
   for (int i = 0; i < p->slots; ++i) {
-    if (p->freed_valid[i]) cudaEventSynchronize(p->freed[i]);
+    for (cudaEvent_t e : p->released[i]) {
+      cudaEventSynchronize(e);
+      cudaEventDestroy(e);
+    }
     cudaEventDestroy(p->ready[i]);
-    cudaEventDestroy(p->freed[i]);
   }
+  for (cudaEvent_t e : p->spare) cudaEventDestroy(e);
   cudaStreamDestroy(p->copy);
   cudaFree(p->dev);
   delete p;

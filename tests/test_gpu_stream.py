@@ -115,3 +115,47 @@ def test_pool_rejects_misuse(lib):
     pool.release(1)
     torch.cuda.synchronize()
     pool.close()
+
+
+def test_refill_waits_for_every_stream_that_released(lib):
+    """One layer acquired on two unordered streams and released from both:
+    the next refill of its slot must wait for the work of both releases,
+    not only the last one.  The first stream's read of the slot is delayed
+    by a device-side sleep, so a refill that waited only for the second
+    stream would land before that read and change its result."""
+    import torch
+
+    wl = syn.Workload("refill", "q8_0", False, 64, 16, 32.0, [syn.Linear("l", 1024, 2048)])
+    l0 = syn.make_linear_inputs(wl, 0, seed=1, layer=0)
+    l1 = syn.make_linear_inputs(wl, 0, seed=2, layer=1)
+    b0, o0 = lib.pack_weight_blob(l0["W"])
+    b1, o1 = lib.pack_weight_blob(l1["W"])
+    h0, h1 = torch.from_numpy(b0).pin_memory(), torch.from_numpy(b1).pin_memory()
+    want = lib.dequant_blocks(lib.DeviceWeight.from_packed(l0["W"]))
+    pool = lib.LayerStream(1, max(b0.nbytes, b1.nbytes))
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    pool.prefetch(0, h0)
+    base1 = pool.acquire(0, s1)
+    base2 = pool.acquire(0, s2)
+    w1 = lib.weight_in_slot(l0["W"], o0, base1)
+    w2 = lib.weight_in_slot(l0["W"], o0, base2)
+    out1 = torch.empty_like(want)
+    out2 = torch.empty_like(want)
+    with torch.cuda.stream(s1):
+        torch.cuda._sleep(200_000_000)        # ~0.1 s of device time before the read
+    lib.dequant_blocks(w1, out=out1, stream=s1)
+    pool.release(0, s1)
+    lib.dequant_blocks(w2, out=out2, stream=s2)
+    pool.release(0, s2)
+    pool.prefetch(1, h1)                      # refills the only slot
+    base = pool.acquire(1)
+    torch.cuda.current_stream().wait_stream(s1)
+    torch.cuda.current_stream().wait_stream(s2)
+    got1 = lib.dequant_blocks(lib.weight_in_slot(l1["W"], o1, base))
+    pool.release(1)
+    torch.cuda.synchronize()
+    pool.close()
+    assert torch.equal(out1.view(torch.int16), want.view(torch.int16)), "slow stream read the refilled slot"
+    assert torch.equal(out2.view(torch.int16), want.view(torch.int16))
+    assert torch.equal(got1.view(torch.int16),
+                       lib.dequant_blocks(lib.DeviceWeight.from_packed(l1["W"])).view(torch.int16))
