@@ -12,7 +12,7 @@
 // bf16 values are computed once (16 fp32 multiplies + 8 conversions) and split
 // into a low-byte and a high-byte plane of 16 bytes each (4 registers each).
 // Each 4-bit code then picks its two bytes with byte permutes (prmt), so the
-// per-element work is a handful of integer ops and no memory lookup.
+// per-element work is about two integer ops and no memory lookup.
 #pragma once
 
 #include <cstdint>
@@ -84,17 +84,26 @@ __device__ __forceinline__ Lut16 lut_q4_0(float d) {
   return lut_from_pairs(pairs);
 }
 
-// Look up 4 codes held in the 4 nibbles of s (bits 0..15): byte i of *L / *H
-// receives the low / high byte of entry (nibble i).
-__device__ __forceinline__ void lut_lookup4(const Lut16& t, uint32_t s, uint32_t& L, uint32_t& H) {
-  const uint32_t sel = s & 0x7777u;
-  const uint32_t m = prmt(0x0000FF00u, 0u, (s >> 3) & 0x1111u);  // 0xFF where code >= 8
-  const uint32_t la = prmt(t.lo[0], t.lo[1], sel);
-  const uint32_t lb = prmt(t.lo[2], t.lo[3], sel);
-  const uint32_t ha = prmt(t.hi[0], t.hi[1], sel);
-  const uint32_t hb = prmt(t.hi[2], t.hi[3], sel);
-  L = (la & ~m) | (lb & m);
-  H = (ha & ~m) | (hb & m);
+// Look up the 8 codes held in the 8 nibbles of w.  For the 4 codes of half h
+// (nibbles 4h .. 4h+3), byte i of L[h] / H[h] receives the low / high byte of
+// entry (code i).  Each half takes 4 byte permutes to fetch the candidates
+// from entries 0..7 and 8..15 (selected by a code's low 3 bits) and 2 more to
+// keep, per byte, the candidate its top bit names; the selectors of both
+// halves come from one mask and one shift of the whole word.
+__device__ __forceinline__ void lut_lookup8(const Lut16& t, uint32_t w, uint32_t (&L)[2], uint32_t (&H)[2]) {
+  const uint32_t idx = w & 0x77777777u;                          // low 3 bits of each code
+  const uint32_t pick = ((w >> 1) & 0x44444444u) | 0x32103210u;  // byte i of a (code < 8) or of b
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t sel = h ? (idx >> 16) : idx;  // prmt reads the low 16 bits of its selector
+    const uint32_t sel2 = h ? (pick >> 16) : pick;
+    const uint32_t la = prmt(t.lo[0], t.lo[1], sel);
+    const uint32_t lb = prmt(t.lo[2], t.lo[3], sel);
+    const uint32_t ha = prmt(t.hi[0], t.hi[1], sel);
+    const uint32_t hb = prmt(t.hi[2], t.hi[3], sel);
+    L[h] = prmt(la, lb, sel2);
+    H[h] = prmt(ha, hb, sel2);
+  }
 }
 
 // ---------------------------------------------------------------- NF4 -------
@@ -104,13 +113,13 @@ __device__ __forceinline__ void decode_nf4_line(const uint4 c0, const uint4 c1, 
   const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    uint32_t L, H, r[4];
+    uint32_t L[2], H[2], r[4];
+    lut_lookup8(t, w[j], L, H);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      lut_lookup4(t, w[j] >> (16 * h), L, H);
       // byte order of L/H: e(4h+1), e(4h+0), e(4h+3), e(4h+2)
-      r[2 * h + 0] = prmt(L, H, 0x4051);  // elements 4h+0, 4h+1
-      r[2 * h + 1] = prmt(L, H, 0x6273);  // elements 4h+2, 4h+3
+      r[2 * h + 0] = prmt(L[h], H[h], 0x4051);  // elements 4h+0, 4h+1
+      r[2 * h + 1] = prmt(L[h], H[h], 0x6273);  // elements 4h+2, 4h+3
     }
     out[j] = make_uint4(r[0], r[1], r[2], r[3]);
   }
@@ -124,13 +133,13 @@ __device__ __forceinline__ void decode_q4_0_block(uint32_t d_bits, const uint32_
   uint32_t lowp[8], highp[8];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
+    uint32_t L[2], H[2];
+    lut_lookup8(t, qs[q], L, H);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      uint32_t L, H;
-      lut_lookup4(t, qs[q] >> (16 * h), L, H);
       // byte order: e(4q+2h), e(16+4q+2h), e(4q+2h+1), e(16+4q+2h+1)
-      lowp[2 * q + h] = prmt(L, H, 0x6240);
-      highp[2 * q + h] = prmt(L, H, 0x7351);
+      lowp[2 * q + h] = prmt(L[h], H[h], 0x6240);
+      highp[2 * q + h] = prmt(L[h], H[h], 0x7351);
     }
   }
   out4[0] = make_uint4(lowp[0], lowp[1], lowp[2], lowp[3]);
