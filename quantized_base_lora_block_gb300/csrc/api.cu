@@ -285,8 +285,7 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
          map2d(&maps.lb, lb, K, rank, 64, 64);
     if (w->fmt == QLORA_FMT_BF16) ok = ok && map2d(&maps.w, w->data, K, N, 64, 64);
   }
-  // pair kernel epilogue: one 32-row x 64-column TMA store per warp and chunk
-  if (pair) ok = ok && map2d(&maps.out, out, dx ? K : N, M, 64, 32);
+  if (pair) ok = ok && map2d(&maps.out, out, dx ? K : N, M, 64, 128);
   // NF4 on 512 x 256 pair tiles: code bytes [N x K/2] through the raw ring,
   // one box per item (forward: 128 weight rows x one 64-element block; dX:
   // 64 weight rows x the CTA's two blocks)

@@ -94,13 +94,12 @@ struct __align__(8) PairBarriers {
   uint64_t raw_empty[4];                  // raw ring: the decode group has read them (this CTA)
   uint32_t tmem_base;
   int abort;
+  int ep_ok;  // epilogue: result of the "accumulator full" wait, for all 4 warps
 };
 
-// epilogue staging: 128-row x 64-column bf16 chunks (128B-swizzled), one
-// 32-row quarter per epilogue warp, each quarter written out with its own
-// TMA tensor store
+// epilogue staging: 128-row x 64-column bf16 chunks (128B-swizzled), each
+// written out with a TMA tensor store
 constexpr int P_STAGE_OUT_BYTES = 128 * 64 * 2;
-constexpr int P_WARP_OUT_BYTES = 32 * 64 * 2;
 
 template <int FMT, int CFG, bool DX>
 constexpr size_t p_smem_bytes() {
@@ -314,21 +313,17 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
-    // Each of the 4 warps drains its own 32 TMEM lanes (32 output rows) with
-    // no synchronisation between the warps.  Per 64-column chunk a thread
-    // converts its row's values to bf16 and writes them as one 128-byte row
-    // of the warp's own 32 x 64 staging tile (128B-swizzled, conflict-free),
-    // 32 columns at a time, each half's registers refilled at once by the
-    // next chunk's TMEM load so that load lands while this chunk is staged;
-    // one lane then stores the tile with a TMA tensor store.  The
-    // accumulator is released as soon as its last TMEM load has completed,
-    // so the next tile's MMAs start while the last chunk is still being
-    // staged.  Chunks wholly outside the output are not stored.
+    // Per 64-column chunk: each thread loads its row's 64 fp32 values from
+    // TMEM, converts them to bf16 and writes one 128-byte row of a
+    // 128B-swizzled staging tile (conflict-free); one thread then stores the
+    // 128 x 64 tile with a TMA tensor store.  With two staging tiles the
+    // store of one chunk overlaps the conversion of the next.  Chunks wholly
+    // outside the output are neither staged nor stored.
     const int quarter = warp & 3;
-    const int swz = lane & 7;
-    const uint32_t wstage = sOut + (uint32_t)quarter * (Raw::OUT_BUFS * P_WARP_OUT_BYTES);
-    constexpr int NCH = TN / 64;
-    uint32_t nstored = 0;  // chunks this warp stored so far (selects the staging tile)
+    const int row_in_tile = quarter * 32 + lane;
+    const int ep = (warp - 2) * 32 + lane;  // 0..127
+    const int swz = row_in_tile & 7;
+    uint32_t nstored = 0;  // chunks stored so far (selects the staging tile)
     for (int lt = 0; lt < my_tiles; ++lt) {
       const PairTile tc = pair_tile<DX, CFG>(args, pair + lt * num_pairs);
       const int buf = lt % NBUF;
@@ -337,72 +332,61 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
 #pragma unroll 1
       for (int a = 0; a < NACC && ok; ++a) {
         const int slot = buf * NACC + a;
-        if (lane == 0) ok = mbar_wait_cluster(smem_u32(&bars->acc_full[slot]), aph, abort, args.err);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        // one thread waits; all four warps take the same decision (they meet
+        // at named barriers below, which must never be left half-entered)
+        if (ep == 0) bars->ep_ok = mbar_wait_cluster(smem_u32(&bars->acc_full[slot]), aph, abort, args.err) ? 1 : 0;
+        named_bar(1, 128);
+        ok = *reinterpret_cast<volatile int*>(&bars->ep_ok) != 0;
+        named_bar(1, 128);  // everyone has read ep_ok before it is rewritten
         if (!ok) break;
         tc_fence_after();
-        const int row0 = tc.m0 + 256 * a + 128 * (int)rank + 32 * quarter;  // this warp's first row
-        const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * (NACC * TN) + a * TN;
-        uint32_t v[64];
-        tmem_ld_32x32b_x32(tcol, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld_32x32b_x32(tcol + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-        tc_wait_ld();
-        // fully unrolled, so the registers a TMEM load fills are only read
-        // after the wait that completes it (no loop-carried copies)
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          const bool last = c + 1 == NCH;
-          if (last) {
-            // every load of this accumulator has completed: release it
+        const int row0 = tc.m0 + 256 * a + 128 * (int)rank;
+#pragma unroll 1
+        for (int c = 0; c < TN / 64; ++c) {
+          uint32_t v0[32], v1[32];
+          const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * (NACC * TN) + a * TN + c * 64;
+          tmem_ld_32x32b_x32(tcol, v0);
+          tmem_ld_32x32b_x32(tcol + 32, v1);
+          tc_wait_ld();
+          if (c == TN / 64 - 1) {
+            // every value of this accumulator is in registers: release it
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[slot]), 0));
           }
-          const bool store = row0 < args.M && tc.n0 + 64 * c < args.n_out;  // the same for the whole warp
-          const uint32_t stile = wstage + (nstored % Raw::OUT_BUFS) * P_WARP_OUT_BYTES;
-          if (store) {
-            ++nstored;
-            if (lane == 0) {  // the store that last read this staging tile is done with it
-              if (Raw::OUT_BUFS == 2)
-                bulk_wait_read1();
-              else
-                bulk_wait_read0();
-            }
-            __syncwarp();
+          // the same for all 128 threads
+          if (row0 >= args.M || tc.n0 + 64 * c >= args.n_out) continue;
+          const uint32_t stile = sOut + (nstored % Raw::OUT_BUFS) * P_STAGE_OUT_BYTES;
+          ++nstored;
+          if (ep == 0) {  // the store that last read this staging tile is done with it
+            if (Raw::OUT_BUFS == 2)
+              bulk_wait_read1();
+            else
+              bulk_wait_read0();
           }
-          const uint32_t srow = stile + (uint32_t)lane * 128;
-          // each half: convert and stage 32 columns, then reuse its registers
-          // for the next chunk's TMEM load, which lands while the rest of
-          // this chunk is staged and stored
+          named_bar(1, 128);
+          const uint32_t srow = stile + (uint32_t)row_in_tile * 128;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (store) {
-#pragma unroll
-              for (int q = 4 * h; q < 4 * h + 4; ++q) {
-                const uint32_t* w = v + 8 * q;
-                sts_v4(srow + ((q ^ swz) << 4),
-                       make_uint4(pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
-                                  pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
-                                  pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
-                                  pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7]))));
-              }
-            }
-            if (!last) tmem_ld_32x32b_x32(tcol + 64 * (c + 1) + 32 * h, *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t* v = q < 4 ? v0 + 8 * q : v1 + 8 * (q - 4);
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+            o.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+            o.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+            o.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+            sts_v4(srow + ((q ^ swz) << 4), o);
           }
-          if (store) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tm_out, stile, tc.n0 + 64 * c, row0);
-              bulk_commit();
-            }
+          fence_proxy_async_smem();
+          named_bar(1, 128);
+          if (ep == 0) {
+            tma_store_2d(&tm_out, stile, tc.n0 + 64 * c, row0);
+            bulk_commit();
           }
-          if (!last) tc_wait_ld();
         }
       }
       if (!ok) break;
     }
-    if (lane == 0) bulk_wait0();
+    if (ep == 0) bulk_wait0();
   } else if (FMT != FMT_BF16 && warp < 6 + Cfg::DQ_WARPS) {
     // ------------------------------------------------------------ decode
     // group g (GROUP_WARPS warps) handles the items with it % GROUPS == g;

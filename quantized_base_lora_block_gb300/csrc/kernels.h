@@ -151,7 +151,7 @@ struct GemmArgs {
 // index outermost.
 struct GemmMaps {
   CUtensorMap a, w, la, lb;
-  CUtensorMap out;  // pair kernel: bf16 output [M x n_out], box [64 x 32] (TMA stores, one per warp)
+  CUtensorMap out;  // pair kernel: bf16 output [M x n_out], box [64 x 128] (TMA stores)
   CUtensorMap aq;   // pair kernel, NF4 dX with raw_dq: int8 absmax codes [N x K/64], box [16 x 64]
 };
 

@@ -151,7 +151,7 @@ def test_refill_waits_for_every_stream_that_released(lib):
     base = pool.acquire(1)
     torch.cuda.current_stream().wait_stream(s1)
     torch.cuda.current_stream().wait_stream(s2)
-    got1 = lib.dequant_blocks(lib.weight_in_slot(l1["W"], o1, base))
+    got1 = lib.dequant_blocks(lib.weight_in_slot(l1["W"], o1, base), out=torch.empty_like(want))
     pool.release(1)
     torch.cuda.synchronize()
     pool.close()
