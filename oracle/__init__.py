@@ -17,4 +17,6 @@ from .qlora_oracle import (  # noqa: F401
     linear_bwd_adapter_grads,
     grouped_fwd,
     grouped_bwd,
+    multi_linear_fwd,
+    multi_linear_bwd,
 )

@@ -223,3 +223,32 @@ def grouped_bwd(X, Wds: Sequence[np.ndarray], A, B, dY, offsets, alpha: float):
             g = linear_bwd(X[lo:hi], Wds[e], A[e], B[e], dY[lo:hi], alpha)
             dX[lo:hi], dA[e], dB[e] = g["dX"], g["dA"], g["dB"]
     return {"dX": dX, "dA": dA, "dB": dB}
+
+
+# ----------------------------------------------------------------------------
+# fused projections that share their input (q, k, v of attention; gate, up of
+# the MLP): P LoRA linears over the same X, each with its own base rows and
+# adapter, computed as one call.  Y is the projections' outputs side by side;
+# the input gradient is the sum of the projections' input gradients (what the
+# layer that feeds X receives); dA, dB stay per projection.  (Surogate README,
+# design bullet "Kernels that do more per launch".)
+# ----------------------------------------------------------------------------
+def multi_linear_fwd(X, Wds: Sequence[np.ndarray], As: Sequence[np.ndarray], Bs: Sequence[np.ndarray],
+                     alpha: float):
+    """Returns (Y [M, sum N_p], T [M, P r]) with projection p in its own column block."""
+    outs = [linear_fwd(X, Wd, A, B, alpha) for Wd, A, B in zip(Wds, As, Bs)]
+    return np.concatenate([y for y, _ in outs], axis=1), np.concatenate([t for _, t in outs], axis=1)
+
+
+def multi_linear_bwd(X, Wds: Sequence[np.ndarray], As: Sequence[np.ndarray], Bs: Sequence[np.ndarray], dY,
+                     alpha: float):
+    """dY [M, sum N_p] (projection p in its column block).  Returns dict with dX
+    (summed over projections), dA [P, r, K], dB [sum N_p, r] (projection p's
+    rows in its block), T and U [M, P r]."""
+    dY = _f64(dY)
+    offs = np.cumsum([0] + [np.asarray(W).shape[0] for W in Wds])
+    gs = [linear_bwd(X, Wd, A, B, dY[:, offs[p]:offs[p + 1]], alpha)
+          for p, (Wd, A, B) in enumerate(zip(Wds, As, Bs))]
+    return {"dX": sum(g["dX"] for g in gs), "dA": np.stack([g["dA"] for g in gs]),
+            "dB": np.concatenate([g["dB"] for g in gs], axis=0),
+            "T": np.concatenate([g["T"] for g in gs], axis=1), "U": np.concatenate([g["U"] for g in gs], axis=1)}

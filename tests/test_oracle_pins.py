@@ -390,3 +390,59 @@ def test_grouped_hand_worked_two_experts():
     assert np.array_equal(g["dX"].reshape(-1), [5.0, 0.0, 0.0])
     assert np.array_equal(g["dA"].reshape(-1), [3.0, 0.0])
     assert np.array_equal(g["dB"].reshape(-1), [1.0, 0.0])
+
+
+def test_multi_projection_hand_worked():
+    # K = 2, two projections with N = 1 each, r = 1, alpha = 1 (s = 1):
+    #   X = [1 2];  p0: W = [1 1], A = [1 0], B = [2];  p1: W = [0 -1], A = [0 1], B = [-1]
+    #   T = [1 | 2];  Y = [3 + 1*2 | -2 + 2*(-1)] = [5 | -4]
+    #   dY = [1 | 3]:  U = [2 | -3]
+    #   dX = (dY0 W0 + U0 A0) + (dY1 W1 + U1 A1) = ([1 1] + [2 0]) + ([0 -3] + [0 -3]) = [3 -5]
+    #   dA0 = U0 X = [2 4], dA1 = U1 X = [-3 -6];  dB0 = dY0 T0 = 1, dB1 = dY1 T1 = 6
+    X = np.array([[1.0, 2.0]])
+    Ws = [np.array([[1.0, 1.0]]), np.array([[0.0, -1.0]])]
+    As = [np.array([[1.0, 0.0]]), np.array([[0.0, 1.0]])]
+    Bs = [np.array([[2.0]]), np.array([[-1.0]])]
+    dY = np.array([[1.0, 3.0]])
+    Y, T = oracle.multi_linear_fwd(X, Ws, As, Bs, 1.0)
+    g = oracle.multi_linear_bwd(X, Ws, As, Bs, dY, 1.0)
+    assert np.array_equal(T, [[1.0, 2.0]]) and np.array_equal(Y, [[5.0, -4.0]])
+    assert np.array_equal(g["U"], [[2.0, -3.0]]) and np.array_equal(g["dX"], [[3.0, -5.0]])
+    assert np.array_equal(g["dA"], [[[2.0, 4.0]], [[-3.0, -6.0]]]) and np.array_equal(g["dB"], [[1.0], [6.0]])
+
+
+def test_multi_projection_is_one_linear_with_block_diagonal_adapter():
+    # P projections over X equal one linear over the stacked base rows whose
+    # adapter is A' = [A_0; ...; A_{P-1}] (rank P r) and the block-diagonal B'
+    # (projection p's rows of B' non-zero only in block p); the summed input
+    # gradient is that linear's dX, and dA_p, dB_p are the blocks of its
+    # gradients.  Checked against plain matrix algebra on random tensors.
+    rng = np.random.default_rng(31)
+    M, K, r, Ns = 5, 7, 2, [3, 4, 2]
+    X = rng.standard_normal((M, K))
+    Ws = [rng.standard_normal((n, K)) for n in Ns]
+    As = [rng.standard_normal((r, K)) for _ in Ns]
+    Bs = [rng.standard_normal((n, r)) for n in Ns]
+    dY = rng.standard_normal((M, sum(Ns)))
+    alpha = 3.0
+    s = alpha / r
+    Y, T = oracle.multi_linear_fwd(X, Ws, As, Bs, alpha)
+    g = oracle.multi_linear_bwd(X, Ws, As, Bs, dY, alpha)
+    W = np.concatenate(Ws, axis=0)
+    A = np.concatenate(As, axis=0)
+    Bbd = np.zeros((sum(Ns), len(Ns) * r))
+    o = 0
+    for p, n in enumerate(Ns):
+        Bbd[o:o + n, p * r:(p + 1) * r] = Bs[p]
+        o += n
+    assert np.allclose(T, X @ A.T, rtol=1e-12, atol=1e-12)
+    assert np.allclose(Y, X @ W.T + s * (X @ A.T) @ Bbd.T, rtol=1e-12, atol=1e-12)
+    U = dY @ Bbd
+    assert np.allclose(g["U"], U, rtol=1e-12, atol=1e-12)
+    assert np.allclose(g["dX"], dY @ W + s * U @ A, rtol=1e-12, atol=1e-12)
+    assert np.allclose(g["dA"].reshape(-1, K), s * U.T @ X, rtol=1e-12, atol=1e-12)
+    dBbd = s * dY.T @ T
+    o = 0
+    for p, n in enumerate(Ns):
+        assert np.allclose(g["dB"][o:o + n], dBbd[o:o + n, p * r:(p + 1) * r], rtol=1e-12, atol=1e-12)
+        o += n
