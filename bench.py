@@ -333,6 +333,56 @@ def moe_leg(q, torch, steps, stream):
             "tflops": flops / (ms / 1e3) / 1e12}
 
 
+def fused_groups(wl):
+    """Linears of a decoder layer that share their input and run as one fused
+    launch (q|k|v, gate|up), where the fused call supports them (widths
+    multiples of 256, P rank <= 64); every other linear on its own."""
+    names = [l.name for l in wl.linears]
+    groups, done = [], set()
+    for members in (("q_proj", "k_proj", "v_proj"), ("gate_proj", "up_proj")):
+        idx = [names.index(n) for n in members if n in names]
+        if (len(idx) == len(members) and len(idx) * wl.rank <= 64 and
+                all(wl.linears[i].N % 256 == 0 for i in idx)):
+            groups.append(idx)
+            done.update(idx)
+    for i in range(len(names)):
+        if i not in done:
+            groups.append([i])
+    return sorted(groups, key=lambda g: g[0])
+
+
+def make_units(q, torch, wl, inputs, dev, groups):
+    """Device tensors of each launch unit: the stacked base, the shared input
+    (the first member's X), stacked adapters, concatenated dY, outputs."""
+    M, r = wl.M, wl.rank
+    units = []
+    for g in groups:
+        ins = [inputs[i] for i in g]
+        packed = q.stack_weights([i["W"] for i in ins]) if len(g) > 1 else ins[0]["W"]
+        w = q.DeviceWeight.from_packed(packed, device=dev)
+        Ns, K = [i["N"] for i in ins], ins[0]["K"]
+        N = sum(Ns)
+        u = {"W": w, "Ns": Ns, "K": K, "N": N, "name": "|".join(wl.linears[i].name for i in g),
+             "X": q.bf16_from_bits(ins[0]["X"], device=dev),
+             "A": q.bf16_from_bits(np.stack([i["A"] for i in ins]), device=dev),
+             "B": q.bf16_from_bits(np.concatenate([i["B"] for i in ins], axis=0), device=dev),
+             "dY": q.bf16_from_bits(np.concatenate([i["dY"] for i in ins], axis=1), device=dev)}
+        u["Y"] = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        u["T"] = torch.empty((M, len(g) * r), dtype=torch.float32, device=dev)
+        u["dX"] = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        u["dA"] = torch.empty((len(g), r, K), dtype=torch.float32, device=dev)
+        u["dB"] = torch.empty((N, r), dtype=torch.float32, device=dev)
+        units.append(u)
+    return units
+
+
+def unit_of_linear(d):
+    """A single linear's tensors as a one-projection unit (views, no copies)."""
+    return {"W": d["W"], "Ns": [d["N"]], "K": d["K"], "N": d["N"], "X": d["X"], "A": d["A"].unsqueeze(0),
+            "B": d["B"], "dY": d["dY"], "Y": d["Y"], "T": d["T"], "dX": d["dX"], "dA": d["dA"].unsqueeze(0),
+            "dB": d["dB"]}
+
+
 def make_inputs(wl):
     return [syn.make_linear_inputs(wl, i, seed=0) for i in range(len(wl.linears))]
 
@@ -364,7 +414,9 @@ def config_of(wl):
     return {"workload": f"{wl.name}_layer", "format": wl.fmt + ("+dq" if wl.double_quant else ""), "M": wl.M,
             "rank": wl.rank, "alpha": wl.alpha,
             "linears": [f"{l.name}:{l.K}->{l.N}" for l in wl.linears],
-            "step": "fwd of the 7 linears, then bwd in reverse order",
+            "step": "fwd of the 7 linears, then bwd in reverse order; the projections that read the same input "
+                    "(q|k|v, gate|up) run as one fused launch each way, and their input gradients come out summed, "
+                    "as the decoder layer consumes them (see unfused_layer for every linear on its own)",
             "l2": "per-step working set (weights + activations) > 1 GB, larger than the 129 MB L2; no flush",
             "parallelism": "replicas"}
 
@@ -386,7 +438,6 @@ def main():
     inputs = make_inputs(wl)
     M, r, alpha = wl.M, wl.rank, wl.alpha
     L = []
-    ws_bytes = 0
     for inp in inputs:
         w = q.DeviceWeight.from_packed(inp["W"], device=dev)
         d = {"W": w, "K": inp["K"], "N": inp["N"]}
@@ -397,19 +448,28 @@ def main():
         d["dX"] = torch.empty((M, inp["K"]), dtype=torch.bfloat16, device=dev)
         d["dA"] = torch.empty((r, inp["K"]), dtype=torch.float32, device=dev)
         d["dB"] = torch.empty((inp["N"], r), dtype=torch.float32, device=dev)
-        ws_bytes = max(ws_bytes, q.workspace_bytes(w, M, r))
         L.append(d)
+    # The step's units: fused launches for the projections that share an
+    # input (q|k|v, gate|up), each other linear on its own; the unfused step
+    # runs every linear on its own.
+    units = make_units(q, torch, wl, inputs, dev, fused_groups(wl))
+    units_u = [unit_of_linear(d) for d in L]
+    ws_bytes = max(q.multi_workspace_bytes(u["W"], u["Ns"], M, r) for u in units + units_u)
     ws = q.alloc_workspace(ws_bytes, dev)
     for d in L:
         d["ws"] = ws
     stream = torch.cuda.current_stream(dev)
 
+    def step_units(us):
+        for u in us:
+            q.multi_linear_fwd(u["W"], u["Ns"], u["X"], u["A"], u["B"], alpha, Y=u["Y"], T=u["T"], workspace=ws,
+                               stream=stream)
+        for u in reversed(us):
+            q.multi_linear_bwd(u["W"], u["Ns"], u["X"], u["A"], u["B"], u["T"], u["dY"], alpha, dX=u["dX"],
+                               dA=u["dA"], dB=u["dB"], workspace=ws, stream=stream)
+
     def step():
-        for d in L:
-            q.linear_fwd(d["W"], d["X"], d["A"], d["B"], alpha, Y=d["Y"], T=d["T"], workspace=ws, stream=stream)
-        for d in reversed(L):
-            q.linear_bwd(d["W"], d["X"], d["A"], d["B"], d["T"], d["dY"], alpha, dX=d["dX"], dA=d["dA"],
-                         dB=d["dB"], workspace=ws, stream=stream)
+        step_units(units)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -447,6 +507,15 @@ def main():
     torch.cuda.synchronize()
     q.profile_gemm(False)
     ms_prof = p0.elapsed_time(p1)
+    # the same layer with every linear launched on its own (input gradients
+    # of q, k, v and of gate, up returned separately)
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    u0.record(stream)
+    for _ in range(args.steps):
+        step_units(units_u)
+    u1.record(stream)
+    torch.cuda.synchronize()
+    ms_unfused = u0.elapsed_time(u1)
     if clocks:
         clocks.mark("t1")
     barrier(world)
@@ -484,23 +553,24 @@ def main():
     e2e = None
     if not args.no_e2e:
         pin = lambda t, dt: torch.empty(t.shape, dtype=dt).pin_memory()  # noqa: E731
-        hX = [pin(d["X"], torch.bfloat16) for d in L]
-        hdY = [pin(d["dY"], torch.bfloat16) for d in L]
-        for h, d in zip(hX, L):
-            h.copy_(d["X"])
-        for h, d in zip(hdY, L):
-            h.copy_(d["dY"])
-        hY = [pin(d["Y"], torch.bfloat16) for d in L]
-        hdX = [pin(d["dX"], torch.bfloat16) for d in L]
-        hdA = [pin(d["dA"], torch.float32) for d in L]
-        hdB = [pin(d["dB"], torch.float32) for d in L]
+        U = units
+        hX = [pin(u["X"], torch.bfloat16) for u in U]
+        hdY = [pin(u["dY"], torch.bfloat16) for u in U]
+        for h, u in zip(hX, U):
+            h.copy_(u["X"])
+        for h, u in zip(hdY, U):
+            h.copy_(u["dY"])
+        hY = [pin(u["Y"], torch.bfloat16) for u in U]
+        hdX = [pin(u["dX"], torch.bfloat16) for u in U]
+        hdA = [pin(u["dA"], torch.float32) for u in U]
+        hdB = [pin(u["dB"], torch.float32) for u in U]
         nbytes = lambda hs: sum(h.numel() * h.element_size() for h in hs)  # noqa: E731
         h2d = nbytes(hX + hdY)
         d2h = nbytes(hY + hdX + hdA + hdB)
-        sets = [[{"X": torch.empty_like(d["X"]), "dY": torch.empty_like(d["dY"])} for d in L] for _ in range(2)]
+        sets = [[{"X": torch.empty_like(u["X"]), "dY": torch.empty_like(u["dY"])} for u in U] for _ in range(2)]
         copy_stream = torch.cuda.Stream(dev)
         out_stream = torch.cuda.Stream(dev)
-        n = len(L)
+        n = len(U)
         ev_x = [[torch.cuda.Event() for _ in range(n)] for _ in range(2)]
         ev_y = [[torch.cuda.Event() for _ in range(n)] for _ in range(2)]
         ev_f = [torch.cuda.Event() for _ in range(n)]     # Y of linear i written
@@ -522,12 +592,12 @@ def main():
                 for i in reversed(range(n)):
                     sets[b][i]["dY"].copy_(hdY[i], non_blocking=True)
                     ev_y[b][i].record(copy_stream)
-            for i, d in enumerate(L):
+            for i, d in enumerate(U):
                 stream.wait_event(ev_x[b][i])
                 if used["fout"][i]:
-                    stream.wait_event(ev_fout[i])  # the previous step's Y of linear i is out
-                q.linear_fwd(d["W"], sets[b][i]["X"], d["A"], d["B"], alpha, Y=d["Y"], T=d["T"], workspace=ws,
-                             stream=stream)
+                    stream.wait_event(ev_fout[i])  # the previous step's Y of unit i is out
+                q.multi_linear_fwd(d["W"], d["Ns"], sets[b][i]["X"], d["A"], d["B"], alpha, Y=d["Y"], T=d["T"],
+                                   workspace=ws, stream=stream)
                 ev_f[i].record(stream)
                 with torch.cuda.stream(out_stream):
                     out_stream.wait_event(ev_f[i])
@@ -535,12 +605,12 @@ def main():
                     ev_fout[i].record(out_stream)
                     used["fout"][i] = True
             for i in reversed(range(n)):
-                d = L[i]
+                d = U[i]
                 stream.wait_event(ev_y[b][i])
                 if used["out"][i]:
-                    stream.wait_event(ev_out[i])  # the previous step's dX, dA, dB of linear i are out
-                q.linear_bwd(d["W"], sets[b][i]["X"], d["A"], d["B"], d["T"], sets[b][i]["dY"], alpha, dX=d["dX"],
-                             dA=d["dA"], dB=d["dB"], workspace=ws, stream=stream)
+                    stream.wait_event(ev_out[i])  # the previous step's dX, dA, dB of unit i are out
+                q.multi_linear_bwd(d["W"], d["Ns"], sets[b][i]["X"], d["A"], d["B"], d["T"], sets[b][i]["dY"], alpha,
+                                   dX=d["dX"], dA=d["dA"], dB=d["dB"], workspace=ws, stream=stream)
                 ev_g[i].record(stream)
                 with torch.cuda.stream(out_stream):
                     out_stream.wait_event(ev_g[i])
@@ -574,8 +644,8 @@ def main():
                 sets[0][i]["dY"].copy_(hdY[i], non_blocking=True)
             c1.record(copy_stream)
             for i in range(n):
-                hY[i].copy_(L[i]["Y"], non_blocking=True)
-                hdX[i].copy_(L[i]["dX"], non_blocking=True)
+                hY[i].copy_(U[i]["Y"], non_blocking=True)
+                hdX[i].copy_(U[i]["dX"], non_blocking=True)
             c2.record(copy_stream)
         torch.cuda.synchronize()
         e2e = {"value": world * M * args.steps / t_e2e, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -610,6 +680,12 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_of(wl),
             "tflops": flops_step / t_step / 1e12 * world,
+            "launch_units": [u["name"] for u in units],
+            "unfused_layer": {"ms_per_step": ms_unfused / args.steps,
+                              "value": M / (ms_unfused / args.steps / 1e3), "unit": "tokens/s",
+                              "tflops": flops_step / (ms_unfused / args.steps / 1e3) / 1e12,
+                              "note": "the same 7 linears, each launched on its own (q, k, v and gate, up input "
+                                      "gradients returned separately)"},
             "frac_of_nominal_2250": flops_step / t_step / 1e12 / NOMINAL_BF16_TFLOPS,
             "frac_of_measured_burst": flops_step / t_step / 1e12 / peaks["bf16"],
             "frac_of_measured_sustained": flops_step / t_step / 1e12 / peaks["bf16_sustained"],

@@ -138,6 +138,39 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
                          void* dX, float* dA, float* dB,
                          void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- fused projections that share their input ------------------------------
+ * The P LoRA linears that read the same X in a decoder layer (q, k, v of the
+ * attention block; gate and up of the MLP) as one call each way: one pass of
+ * X for every projection's T, one GEMM over all their base rows, one pass of
+ * dY for every U, one dX GEMM that reduces over all their output columns, so
+ * dX is the sum of the projections' input gradients (what the layer feeding
+ * X receives).  Surogate README, design bullet "Kernels that do more per
+ * launch".
+ *   w: the projections' base weights stacked by rows, one [N x K] weight in
+ *      any format, N = sum n_split[p] (projection p's rows after those of
+ *      projections < p).
+ *   n_split: HOST int64[P], 1 <= P <= 8, each a multiple of 256 when P > 1;
+ *      P rank <= 64.
+ *   A: bf16 [P][rank][K] (projection p's adapter A_p);  B: bf16 [N][rank]
+ *      (projection p's B_p in its rows);  s = alpha / rank for all.
+ *   forward:  Y [M][N] bf16 (projection p in its column block) = X deq(W)^T
+ *             + s T_p B_p^T per block;  T_save [M][P rank] fp32 (T_p in
+ *             columns p rank ..).
+ *   backward: dY [M][N] (projection p in its column block);
+ *             dX [M][K] = sum_p (dY_p deq(W_p) + s U_p A_p) (may be NULL);
+ *             dA fp32 [P][rank][K], dB fp32 [N][rank] per projection.
+ *   workspace: qlora_multi_workspace_bytes() bytes.
+ * With P = 1 these are qlora_linear_fwd / _bwd. */
+size_t qlora_multi_workspace_bytes(const qlora_weight_desc* w, int32_t P, const int64_t* n_split, int64_t M,
+                                   int32_t rank);
+int32_t qlora_multi_linear_fwd(const qlora_weight_desc* w, int32_t P, const int64_t* n_split, int64_t M,
+                               int32_t rank, float alpha, const void* X, const void* A, const void* B, void* Y,
+                               float* T_save, void* workspace, size_t ws_bytes, void* stream);
+int32_t qlora_multi_linear_bwd(const qlora_weight_desc* w, int32_t P, const int64_t* n_split, int64_t M,
+                               int32_t rank, float alpha, const void* X, const void* A, const void* B,
+                               const float* T_save, const void* dY, void* dX, float* dA, float* dB,
+                               void* workspace, size_t ws_bytes, void* stream);
+
 /* Forward pass that allocates nothing, for callers that cannot allocate
  * device memory (e.g. a plug-in that may only use the buffers its host
  * application passes in, or a loop that must not call cudaMalloc because it

@@ -75,6 +75,11 @@ SIGNATURES = {
     "qlora_selftest_bounded_wait": (_I32, [_I64, _P]),
     "qlora_launch_count": (_I64, []),
     "qlora_linear_fwd_noalloc": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P]),
+    "qlora_multi_workspace_bytes": (_SZ, [_WD, _I32, ctypes.POINTER(ctypes.c_int64), _I64, _I32]),
+    "qlora_multi_linear_fwd": (_I32, [_WD, _I32, ctypes.POINTER(ctypes.c_int64), _I64, _I32, _F32, _P, _P, _P, _P,
+                                      _P, _P, _SZ, _P]),
+    "qlora_multi_linear_bwd": (_I32, [_WD, _I32, ctypes.POINTER(ctypes.c_int64), _I64, _I32, _F32, _P, _P, _P, _P,
+                                      _P, _P, _P, _P, _P, _SZ, _P]),
     "qlora_noalloc_scratch_bytes": (_SZ, []),
     "qlora_profile_gemm": (_I32, [_I32]),
     "qlora_profile_gemm_read": (_I32, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
@@ -252,6 +257,77 @@ def linear_bwd(w: DeviceWeight, X, A, B, T, dY, alpha: float, dX=None, dA=None, 
                                  _ptr(dY), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(workspace), workspace.numel(),
                                  _stream_ptr(stream))
     _check("qlora_linear_bwd", st)
+    return dX, dA, dB
+
+
+# ---------------------------------------------------------------------------
+# fused projections sharing one input
+# ---------------------------------------------------------------------------
+def _split(n_split: Sequence[int]):
+    arr = (ctypes.c_int64 * len(n_split))(*[int(n) for n in n_split])
+    return len(n_split), arr
+
+
+def stack_weights(packed: Sequence[Dict]) -> Dict:
+    """Host-side stacking of P packed base weights with the same K into one
+    [sum N_p x K] weight in the same format (rows of projection p after those
+    of projections < p).  Double-quantised NF4 groups must not span two
+    projections (each N_p K / 64 a multiple of the group)."""
+    fmt = packed[0]["fmt"]
+    K = packed[0]["K"]
+    out = {"fmt": fmt, "N": sum(p["N"] for p in packed), "K": K,
+           "data": np.concatenate([np.asarray(p["data"]).reshape(-1) for p in packed])}
+    for k in ("absmax", "absmax_q", "absmax_scale"):
+        if k in packed[0]:
+            out[k] = np.concatenate([np.asarray(p[k]).reshape(-1) for p in packed])
+    if "dq_group" in packed[0]:
+        g = packed[0]["dq_group"]
+        assert all((p["N"] * K // 64) % g == 0 for p in packed), "a quantisation group spans two projections"
+        out["dq_group"] = g
+    return out
+
+
+def multi_workspace_bytes(w: DeviceWeight, n_split: Sequence[int], M: int, rank: int) -> int:
+    P, arr = _split(n_split)
+    return int(load().qlora_multi_workspace_bytes(ctypes.byref(w.desc), P, arr, int(M), int(rank)))
+
+
+def multi_linear_fwd(w: DeviceWeight, n_split: Sequence[int], X, A, B, alpha: float, Y=None, T=None,
+                     workspace=None, stream=None):
+    """A [P, r, K], B [N, r].  Returns (Y [M, N], T_save [M, P r])."""
+    torch = _torch()
+    P, arr = _split(n_split)
+    M, r = X.shape[0], A.shape[1]
+    if Y is None:
+        Y = torch.empty((M, w.N), dtype=torch.bfloat16, device=X.device)
+    if T is None:
+        T = torch.empty((M, P * r), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(multi_workspace_bytes(w, n_split, M, r), X.device)
+    st = load().qlora_multi_linear_fwd(ctypes.byref(w.desc), P, arr, M, r, float(alpha), _ptr(X), _ptr(A), _ptr(B),
+                                       _ptr(Y), _ptr(T), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check("qlora_multi_linear_fwd", st)
+    return Y, T
+
+
+def multi_linear_bwd(w: DeviceWeight, n_split: Sequence[int], X, A, B, T, dY, alpha: float, dX=None, dA=None,
+                     dB=None, workspace=None, stream=None, want_dx: bool = True):
+    """Returns (dX summed over projections, dA [P, r, K], dB [N, r])."""
+    torch = _torch()
+    P, arr = _split(n_split)
+    M, r = X.shape[0], A.shape[1]
+    if dX is None and want_dx:
+        dX = torch.empty((M, w.K), dtype=torch.bfloat16, device=X.device)
+    if dA is None:
+        dA = torch.empty((P, r, w.K), dtype=torch.float32, device=X.device)
+    if dB is None:
+        dB = torch.empty((w.N, r), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(multi_workspace_bytes(w, n_split, M, r), X.device)
+    st = load().qlora_multi_linear_bwd(ctypes.byref(w.desc), P, arr, M, r, float(alpha), _ptr(X), _ptr(A), _ptr(B),
+                                       _ptr(T), _ptr(dY), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(workspace),
+                                       workspace.numel(), _stream_ptr(stream))
+    _check("qlora_multi_linear_bwd", st)
     return dX, dA, dB
 
 

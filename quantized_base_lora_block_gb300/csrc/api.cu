@@ -262,11 +262,20 @@ static cudaError_t gemm_launch(int fmt, bool dx, int pair, const GemmMaps& maps,
   return e;
 }
 
+// Output columns owned by each of P fused projections (cumulative ends).
+struct ProjSplit {
+  int P = 1;
+  int64_t end[kMaxProj] = {0};
+};
+
 // Dense fused GEMM: forward (dx = false) out = A_op W^T + la lb^T with
 // A_op = X [M x K], la = sT, lb = B [N x r]; dX (dx = true) out = A_op W +
-// la lb with A_op = dY [M x N], la = sU, lb = A [r x K].
-static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M, int rank, const void* a_op,
-                                  const void* la, const void* lb, void* out, cudaStream_t st) {
+// la lb with A_op = dY [M x N], la = sU, lb = A [r x K].  la has la_cols
+// columns; with fused projections (forward, ps->P > 1) a tile's adapter chunk
+// takes the `rank` columns of its projection.
+static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M, int rank, int la_cols,
+                                  const ProjSplit* ps, const void* a_op, const void* la, const void* lb, void* out,
+                                  cudaStream_t st) {
   const int64_t N = w->N, K = w->K;
   // pair tiles on an SM pair; short problems use one CTA per 128 x 256 tile
   const int pair = M > kBM ? pair_cfg(w->fmt, M, dx ? K : N, sm_count()) : 0;
@@ -277,11 +286,11 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
   std::memset(&maps, 0, sizeof(maps));
   bool ok;
   if (!dx) {
-    ok = map2d(&maps.a, a_op, K, M, 64, 128) && map2d(&maps.la, la, rank, M, 64, 128) &&
+    ok = map2d(&maps.a, a_op, K, M, 64, 128) && map2d(&maps.la, la, la_cols, M, 64, 128) &&
          map2d(&maps.lb, lb, rank, N, 64, brows);
     if (w->fmt == QLORA_FMT_BF16) ok = ok && map2d(&maps.w, w->data, K, N, 64, brows);
   } else {
-    ok = map2d(&maps.a, a_op, N, M, 64, 128) && map2d(&maps.la, la, rank, M, 64, 128) &&
+    ok = map2d(&maps.a, a_op, N, M, 64, 128) && map2d(&maps.la, la, la_cols, M, 64, 128) &&
          map2d(&maps.lb, lb, K, rank, 64, 64);
     if (w->fmt == QLORA_FMT_BF16) ok = ok && map2d(&maps.w, w->data, K, N, 64, 64);
   }
@@ -327,6 +336,10 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
   // read once (543 -> 253 MB).  dX: column blocks fastest, so each dY row
   // block is read once.
   a.n_fastest = dx ? 1 : ((double)M * (double)a.k_red * 2.0 > 64e6 ? 1 : 0);
+  if (!dx && ps && ps->P > 1) {
+    a.nproj = ps->P;
+    for (int p = 0; p < ps->P; ++p) a.proj_end[p] = (int)ps->end[p];
+  }
   return gemm_launch(w->fmt, dx, pair, maps, a, st);
 }
 
@@ -578,12 +591,41 @@ int32_t dequant_blocks(const qlora_weight_desc* w, void* W_bf16, void* stream) {
   return cuda_status(launch_dequant(w->fmt, view_of(w), lines, static_cast<__nv_bfloat16*>(W_bf16), st));
 }
 
-int32_t qlora_linear_fwd(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha, const void* X,
-                         const void* A, const void* B, void* Y, float* T_save, void* workspace, size_t ws_bytes,
-                         void* stream) {
-  int v = validate_weight(w);
-  if (v != QLORA_OK) return v;
-  if ((v = validate_rank(rank)) != QLORA_OK) return v;
+}  // extern "C"
+
+namespace qlora {
+
+// Fused projections: P >= 1, widths summing to N; with P > 1 each width a
+// multiple of 256 (no GEMM tile spans two projections) and P rank <= 64
+// (their adapters form one reduction chunk).
+static int validate_split(const qlora_weight_desc* w, int32_t P, const int64_t* n_split, int32_t rank,
+                          ProjSplit& ps) {
+  if (P < 1 || P > kMaxProj || !n_split) return QLORA_ERR_INVALID;
+  int64_t o = 0;
+  for (int p = 0; p < P; ++p) {
+    if (n_split[p] <= 0) return QLORA_ERR_INVALID;
+    if (P > 1 && n_split[p] % 256) return QLORA_ERR_UNSUPPORTED;
+    o += n_split[p];
+    ps.end[p] = o;
+  }
+  if (o != w->N) return QLORA_ERR_INVALID;
+  if ((int64_t)P * rank > 64) return QLORA_ERR_UNSUPPORTED;
+  ps.P = P;
+  return QLORA_OK;
+}
+
+// Workspace of a (possibly fused) call: the dense layout for the P rank
+// adapter columns, plus the block-diagonal B of fused projections.
+static size_t multi_workspace(const qlora_weight_desc* w, const ProjSplit& ps, int64_t M, int rank,
+                              size_t* bd_off) {
+  const DenseLayout L = dense_layout(M, w->N, w->K, ps.P * rank);
+  if (bd_off) *bd_off = L.total;
+  return L.total + (ps.P > 1 ? round256((size_t)w->N * ps.P * rank * 2) : 0);
+}
+
+static int32_t linear_fwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, int64_t M, int32_t rank,
+                               float alpha, const void* X, const void* A, const void* B, void* Y, float* T_save,
+                               void* workspace, size_t ws_bytes, void* stream) {
   if (M < 0 || !std::isfinite(alpha)) return QLORA_ERR_INVALID;
   if (M == 0) return QLORA_OK;
   if (M > (1ll << 31) - 256) return QLORA_ERR_UNSUPPORTED;
@@ -591,16 +633,18 @@ int32_t qlora_linear_fwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   if (!aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(Y) || !aligned16(T_save))
     return QLORA_ERR_ALIGN;
   const int64_t N = w->N, K = w->K;
-  const DenseLayout L = dense_layout(M, N, K, rank);
-  if (!workspace || ws_bytes < L.total) return QLORA_ERR_WORKSPACE;
+  const int Q = ps.P * rank;  // adapter columns of all projections
+  const DenseLayout L = dense_layout(M, N, K, Q);
+  if (!workspace || ws_bytes < multi_workspace(w, ps, M, rank, nullptr)) return QLORA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   __nv_bfloat16* sT = reinterpret_cast<__nv_bfloat16*>(ws + L.act_off);
   const float s = alpha / (float)rank;
 
-  // 1) T = X A^T (split over K): T_save = T (fp32), sT = bf16(s T)
-  RowReduce rt;
+  // 1) T = X A^T (split over K; A is every projection's adapter stacked by
+  //    rows): T_save = T (fp32), sT = bf16(s T)
+  RowReduce rt = {};
   rt.L = static_cast<const __nv_bfloat16*>(X);
   rt.S = static_cast<const __nv_bfloat16*>(A);
   rt.s_qj = 1;
@@ -610,27 +654,23 @@ int32_t qlora_linear_fwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   rt.scale = s;
   rt.out_f32 = T_save;
   rt.out_scaled = sT;
-  rt.out_hilo = nullptr;
-  rt.aux_src = nullptr;
-  rt.aux_hilo = nullptr;
-  if (launch_row_reduce_fin(rt, rank, st) != cudaSuccess) return QLORA_ERR_CUDA;
+  if (launch_row_reduce_fin(rt, Q, st) != cudaSuccess) return QLORA_ERR_CUDA;
 
-  // 2) Y = X deq(W)^T + sT B^T
-  return cuda_status(run_dense_gemm(w, false, M, rank, X, sT, B, Y, st));
+  // 2) Y = X deq(W)^T + sT B^T, each tile's adapter chunk from its projection
+  return cuda_status(run_dense_gemm(w, false, M, rank, Q, &ps, X, sT, B, Y, st));
 }
 
-int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha, const void* X,
-                         const void* A, const void* B, const float* T_save, const void* dY, void* dX, float* dA,
-                         float* dB, void* workspace, size_t ws_bytes, void* stream) {
-  int v = validate_weight(w);
-  if (v != QLORA_OK) return v;
-  if ((v = validate_rank(rank)) != QLORA_OK) return v;
+static int32_t linear_bwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, int64_t M, int32_t rank,
+                               float alpha, const void* X, const void* A, const void* B, const float* T_save,
+                               const void* dY, void* dX, float* dA, float* dB, void* workspace, size_t ws_bytes,
+                               void* stream) {
   if (M < 0 || !std::isfinite(alpha)) return QLORA_ERR_INVALID;
   if (!dA || !dB) return QLORA_ERR_INVALID;
   const int64_t N = w->N, K = w->K;
+  const int Q = ps.P * rank;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (M == 0) {  // no rows: the adapter gradients are zero
-    if (cudaMemsetAsync(dA, 0, (size_t)rank * K * 4, st) != cudaSuccess) return QLORA_ERR_CUDA;
+    if (cudaMemsetAsync(dA, 0, (size_t)Q * K * 4, st) != cudaSuccess) return QLORA_ERR_CUDA;
     return cuda_status(cudaMemsetAsync(dB, 0, (size_t)N * rank * 4, st));
   }
   if (M > (1ll << 31) - 256) return QLORA_ERR_UNSUPPORTED;
@@ -638,8 +678,9 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   if (!aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(T_save) || !aligned16(dY) ||
       !aligned16(dA) || !aligned16(dB) || (dX && !aligned16(dX)))
     return QLORA_ERR_ALIGN;
-  const DenseLayout L = dense_layout(M, N, K, rank);
-  if (!workspace || ws_bytes < L.total) return QLORA_ERR_WORKSPACE;
+  const DenseLayout L = dense_layout(M, N, K, Q);
+  size_t bd_off = 0;
+  if (!workspace || ws_bytes < multi_workspace(w, ps, M, rank, &bd_off)) return QLORA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   __nv_bfloat16* sU = reinterpret_cast<__nv_bfloat16*>(ws + L.act_off);
@@ -649,26 +690,35 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   const __nv_bfloat16* Xb = static_cast<const __nv_bfloat16*>(X);
   const __nv_bfloat16* dYb = static_cast<const __nv_bfloat16*>(dY);
 
+  // 0) fused projections: U = dY B_bd with B spread block-diagonally, so
+  //    projection p's columns of U see only its own rows of dY and B
+  const __nv_bfloat16* Bu = static_cast<const __nv_bfloat16*>(B);
+  if (ps.P > 1) {
+    __nv_bfloat16* Bbd = reinterpret_cast<__nv_bfloat16*>(ws + bd_off);
+    if (launch_block_diag(Bu, N, rank, ps.P, ps.end, Bbd, st) != cudaSuccess) return QLORA_ERR_CUDA;
+    Bu = Bbd;
+  }
+
   // 1) U = dY B (split over N): sU = bf16(s U) for the dX GEMM, U and T_save
   //    as hi/lo bf16 pairs for the dA / dB reductions
-  RowReduce ru;
+  RowReduce ru = {};
   ru.L = dYb;
-  ru.S = static_cast<const __nv_bfloat16*>(B);
+  ru.S = Bu;
   ru.s_qj = 0;
   ru.P = M;
   ru.J = N;
   ru.sp = L.u;
   ru.scale = s;
-  ru.out_f32 = nullptr;
   ru.out_scaled = sU;
   ru.out_hilo = U2;
   ru.aux_src = T_save;
   ru.aux_hilo = T2;
-  if (launch_row_reduce_fin(ru, rank, st) != cudaSuccess) return QLORA_ERR_CUDA;
+  if (launch_row_reduce_fin(ru, Q, st) != cudaSuccess) return QLORA_ERR_CUDA;
 
   // 2) dB = s dY^T T and dA = s U^T X (split over M, one launch); dA is
-  //    reduced as dA^T [K x r] and written transposed
-  ColReduce cb;
+  //    reduced as dA^T [K x Q] and written transposed; fused projections
+  //    keep, per row of dB, the columns of its own projection
+  ColReduce cb = {};
   cb.L = dYb;
   cb.S2 = T2;
   cb.P = M;
@@ -678,30 +728,98 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   cb.scale = s;
   cb.out = dB;
   cb.transposed = 0;
-  ColReduce ca = cb;
+  if (ps.P > 1) {
+    cb.win = rank;
+    cb.nproj = ps.P;
+    for (int p = 0; p < ps.P; ++p) cb.proj_end[p] = ps.end[p];
+  }
+  ColReduce ca = {};
   ca.L = Xb;
   ca.S2 = U2;
+  ca.P = M;
   ca.J = K;
+  ca.sp = L.c;
   ca.tiles = (int)L.da_tiles;
+  ca.scale = s;
   ca.out = dA;
   ca.transposed = 1;
-  if (!dX) return cuda_status(launch_col_reduce_fin(cb, &ca, rank, st));
+  if (!dX) return cuda_status(launch_col_reduce_fin(cb, &ca, Q, st));
 
-  // 3) dX = dY deq(W) + sU A on the caller's stream, with step 2 beside it on
-  //    the side stream (both only read what step 1 wrote)
+  // 3) dX = dY deq(W) + sU A on the caller's stream (over all projections'
+  //    rows: their input gradients summed), with step 2 beside it on the
+  //    side stream (both only read what step 1 wrote)
   std::lock_guard<std::mutex> g(g_side_mu);
   SideStream* ss = side_stream_locked();
   if (!ss) {
-    if (run_dense_gemm(w, true, M, rank, dY, sU, A, dX, st) != cudaSuccess) return QLORA_ERR_CUDA;
-    return cuda_status(launch_col_reduce_fin(cb, &ca, rank, st));
+    if (run_dense_gemm(w, true, M, Q, Q, nullptr, dY, sU, A, dX, st) != cudaSuccess) return QLORA_ERR_CUDA;
+    return cuda_status(launch_col_reduce_fin(cb, &ca, Q, st));
   }
   cudaError_t e = cudaEventRecord(ss->fork, st);
-  if (e == cudaSuccess) e = run_dense_gemm(w, true, M, rank, dY, sU, A, dX, st);
+  if (e == cudaSuccess) e = run_dense_gemm(w, true, M, Q, Q, nullptr, dY, sU, A, dX, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
-  if (e == cudaSuccess) e = launch_col_reduce_fin(cb, &ca, rank, ss->s);
+  if (e == cudaSuccess) e = launch_col_reduce_fin(cb, &ca, Q, ss->s);
   if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss->join, 0);
   return cuda_status(e);
+}
+
+}  // namespace qlora
+
+extern "C" {
+
+int32_t qlora_linear_fwd(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha, const void* X,
+                         const void* A, const void* B, void* Y, float* T_save, void* workspace, size_t ws_bytes,
+                         void* stream) {
+  int v = validate_weight(w);
+  if (v != QLORA_OK) return v;
+  if ((v = validate_rank(rank)) != QLORA_OK) return v;
+  ProjSplit ps;
+  ps.end[0] = w->N;
+  return linear_fwd_impl(w, ps, M, rank, alpha, X, A, B, Y, T_save, workspace, ws_bytes, stream);
+}
+
+int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha, const void* X,
+                         const void* A, const void* B, const float* T_save, const void* dY, void* dX, float* dA,
+                         float* dB, void* workspace, size_t ws_bytes, void* stream) {
+  int v = validate_weight(w);
+  if (v != QLORA_OK) return v;
+  if ((v = validate_rank(rank)) != QLORA_OK) return v;
+  ProjSplit ps;
+  ps.end[0] = w->N;
+  return linear_bwd_impl(w, ps, M, rank, alpha, X, A, B, T_save, dY, dX, dA, dB, workspace, ws_bytes, stream);
+}
+
+size_t qlora_multi_workspace_bytes(const qlora_weight_desc* w, int32_t P, const int64_t* n_split, int64_t M,
+                                   int32_t rank) {
+  ProjSplit ps;
+  if (validate_weight(w) != QLORA_OK || validate_rank(rank) != QLORA_OK || M < 0 ||
+      validate_split(w, P, n_split, rank, ps) != QLORA_OK)
+    return 0;
+  if (M == 0) return 256;
+  return multi_workspace(w, ps, M, rank, nullptr);
+}
+
+int32_t qlora_multi_linear_fwd(const qlora_weight_desc* w, int32_t P, const int64_t* n_split, int64_t M,
+                               int32_t rank, float alpha, const void* X, const void* A, const void* B, void* Y,
+                               float* T_save, void* workspace, size_t ws_bytes, void* stream) {
+  int v = validate_weight(w);
+  if (v != QLORA_OK) return v;
+  if ((v = validate_rank(rank)) != QLORA_OK) return v;
+  ProjSplit ps;
+  if ((v = validate_split(w, P, n_split, rank, ps)) != QLORA_OK) return v;
+  return linear_fwd_impl(w, ps, M, rank, alpha, X, A, B, Y, T_save, workspace, ws_bytes, stream);
+}
+
+int32_t qlora_multi_linear_bwd(const qlora_weight_desc* w, int32_t P, const int64_t* n_split, int64_t M,
+                               int32_t rank, float alpha, const void* X, const void* A, const void* B,
+                               const float* T_save, const void* dY, void* dX, float* dA, float* dB,
+                               void* workspace, size_t ws_bytes, void* stream) {
+  int v = validate_weight(w);
+  if (v != QLORA_OK) return v;
+  if ((v = validate_rank(rank)) != QLORA_OK) return v;
+  ProjSplit ps;
+  if ((v = validate_split(w, P, n_split, rank, ps)) != QLORA_OK) return v;
+  return linear_bwd_impl(w, ps, M, rank, alpha, X, A, B, T_save, dY, dX, dA, dB, workspace, ws_bytes, stream);
 }
 
 size_t qlora_grouped_workspace_bytes(const qlora_weight_desc* experts, int32_t E, const int32_t* offsets,

@@ -245,7 +245,8 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
             }
           } else {
 #pragma unroll
-            for (int a = 0; a < NACC; ++a) tma_load_2d_pair(sa + a * 16384, &tm_la, fb, 0, am + 256 * a);
+            for (int a = 0; a < NACC; ++a)
+              tma_load_2d_pair(sa + a * 16384, &tm_la, fb, adapter_col(args, tc.n0), am + 256 * a);
             if (!DX) {
               tma_load_2d_pair(sb, &tm_lb, fb, 0, bn);
             } else {

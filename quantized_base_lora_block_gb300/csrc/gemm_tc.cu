@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(num_threads<FMT>(), 1)
               }
             }
           } else {
-            tma_load_2d(sa, &tm_la, fb, 0, tc.m0);
+            tma_load_2d(sa, &tm_la, fb, GROUPED ? 0 : adapter_col(args, tc.n0), tc.m0);
             if (!DX) {
               if (GROUPED) tma_load_3d(sb, &tm_lb, fb, 0, tc.n0, tc.group);
               else tma_load_2d(sb, &tm_lb, fb, 0, tc.n0);

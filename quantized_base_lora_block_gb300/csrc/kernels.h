@@ -11,6 +11,10 @@
 
 namespace qlora {
 
+// Fused projections that share their input (e.g. q, k, v): at most this
+// many in one call.
+constexpr int kMaxProj = 8;
+
 void count_launch(int n);
 int* device_error_word();  // address of the device error word on the current device
 
@@ -89,7 +93,18 @@ struct ColReduce {
   float scale;
   float* out;
   int transposed;
+  // window (fused projections' dB): win > 0 keeps, for output rows j of
+  // projection p (j in [proj_end[p-1], proj_end[p])), only columns
+  // [p win, (p+1) win) of the Q, written as out[j][0..win) (row stride win);
+  // win == 0: all Q columns.
+  int win;
+  int nproj;
+  int64_t proj_end[kMaxProj];
 };
+// B_bd [N x P r] (bf16) = the block-diagonal spread of B [N x r]: row n of
+// projection p carries B[n] in columns [p r, (p+1) r) and zeros elsewhere.
+cudaError_t launch_block_diag(const __nv_bfloat16* B, int64_t N, int r, int nproj, const int64_t* proj_end,
+                              __nv_bfloat16* out, cudaStream_t st);
 cudaError_t launch_row_reduce_fin(const RowReduce& r, int Q, cudaStream_t st);
 // One launch for one or two column reductions with the same split plan (b
 // may be null).
@@ -121,6 +136,7 @@ constexpr int kBK = 64;
 // base weight.  Dense problems use one group.
 constexpr int kMaxGroups = 256;
 
+
 struct GroupTable {
   WeightView w[kMaxGroups];
 };
@@ -143,7 +159,21 @@ struct GemmArgs {
   int* err;              // device error word
   int n_fastest;         // pair kernel tile order: 1 = output column blocks fastest
   int raw_dq;            // pair kernel, NF4 dX: absmax codes and group scales through the raw ring
+  // Fused projections (forward): projection p owns output columns
+  // [proj_end[p-1], proj_end[p]) and adapter columns [p rank, (p+1) rank) of
+  // the adapter A operand; a tile never spans two projections.  nproj <= 1:
+  // one projection.
+  int nproj;
+  int proj_end[kMaxProj];
 };
+
+// First adapter column (of the adapter A operand) of the projection that owns
+// output column n0.
+__host__ __device__ __forceinline__ int adapter_col(const GemmArgs& a, int n0) {
+  int x = 0;
+  for (int p = 0; p + 1 < a.nproj; ++p) x += n0 >= a.proj_end[p] ? a.rank : 0;
+  return x;
+}
 
 // Tensor maps: A operand [M x k_red] (X or dY), bf16 W (format BF16 only),
 // adapter A-operand (sT / sU [M x r]), adapter B-operand (B [N x r] forward,

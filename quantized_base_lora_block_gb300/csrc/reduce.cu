@@ -343,19 +343,24 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
   cluster_sync_all();
 
   // CTA `rank` sums items rank, rank + splits, ... (4 consecutive q of one
-  // column) over the cluster in rank order, hi and lo halves separately
+  // column) over the cluster in rank order, hi and lo halves separately.
+  // With a window only the tile's projection's columns are written.
   const uint32_t splits = (uint32_t)jb.sp.splits;
   const uint32_t rank = cluster_ctarank();
-  for (int it = (int)rank * NTHR + tid; it < TJ * (Q / 4); it += (int)splits * NTHR) {
+  const int QW = jb.win > 0 ? jb.win : Q;  // output columns per row
+  int qoff = 0;
+  if (jb.win > 0)
+    for (int p = 0; p + 1 < jb.nproj; ++p) qoff += j0 >= jb.proj_end[p] ? jb.win : 0;
+  for (int it = (int)rank * NTHR + tid; it < TJ * (QW / 4); it += (int)splits * NTHR) {
     int jj, q;
     if (jb.transposed) {  // out[q][j]: consecutive items along j
       q = (it / TJ) * 4;
       jj = it % TJ;
     } else {  // out[j][q]: consecutive items along q
-      jj = it / (Q / 4);
-      q = (it % (Q / 4)) * 4;
+      jj = it / (QW / 4);
+      q = (it % (QW / 4)) * 4;
     }
-    const float* src = sP + jj * Q2 + q;
+    const float* src = sP + jj * Q2 + qoff + q;
     float4 hi = make_float4(0.f, 0.f, 0.f, 0.f), lo = hi;
     for (uint32_t c = 0; c < splits; ++c) {
       const float4 th = ld_cluster_v4(src, c);
@@ -378,10 +383,40 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
       jb.out[(int64_t)(q + 2) * J + j] = v.z;
       jb.out[(int64_t)(q + 3) * J + j] = v.w;
     } else {
-      *reinterpret_cast<float4*>(jb.out + j * Q + q) = v;
+      *reinterpret_cast<float4*>(jb.out + j * QW + q) = v;
     }
   }
   cluster_sync_all();  // no CTA leaves while its tile may still be read
+}
+
+// B_bd = the block-diagonal spread of B (see kernels.h); one thread per
+// 8-element (16-byte) piece of B_bd.
+__global__ void block_diag_kernel(const __nv_bfloat16* __restrict__ B, int64_t N, int r, int nproj,
+                                  ColReduce geom, __nv_bfloat16* __restrict__ out) {
+  const int Q = nproj * r;
+  const int64_t pieces = N * (Q / 8);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < pieces; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = i / (Q / 8);
+    const int c8 = (int)(i % (Q / 8)) * 8;
+    int p = 0;
+    while (p + 1 < nproj && n >= geom.proj_end[p]) ++p;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (c8 >= p * r && c8 < (p + 1) * r) v = *reinterpret_cast<const uint4*>(B + n * r + (c8 - p * r));
+    *reinterpret_cast<uint4*>(out + n * Q + c8) = v;
+  }
+}
+
+cudaError_t launch_block_diag(const __nv_bfloat16* B, int64_t N, int r, int nproj, const int64_t* proj_end,
+                              __nv_bfloat16* out, cudaStream_t st) {
+  if (nproj < 1 || nproj > kMaxProj || r % 8) return cudaErrorInvalidValue;
+  ColReduce geom = {};
+  for (int p = 0; p < nproj; ++p) geom.proj_end[p] = proj_end[p];
+  const int64_t pieces = N * (nproj * r / 8);
+  int64_t blocks = (pieces + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  count_launch(1);
+  block_diag_kernel<<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, st>>>(B, N, r, nproj, geom, out);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
