@@ -342,47 +342,61 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
         if (!ok) break;
         tc_fence_after();
         const int row0 = tc.m0 + 256 * a + 128 * (int)rank;
-#pragma unroll 1
-        for (int c = 0; c < TN / 64; ++c) {
-          uint32_t v0[32], v1[32];
-          const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * (NACC * TN) + a * TN + c * 64;
-          tmem_ld_32x32b_x32(tcol, v0);
-          tmem_ld_32x32b_x32(tcol + 32, v1);
-          tc_wait_ld();
-          if (c == TN / 64 - 1) {
+        constexpr int NCH = TN / 64;
+        const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * (NACC * TN) + a * TN;
+        uint32_t v[64];
+        tmem_ld_32x32b_x32(tcol, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld_32x32b_x32(tcol + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tc_wait_ld();
+        // fully unrolled: the registers a TMEM load fills are read only after
+        // the wait that completes it (no loop-carried copies in between)
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const bool last = c + 1 == NCH;
+          if (last) {
             // every value of this accumulator is in registers: release it
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[slot]), 0));
           }
           // the same for all 128 threads
-          if (row0 >= args.M || tc.n0 + 64 * c >= args.n_out) continue;
+          const bool store = row0 < args.M && tc.n0 + 64 * c < args.n_out;
           const uint32_t stile = sOut + (nstored % Raw::OUT_BUFS) * P_STAGE_OUT_BYTES;
-          ++nstored;
-          if (ep == 0) {  // the store that last read this staging tile is done with it
-            if (Raw::OUT_BUFS == 2)
-              bulk_wait_read1();
-            else
-              bulk_wait_read0();
-          }
-          named_bar(1, 128);
-          const uint32_t srow = stile + (uint32_t)row_in_tile * 128;
+          if (store) {
+            ++nstored;
+            if (ep == 0) {  // the store that last read this staging tile is done with it
+              if (Raw::OUT_BUFS == 2)
+                bulk_wait_read1();
+              else
+                bulk_wait_read0();
+            }
+            named_bar(1, 128);
+            const uint32_t srow = stile + (uint32_t)row_in_tile * 128;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t* v = q < 4 ? v0 + 8 * q : v1 + 8 * (q - 4);
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
-            o.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
-            o.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
-            o.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
-            sts_v4(srow + ((q ^ swz) << 4), o);
+            for (int q = 0; q < 8; ++q) {
+              const uint32_t* w = v + 8 * q;
+              uint4 o;
+              o.x = pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1]));
+              o.y = pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3]));
+              o.z = pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5]));
+              o.w = pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7]));
+              sts_v4(srow + ((q ^ swz) << 4), o);
+            }
           }
-          fence_proxy_async_smem();
-          named_bar(1, 128);
-          if (ep == 0) {
-            tma_store_2d(&tm_out, stile, tc.n0 + 64 * c, row0);
-            bulk_commit();
+          // the next chunk's TMEM load lands while this one is stored
+          if (!last) {
+            tmem_ld_32x32b_x32(tcol + 64 * (c + 1), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld_32x32b_x32(tcol + 64 * (c + 1) + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           }
+          if (store) {
+            fence_proxy_async_smem();
+            named_bar(1, 128);
+            if (ep == 0) {
+              tma_store_2d(&tm_out, stile, tc.n0 + 64 * c, row0);
+              bulk_commit();
+            }
+          }
+          if (!last) tc_wait_ld();
         }
       }
       if (!ok) break;
