@@ -19,4 +19,6 @@ from .qlora_oracle import (  # noqa: F401
     grouped_bwd,
     multi_linear_fwd,
     multi_linear_bwd,
+    stacked_linear_fwd,
+    stacked_linear_bwd,
 )

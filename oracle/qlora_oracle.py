@@ -252,3 +252,40 @@ def multi_linear_bwd(X, Wds: Sequence[np.ndarray], As: Sequence[np.ndarray], Bs:
     return {"dX": sum(g["dX"] for g in gs), "dA": np.stack([g["dA"] for g in gs]),
             "dB": np.concatenate([g["dB"] for g in gs], axis=0),
             "T": np.concatenate([g["T"] for g in gs], axis=1), "U": np.concatenate([g["U"] for g in gs], axis=1)}
+
+
+# ----------------------------------------------------------------------------
+# stacked adapters: several LoRA pairs on the same frozen base, trained (or
+# kept frozen) on top of each other without merging them into the base
+# (heatdrop.ai summary, "Key highlights"; Surogate README, "LoRA & QLoRA"
+# row).  Adapter i has its own rank r_i and scale s_i = alpha_i / r_i.
+# ----------------------------------------------------------------------------
+def stacked_linear_fwd(X, Wd, As: Sequence[np.ndarray], Bs: Sequence[np.ndarray], alphas: Sequence[float]):
+    """Y = X Wd^T + sum_i s_i (X A_i^T) B_i^T.  Returns (Y, T) with T = [T_0 | T_1 | ...]."""
+    X, Wd = _f64(X), _f64(Wd)
+    Y = X @ Wd.T
+    Ts = []
+    for A, B, alpha in zip(As, Bs, alphas):
+        A, B = _f64(A), _f64(B)
+        s = float(alpha) / A.shape[0]
+        T = X @ A.T
+        Y = Y + s * (T @ B.T)
+        Ts.append(T)
+    return Y, np.concatenate(Ts, axis=1)
+
+
+def stacked_linear_bwd(X, Wd, As: Sequence[np.ndarray], Bs: Sequence[np.ndarray], dY, alphas: Sequence[float]):
+    """dX = dY Wd + sum_i s_i (dY B_i) A_i;  dA_i = s_i U_i^T X, dB_i = s_i dY^T T_i.
+    Returns dict with dX and lists dA, dB."""
+    X, Wd, dY = _f64(X), _f64(Wd), _f64(dY)
+    dX = dY @ Wd
+    dA, dB = [], []
+    for A, B, alpha in zip(As, Bs, alphas):
+        A, B = _f64(A), _f64(B)
+        s = float(alpha) / A.shape[0]
+        T = X @ A.T
+        U = dY @ B
+        dX = dX + s * (U @ A)
+        dA.append(s * (U.T @ X))
+        dB.append(s * (dY.T @ T))
+    return {"dX": dX, "dA": dA, "dB": dB}

@@ -615,12 +615,9 @@ static int validate_split(const qlora_weight_desc* w, int32_t P, const int64_t* 
 }
 
 // Workspace of a (possibly fused) call: the dense layout for the P rank
-// adapter columns, plus the block-diagonal B of fused projections.
-static size_t multi_workspace(const qlora_weight_desc* w, const ProjSplit& ps, int64_t M, int rank,
-                              size_t* bd_off) {
-  const DenseLayout L = dense_layout(M, w->N, w->K, ps.P * rank);
-  if (bd_off) *bd_off = L.total;
-  return L.total + (ps.P > 1 ? round256((size_t)w->N * ps.P * rank * 2) : 0);
+// adapter columns.
+static size_t multi_workspace(const qlora_weight_desc* w, const ProjSplit& ps, int64_t M, int rank) {
+  return dense_layout(M, w->N, w->K, ps.P * rank).total;
 }
 
 static int32_t linear_fwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, int64_t M, int32_t rank,
@@ -635,7 +632,7 @@ static int32_t linear_fwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, 
   const int64_t N = w->N, K = w->K;
   const int Q = ps.P * rank;  // adapter columns of all projections
   const DenseLayout L = dense_layout(M, N, K, Q);
-  if (!workspace || ws_bytes < multi_workspace(w, ps, M, rank, nullptr)) return QLORA_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < multi_workspace(w, ps, M, rank)) return QLORA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -679,8 +676,7 @@ static int32_t linear_bwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, 
       !aligned16(dA) || !aligned16(dB) || (dX && !aligned16(dX)))
     return QLORA_ERR_ALIGN;
   const DenseLayout L = dense_layout(M, N, K, Q);
-  size_t bd_off = 0;
-  if (!workspace || ws_bytes < multi_workspace(w, ps, M, rank, &bd_off)) return QLORA_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < multi_workspace(w, ps, M, rank)) return QLORA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   __nv_bfloat16* sU = reinterpret_cast<__nv_bfloat16*>(ws + L.act_off);
@@ -690,20 +686,18 @@ static int32_t linear_bwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, 
   const __nv_bfloat16* Xb = static_cast<const __nv_bfloat16*>(X);
   const __nv_bfloat16* dYb = static_cast<const __nv_bfloat16*>(dY);
 
-  // 0) fused projections: U = dY B_bd with B spread block-diagonally, so
-  //    projection p's columns of U see only its own rows of dY and B
-  const __nv_bfloat16* Bu = static_cast<const __nv_bfloat16*>(B);
-  if (ps.P > 1) {
-    __nv_bfloat16* Bbd = reinterpret_cast<__nv_bfloat16*>(ws + bd_off);
-    if (launch_block_diag(Bu, N, rank, ps.P, ps.end, Bbd, st) != cudaSuccess) return QLORA_ERR_CUDA;
-    Bu = Bbd;
-  }
-
   // 1) U = dY B (split over N): sU = bf16(s U) for the dX GEMM, U and T_save
-  //    as hi/lo bf16 pairs for the dA / dB reductions
+  //    as hi/lo bf16 pairs for the dA / dB reductions.  Fused projections:
+  //    B is read spread block-diagonally, so projection p's columns of U see
+  //    only its own rows of dY and B.
   RowReduce ru = {};
   ru.L = dYb;
-  ru.S = Bu;
+  ru.S = static_cast<const __nv_bfloat16*>(B);
+  if (ps.P > 1) {
+    ru.bd_nproj = ps.P;
+    ru.bd_r = rank;
+    for (int p = 0; p < ps.P; ++p) ru.bd_end[p] = ps.end[p];
+  }
   ru.s_qj = 0;
   ru.P = M;
   ru.J = N;
@@ -796,7 +790,7 @@ size_t qlora_multi_workspace_bytes(const qlora_weight_desc* w, int32_t P, const 
       validate_split(w, P, n_split, rank, ps) != QLORA_OK)
     return 0;
   if (M == 0) return 256;
-  return multi_workspace(w, ps, M, rank, nullptr);
+  return multi_workspace(w, ps, M, rank);
 }
 
 int32_t qlora_multi_linear_fwd(const qlora_weight_desc* w, int32_t P, const int64_t* n_split, int64_t M,

@@ -79,6 +79,13 @@ struct RowReduce {
   __nv_bfloat16* out_hilo;
   const float* aux_src;
   __nv_bfloat16* aux_hilo;
+  // S given as [J x Q] (s_qj == 0) only: with bd_nproj > 1, S is read as the
+  // block-diagonal spread of B [J x bd_r] (row j of projection p, i.e. j in
+  // [bd_end[p-1], bd_end[p]), holds B[j] in columns [p bd_r, (p+1) bd_r) and
+  // zeros elsewhere; Q = bd_nproj bd_r), built while the tiles are loaded.
+  int bd_nproj;
+  int bd_r;
+  int64_t bd_end[kMaxProj];
 };
 // Column reduce out[j, q] = scale sum_p L[p, j] S[p, q], L [P x J] bf16
 // (J a multiple of 64), S given as its hi/lo bf16 split [P x 2Q] (hi in
@@ -101,10 +108,7 @@ struct ColReduce {
   int nproj;
   int64_t proj_end[kMaxProj];
 };
-// B_bd [N x P r] (bf16) = the block-diagonal spread of B [N x r]: row n of
-// projection p carries B[n] in columns [p r, (p+1) r) and zeros elsewhere.
-cudaError_t launch_block_diag(const __nv_bfloat16* B, int64_t N, int r, int nproj, const int64_t* proj_end,
-                              __nv_bfloat16* out, cudaStream_t st);
+
 cudaError_t launch_row_reduce_fin(const RowReduce& r, int Q, cudaStream_t st);
 // One launch for one or two column reductions with the same split plan (b
 // may be null).

@@ -117,10 +117,20 @@ __global__ void __launch_bounds__(NTHR) rr_fin_kernel(const RowReduce jb) {
         const int r = piece >> 3, c8 = (piece & 7) * 8;
         cp_async16(s_addr(dS + r * SP + c8), S + (int64_t)r * J + j0 + c8, true);
       }
-    } else {  // 64 rows x Q columns
+    } else if (jb.bd_nproj <= 1) {  // 64 rows x Q columns
       for (int piece = tid; piece < TJ * (Q / 8); piece += NTHR) {
         const int r = piece / (Q / 8), c8 = (piece % (Q / 8)) * 8;
         cp_async16(s_addr(dS + r * SP + c8), S + (j0 + r) * Q + c8, true);
+      }
+    } else {  // block-diagonal spread of B [J x bd_r]: zeros outside the row's block
+      for (int piece = tid; piece < TJ * (Q / 8); piece += NTHR) {
+        const int r = piece / (Q / 8), c8 = (piece % (Q / 8)) * 8;
+        const int64_t j = j0 + r;
+        int p = 0;
+        while (p + 1 < jb.bd_nproj && j >= jb.bd_end[p]) ++p;
+        const int c = c8 - p * jb.bd_r;
+        const bool in = c >= 0 && c < jb.bd_r;
+        cp_async16(s_addr(dS + r * SP + c8), S + j * jb.bd_r + (in ? c : 0), in);
       }
     }
   };
@@ -387,36 +397,6 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
     }
   }
   cluster_sync_all();  // no CTA leaves while its tile may still be read
-}
-
-// B_bd = the block-diagonal spread of B (see kernels.h); one thread per
-// 8-element (16-byte) piece of B_bd.
-__global__ void block_diag_kernel(const __nv_bfloat16* __restrict__ B, int64_t N, int r, int nproj,
-                                  ColReduce geom, __nv_bfloat16* __restrict__ out) {
-  const int Q = nproj * r;
-  const int64_t pieces = N * (Q / 8);
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < pieces; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t n = i / (Q / 8);
-    const int c8 = (int)(i % (Q / 8)) * 8;
-    int p = 0;
-    while (p + 1 < nproj && n >= geom.proj_end[p]) ++p;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (c8 >= p * r && c8 < (p + 1) * r) v = *reinterpret_cast<const uint4*>(B + n * r + (c8 - p * r));
-    *reinterpret_cast<uint4*>(out + n * Q + c8) = v;
-  }
-}
-
-cudaError_t launch_block_diag(const __nv_bfloat16* B, int64_t N, int r, int nproj, const int64_t* proj_end,
-                              __nv_bfloat16* out, cudaStream_t st) {
-  if (nproj < 1 || nproj > kMaxProj || r % 8) return cudaErrorInvalidValue;
-  ColReduce geom = {};
-  for (int p = 0; p < nproj; ++p) geom.proj_end[p] = proj_end[p];
-  const int64_t pieces = N * (nproj * r / 8);
-  int64_t blocks = (pieces + 255) / 256;
-  if (blocks > 4096) blocks = 4096;
-  count_launch(1);
-  block_diag_kernel<<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, st>>>(B, N, r, nproj, geom, out);
-  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------

@@ -446,3 +446,63 @@ def test_multi_projection_is_one_linear_with_block_diagonal_adapter():
     for p, n in enumerate(Ns):
         assert np.allclose(g["dB"][o:o + n], dBbd[o:o + n, p * r:(p + 1) * r], rtol=1e-12, atol=1e-12)
         o += n
+
+
+def test_stacked_adapters_match_merged_weight_and_single_adapter():
+    # two adapters of different ranks and scales: the forward equals the
+    # merged weight W + s0 B0 A0 + s1 B1 A1 and dX its product with dY; each
+    # adapter's gradients equal those of a single-adapter layer over the
+    # same base with the other adapter merged into it (the loss is linear in
+    # each adapter's A and B separately given the rest)
+    rng = np.random.default_rng(41)
+    M, K, N = 6, 9, 5
+    X = rng.standard_normal((M, K))
+    W = rng.standard_normal((N, K))
+    As = [rng.standard_normal((2, K)), rng.standard_normal((3, K))]
+    Bs = [rng.standard_normal((N, 2)), rng.standard_normal((N, 3))]
+    alphas = [4.0, 1.5]
+    dY = rng.standard_normal((M, N))
+    Y, T = oracle.stacked_linear_fwd(X, W, As, Bs, alphas)
+    g = oracle.stacked_linear_bwd(X, W, As, Bs, dY, alphas)
+    s = [a / A.shape[0] for a, A in zip(alphas, As)]
+    Wm = W + s[0] * Bs[0] @ As[0] + s[1] * Bs[1] @ As[1]
+    assert np.allclose(Y, X @ Wm.T, rtol=1e-12, atol=1e-12)
+    assert np.allclose(g["dX"], dY @ Wm, rtol=1e-12, atol=1e-12)
+    assert np.allclose(T, np.concatenate([X @ As[0].T, X @ As[1].T], axis=1), rtol=1e-12, atol=1e-12)
+    for i in (0, 1):
+        o = 1 - i
+        g1 = oracle.linear_bwd(X, W + s[o] * Bs[o] @ As[o], As[i], Bs[i], dY, alphas[i])
+        assert np.allclose(g["dA"][i], g1["dA"], rtol=1e-12, atol=1e-12)
+        assert np.allclose(g["dB"][i], g1["dB"], rtol=1e-12, atol=1e-12)
+
+
+def test_stacked_adapters_finite_differences():
+    rng = np.random.default_rng(43)
+    M, K, N = 3, 4, 3
+    X = rng.standard_normal((M, K))
+    W = rng.standard_normal((N, K))
+    As = [rng.standard_normal((1, K)), rng.standard_normal((2, K))]
+    Bs = [rng.standard_normal((N, 1)), rng.standard_normal((N, 2))]
+    alphas = [2.0, 3.0]
+    dY = rng.standard_normal((M, N))
+    g = oracle.stacked_linear_bwd(X, W, As, Bs, dY, alphas)
+
+    def loss(As_, Bs_):
+        Y, _ = oracle.stacked_linear_fwd(X, W, As_, Bs_, alphas)
+        return float(np.sum(dY * Y))
+
+    h = 1e-3
+    for i in (0, 1):
+        for which, grads in (("A", g["dA"][i]), ("B", g["dB"][i])):
+            base = As[i] if which == "A" else Bs[i]
+            num = np.zeros_like(base)
+            for idx in np.ndindex(base.shape):
+                vals = []
+                for sgn in (1, -1):
+                    pert = base.copy()
+                    pert[idx] += sgn * h
+                    A2 = [pert if (which == "A" and j == i) else As[j] for j in range(2)]
+                    B2 = [pert if (which == "B" and j == i) else Bs[j] for j in range(2)]
+                    vals.append(loss(A2, B2))
+                num[idx] = (vals[0] - vals[1]) / (2 * h)
+            assert np.allclose(num, grads, rtol=1e-9, atol=1e-9), (i, which)
