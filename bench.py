@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--stream-layers", type=int, default=32,
                    help="layers for the streamed leg (0 = skip); Llama workload only")
     p.add_argument("--no-moe", action="store_true", help="skip the grouped MoE leg")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the layer legs of the other configurations (Qwen3-0.6B bf16, Qwen3-8B Q4_0 / Q8_0)")
     return p.parse_args()
 
 
@@ -383,6 +385,44 @@ def unit_of_linear(d):
             "dB": d["dB"]}
 
 
+def config_leg(q, torch, name, steps, dev):
+    """The layer step of another configuration (fused launches where the
+    fused call supports them), timed on its own: ms per step, tokens/s,
+    algorithmic TFLOP/s and fractions of the peaks."""
+    wl = syn.WORKLOADS[name]
+    inputs = make_inputs(wl)
+    M, r, alpha = wl.M, wl.rank, wl.alpha
+    units = make_units(q, torch, wl, inputs, dev, fused_groups(wl))
+    ws = q.alloc_workspace(max(q.multi_workspace_bytes(u["W"], u["Ns"], M, r) for u in units), dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for u in units:
+            q.multi_linear_fwd(u["W"], u["Ns"], u["X"], u["A"], u["B"], alpha, Y=u["Y"], T=u["T"], workspace=ws,
+                               stream=stream)
+        for u in reversed(units):
+            q.multi_linear_bwd(u["W"], u["Ns"], u["X"], u["A"], u["B"], u["T"], u["dY"], alpha, dX=u["dX"],
+                               dA=u["dA"], dB=u["dB"], workspace=ws, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    assert q.device_error() == 0, f"device error in the {name} leg"
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    flops = sum(syn.linear_flops(M, l.K, l.N, r) for l in wl.linears)
+    peaks = measured_peaks()
+    tf = flops / (ms / 1e3) / 1e12
+    return {"workload": f"{name}_layer", "format": wl.fmt, "M": M, "rank": r, "alpha": alpha,
+            "launch_units": [u["name"] for u in units], "ms_per_step": ms, "tokens_per_s": M / (ms / 1e3),
+            "tflops": tf, "frac_of_nominal_2250": tf / NOMINAL_BF16_TFLOPS, "frac_of_measured_burst": tf / peaks["bf16"]}
+
+
 def make_inputs(wl):
     return [syn.make_linear_inputs(wl, i, seed=0) for i in range(len(wl.linears))]
 
@@ -663,6 +703,10 @@ def main():
     moe_res = None
     if not args.no_moe and rank == 0:
         moe_res = moe_leg(q, torch, 10, stream)
+    cfg_res = None
+    if not args.no_configs and rank == 0:
+        cfg_res = [config_leg(q, torch, name, 10, dev)
+                   for name in ("qwen3_0p6b_bf16", "qwen3_8b_q4_0", "qwen3_8b_q8_0") if name != wl.name]
 
     # --------------------------------------------------------- CPU oracle
     cpu = None
@@ -693,7 +737,7 @@ def main():
                        "needed_tflops": 0.6 * NOMINAL_BF16_TFLOPS,
                        "met": flops_step / t_step / 1e12 >= 0.6 * NOMINAL_BF16_TFLOPS},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-            "clocks": clk, "stream": stream_res, "moe": moe_res,
+            "clocks": clk, "stream": stream_res, "moe": moe_res, "configs": cfg_res,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -171,6 +171,40 @@ int32_t qlora_multi_linear_bwd(const qlora_weight_desc* w, int32_t P, const int6
                                const float* T_save, const void* dY, void* dX, float* dA, float* dB,
                                void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- stacked adapters --------------------------------------------------------
+ * Several LoRA pairs on the same frozen base, applied together without
+ * merging any of them into the base, so an adapter can be trained on top of
+ * others (heatdrop.ai summary, "Key highlights": stacked LoRA; Surogate
+ * README, "LoRA & QLoRA" row).  Adapter i: rank r_i, scale s_i = alpha_i / r_i,
+ * A_i bf16 [r_i x K], B_i bf16 [N x r_i] (device).
+ *   forward:  Y = X deq(W)^T + sum_i s_i (X A_i^T) B_i^T;
+ *             T_save [M x sum r_i] fp32, T_i = X A_i^T in columns off_i ..
+ *   backward: dX = dY deq(W) + sum_i s_i (dY B_i) A_i (dX may be NULL);
+ *             dA_i = s_i (dY B_i)^T X, dB_i = s_i dY^T T_i into dA[i] fp32
+ *             [r_i x K], dB[i] fp32 [N x r_i]; dA, dB are HOST arrays of
+ *             n_adapters device pointers, and a NULL entry leaves that
+ *             adapter without gradient (a frozen adapter under a trained one).
+ *   Limits: 1 <= n_adapters <= 4, each r_i a multiple of 8 in [8, 64],
+ *   sum r_i <= 64.  The adapters are packed into the workspace
+ *   (qlora_stacked_workspace_bytes()) and run as one adapter chunk of the
+ *   fused GEMM. */
+typedef struct {
+  int32_t rank;   /* r_i */
+  float alpha;    /* s_i = alpha / r_i */
+  const void* A;  /* bf16 [r_i x K], device */
+  const void* B;  /* bf16 [N x r_i], device */
+} qlora_adapter;
+
+size_t qlora_stacked_workspace_bytes(const qlora_weight_desc* w, int64_t M, int32_t n_adapters,
+                                     const qlora_adapter* adapters);
+int32_t qlora_stacked_linear_fwd(const qlora_weight_desc* w, int64_t M, int32_t n_adapters,
+                                 const qlora_adapter* adapters, const void* X, void* Y, float* T_save,
+                                 void* workspace, size_t ws_bytes, void* stream);
+int32_t qlora_stacked_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t n_adapters,
+                                 const qlora_adapter* adapters, const void* X, const float* T_save,
+                                 const void* dY, void* dX, float* const* dA, float* const* dB,
+                                 void* workspace, size_t ws_bytes, void* stream);
+
 /* Forward pass that allocates nothing, for callers that cannot allocate
  * device memory (e.g. a plug-in that may only use the buffers its host
  * application passes in, or a loop that must not call cudaMalloc because it

@@ -35,6 +35,10 @@ class QloraError(RuntimeError):
         self.status = status
 
 
+class AdapterDesc(ctypes.Structure):
+    _fields_ = [("rank", ctypes.c_int32), ("alpha", ctypes.c_float), ("A", ctypes.c_void_p), ("B", ctypes.c_void_p)]
+
+
 class WeightDesc(ctypes.Structure):
     _fields_ = [
         ("fmt", ctypes.c_int32),
@@ -53,6 +57,8 @@ _lib: Optional[ctypes.CDLL] = None
 # name -> (restype, argtypes)
 _P, _I32, _I64, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
 _WD = ctypes.POINTER(WeightDesc)
+_AD = ctypes.POINTER(AdapterDesc)
+_PP = ctypes.POINTER(ctypes.c_void_p)
 SIGNATURES = {
     "qlora_status_string": (ctypes.c_char_p, [_I32]),
     "qlora_version": (_I32, []),
@@ -75,6 +81,9 @@ SIGNATURES = {
     "qlora_selftest_bounded_wait": (_I32, [_I64, _P]),
     "qlora_launch_count": (_I64, []),
     "qlora_linear_fwd_noalloc": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P]),
+    "qlora_stacked_workspace_bytes": (_SZ, [_WD, _I64, _I32, _AD]),
+    "qlora_stacked_linear_fwd": (_I32, [_WD, _I64, _I32, _AD, _P, _P, _P, _P, _SZ, _P]),
+    "qlora_stacked_linear_bwd": (_I32, [_WD, _I64, _I32, _AD, _P, _P, _P, _P, _PP, _PP, _P, _SZ, _P]),
     "qlora_multi_workspace_bytes": (_SZ, [_WD, _I32, ctypes.POINTER(ctypes.c_int64), _I64, _I32]),
     "qlora_multi_linear_fwd": (_I32, [_WD, _I32, ctypes.POINTER(ctypes.c_int64), _I64, _I32, _F32, _P, _P, _P, _P,
                                       _P, _P, _SZ, _P]),
@@ -258,6 +267,63 @@ def linear_bwd(w: DeviceWeight, X, A, B, T, dY, alpha: float, dX=None, dA=None, 
                                  _stream_ptr(stream))
     _check("qlora_linear_bwd", st)
     return dX, dA, dB
+
+
+# ---------------------------------------------------------------------------
+# stacked adapters on one base
+# ---------------------------------------------------------------------------
+def _adapters(As, Bs, alphas):
+    n = len(As)
+    arr = (AdapterDesc * n)(*[AdapterDesc(int(A.shape[0]), float(al), _ptr(A), _ptr(B))
+                              for A, B, al in zip(As, Bs, alphas)])
+    return n, arr
+
+
+def stacked_workspace_bytes(w: DeviceWeight, M: int, As, Bs, alphas) -> int:
+    n, arr = _adapters(As, Bs, alphas)
+    return int(load().qlora_stacked_workspace_bytes(ctypes.byref(w.desc), int(M), n, arr))
+
+
+def stacked_linear_fwd(w: DeviceWeight, X, As, Bs, alphas, Y=None, T=None, workspace=None, stream=None):
+    """Adapters i = 0.. with A_i [r_i, K], B_i [N, r_i], alpha_i.  Returns (Y, T_save [M, sum r_i])."""
+    torch = _torch()
+    n, arr = _adapters(As, Bs, alphas)
+    M = X.shape[0]
+    Q = sum(int(A.shape[0]) for A in As)
+    if Y is None:
+        Y = torch.empty((M, w.N), dtype=torch.bfloat16, device=X.device)
+    if T is None:
+        T = torch.empty((M, Q), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(stacked_workspace_bytes(w, M, As, Bs, alphas), X.device)
+    st = load().qlora_stacked_linear_fwd(ctypes.byref(w.desc), M, n, arr, _ptr(X), _ptr(Y), _ptr(T), _ptr(workspace),
+                                         workspace.numel(), _stream_ptr(stream))
+    _check("qlora_stacked_linear_fwd", st)
+    return Y, T
+
+
+def stacked_linear_bwd(w: DeviceWeight, X, As, Bs, alphas, T, dY, trainable=None, dX=None, workspace=None,
+                       stream=None, want_dx: bool = True):
+    """Returns (dX, [dA_i or None], [dB_i or None]); trainable[i] False leaves
+    adapter i without gradient."""
+    torch = _torch()
+    n, arr = _adapters(As, Bs, alphas)
+    M = X.shape[0]
+    trainable = [True] * n if trainable is None else list(trainable)
+    dAs = [torch.empty((int(A.shape[0]), w.K), dtype=torch.float32, device=X.device) if t else None
+           for A, t in zip(As, trainable)]
+    dBs = [torch.empty((w.N, int(A.shape[0])), dtype=torch.float32, device=X.device) if t else None
+           for A, t in zip(As, trainable)]
+    pa = (ctypes.c_void_p * n)(*[_ptr(t) for t in dAs])
+    pb = (ctypes.c_void_p * n)(*[_ptr(t) for t in dBs])
+    if dX is None and want_dx:
+        dX = torch.empty((M, w.K), dtype=torch.bfloat16, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(stacked_workspace_bytes(w, M, As, Bs, alphas), X.device)
+    st = load().qlora_stacked_linear_bwd(ctypes.byref(w.desc), M, n, arr, _ptr(X), _ptr(T), _ptr(dY), _ptr(dX), pa, pb,
+                                         _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check("qlora_stacked_linear_bwd", st)
+    return dX, dAs, dBs
 
 
 # ---------------------------------------------------------------------------

@@ -816,6 +816,199 @@ int32_t qlora_multi_linear_bwd(const qlora_weight_desc* w, int32_t P, const int6
   return linear_bwd_impl(w, ps, M, rank, alpha, X, A, B, T_save, dY, dX, dA, dB, workspace, ws_bytes, stream);
 }
 
+// ---------------------------------------------------------------- stacked ---
+}  // extern "C"
+
+namespace qlora {
+
+struct StackedPlan {
+  AdapterPack ap;
+  int Q = 0;
+  int seg_end[kMaxAdapters];
+  float seg_scale[kMaxAdapters];
+  DenseLayout L;
+  size_t a_off = 0, b_off = 0, total = 0;
+};
+
+static int plan_stacked(const qlora_weight_desc* w, int64_t M, int32_t n, const qlora_adapter* ad, StackedPlan& P) {
+  if (n < 1 || n > kMaxAdapters || !ad) return QLORA_ERR_INVALID;
+  P.ap.n = n;
+  P.Q = 0;
+  for (int i = 0; i < n; ++i) {
+    if (validate_rank(ad[i].rank) != QLORA_OK || !std::isfinite(ad[i].alpha)) return QLORA_ERR_INVALID;
+    P.ap.r[i] = ad[i].rank;
+    P.ap.A[i] = static_cast<const __nv_bfloat16*>(ad[i].A);
+    P.ap.B[i] = static_cast<const __nv_bfloat16*>(ad[i].B);
+    P.Q += ad[i].rank;
+    P.seg_end[i] = P.Q;
+    P.seg_scale[i] = ad[i].alpha / (float)ad[i].rank;
+  }
+  if (P.Q > 64) return QLORA_ERR_UNSUPPORTED;
+  P.L = dense_layout(M, w->N, w->K, P.Q);
+  P.a_off = P.L.total;
+  P.b_off = P.a_off + round256((size_t)P.Q * w->K * 2);
+  P.total = P.b_off + round256((size_t)w->N * P.Q * 2);
+  return QLORA_OK;
+}
+
+static int check_adapter_ptrs(const StackedPlan& P) {
+  for (int i = 0; i < P.ap.n; ++i) {
+    if (!P.ap.A[i] || !P.ap.B[i]) return QLORA_ERR_INVALID;
+    if (!aligned16(P.ap.A[i]) || !aligned16(P.ap.B[i])) return QLORA_ERR_ALIGN;
+  }
+  return QLORA_OK;
+}
+
+}  // namespace qlora
+
+extern "C" {
+
+size_t qlora_stacked_workspace_bytes(const qlora_weight_desc* w, int64_t M, int32_t n_adapters,
+                                     const qlora_adapter* adapters) {
+  StackedPlan P;
+  if (validate_weight(w) != QLORA_OK || M < 0 || plan_stacked(w, M, n_adapters, adapters, P) != QLORA_OK) return 0;
+  if (M == 0) return 256;
+  return P.total;
+}
+
+int32_t qlora_stacked_linear_fwd(const qlora_weight_desc* w, int64_t M, int32_t n_adapters,
+                                 const qlora_adapter* adapters, const void* X, void* Y, float* T_save,
+                                 void* workspace, size_t ws_bytes, void* stream) {
+  int v = validate_weight(w);
+  if (v != QLORA_OK) return v;
+  StackedPlan P;
+  if ((v = plan_stacked(w, M, n_adapters, adapters, P)) != QLORA_OK) return v;
+  if (M < 0) return QLORA_ERR_INVALID;
+  if (M == 0) return QLORA_OK;
+  if (M > (1ll << 31) - 256) return QLORA_ERR_UNSUPPORTED;
+  if (!X || !Y || !T_save) return QLORA_ERR_INVALID;
+  if ((v = check_adapter_ptrs(P)) != QLORA_OK) return v;
+  if (!aligned16(X) || !aligned16(Y) || !aligned16(T_save)) return QLORA_ERR_ALIGN;
+  if (!workspace || ws_bytes < P.total) return QLORA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* sT = reinterpret_cast<__nv_bfloat16*>(ws + P.L.act_off);
+  __nv_bfloat16* Acat = reinterpret_cast<__nv_bfloat16*>(ws + P.a_off);
+  __nv_bfloat16* Bcat = reinterpret_cast<__nv_bfloat16*>(ws + P.b_off);
+  // 0) the adapters stacked: A_cat [Q x K], B_cat [N x Q]
+  if (launch_pack_adapters(P.ap, w->N, w->K, Acat, Bcat, st) != cudaSuccess) return QLORA_ERR_CUDA;
+  // 1) T = X A_cat^T: T_save = T, sT = s_i T_i per adapter
+  RowReduce rt = {};
+  rt.L = static_cast<const __nv_bfloat16*>(X);
+  rt.S = Acat;
+  rt.s_qj = 1;
+  rt.P = M;
+  rt.J = w->K;
+  rt.sp = P.L.t;
+  rt.scale = 1.f;
+  rt.out_f32 = T_save;
+  rt.out_scaled = sT;
+  rt.nseg = P.ap.n;
+  for (int i = 0; i < P.ap.n; ++i) {
+    rt.seg_end[i] = P.seg_end[i];
+    rt.seg_scale[i] = P.seg_scale[i];
+  }
+  if (launch_row_reduce_fin(rt, P.Q, st) != cudaSuccess) return QLORA_ERR_CUDA;
+  // 2) Y = X deq(W)^T + sT B_cat^T: every adapter in the one adapter chunk
+  return cuda_status(run_dense_gemm(w, false, M, P.Q, P.Q, nullptr, X, sT, Bcat, Y, st));
+}
+
+int32_t qlora_stacked_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t n_adapters,
+                                 const qlora_adapter* adapters, const void* X, const float* T_save, const void* dY,
+                                 void* dX, float* const* dA, float* const* dB, void* workspace, size_t ws_bytes,
+                                 void* stream) {
+  int v = validate_weight(w);
+  if (v != QLORA_OK) return v;
+  StackedPlan P;
+  if ((v = plan_stacked(w, M, n_adapters, adapters, P)) != QLORA_OK) return v;
+  if (M < 0 || !dA || !dB) return QLORA_ERR_INVALID;
+  const int64_t N = w->N, K = w->K;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int i = 0; i < P.ap.n; ++i)
+    if ((dA[i] && !aligned16(dA[i])) || (dB[i] && !aligned16(dB[i]))) return QLORA_ERR_ALIGN;
+  if (M == 0) {  // no rows: the adapter gradients are zero
+    for (int i = 0; i < P.ap.n; ++i) {
+      if (dA[i] && cudaMemsetAsync(dA[i], 0, (size_t)P.ap.r[i] * K * 4, st) != cudaSuccess) return QLORA_ERR_CUDA;
+      if (dB[i] && cudaMemsetAsync(dB[i], 0, (size_t)N * P.ap.r[i] * 4, st) != cudaSuccess) return QLORA_ERR_CUDA;
+    }
+    return QLORA_OK;
+  }
+  if (M > (1ll << 31) - 256) return QLORA_ERR_UNSUPPORTED;
+  if (!X || !T_save || !dY) return QLORA_ERR_INVALID;
+  if ((v = check_adapter_ptrs(P)) != QLORA_OK) return v;
+  if (!aligned16(X) || !aligned16(T_save) || !aligned16(dY) || (dX && !aligned16(dX))) return QLORA_ERR_ALIGN;
+  if (!workspace || ws_bytes < P.total) return QLORA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* sU = reinterpret_cast<__nv_bfloat16*>(ws + P.L.act_off);
+  __nv_bfloat16* U2 = reinterpret_cast<__nv_bfloat16*>(ws + P.L.u_off);
+  __nv_bfloat16* T2 = reinterpret_cast<__nv_bfloat16*>(ws + P.L.t_off);
+  __nv_bfloat16* Acat = reinterpret_cast<__nv_bfloat16*>(ws + P.a_off);
+  __nv_bfloat16* Bcat = reinterpret_cast<__nv_bfloat16*>(ws + P.b_off);
+  const __nv_bfloat16* Xb = static_cast<const __nv_bfloat16*>(X);
+  const __nv_bfloat16* dYb = static_cast<const __nv_bfloat16*>(dY);
+  if (launch_pack_adapters(P.ap, N, K, Acat, Bcat, st) != cudaSuccess) return QLORA_ERR_CUDA;
+  // 1) U = dY B_cat: sU = s_i U_i per adapter; U and T_save as hi/lo pairs
+  RowReduce ru = {};
+  ru.L = dYb;
+  ru.S = Bcat;
+  ru.s_qj = 0;
+  ru.P = M;
+  ru.J = N;
+  ru.sp = P.L.u;
+  ru.scale = 1.f;
+  ru.out_scaled = sU;
+  ru.out_hilo = U2;
+  ru.aux_src = T_save;
+  ru.aux_hilo = T2;
+  ru.nseg = P.ap.n;
+  for (int i = 0; i < P.ap.n; ++i) {
+    ru.seg_end[i] = P.seg_end[i];
+    ru.seg_scale[i] = P.seg_scale[i];
+  }
+  if (launch_row_reduce_fin(ru, P.Q, st) != cudaSuccess) return QLORA_ERR_CUDA;
+  // 2) dB_i = s_i dY^T T_i and dA_i = s_i U_i^T X, each adapter's columns to
+  //    its own arrays (none for a frozen adapter)
+  ColReduce cb = {};
+  cb.L = dYb;
+  cb.S2 = T2;
+  cb.P = M;
+  cb.J = N;
+  cb.sp = P.L.c;
+  cb.tiles = (int)P.L.db_tiles;
+  cb.scale = 1.f;
+  cb.transposed = 0;
+  cb.nseg = P.ap.n;
+  ColReduce ca = cb;
+  ca.L = Xb;
+  ca.S2 = U2;
+  ca.J = K;
+  ca.tiles = (int)P.L.da_tiles;
+  ca.transposed = 1;
+  for (int i = 0; i < P.ap.n; ++i) {
+    cb.seg_end[i] = ca.seg_end[i] = P.seg_end[i];
+    cb.seg_scale[i] = ca.seg_scale[i] = P.seg_scale[i];
+    cb.seg_out[i] = dB[i];
+    ca.seg_out[i] = dA[i];
+  }
+  if (!dX) return cuda_status(launch_col_reduce_fin(cb, &ca, P.Q, st));
+  // 3) dX = dY deq(W) + sU A_cat, with step 2 beside it on the side stream
+  std::lock_guard<std::mutex> g(g_side_mu);
+  SideStream* ss = side_stream_locked();
+  if (!ss) {
+    if (run_dense_gemm(w, true, M, P.Q, P.Q, nullptr, dY, sU, Acat, dX, st) != cudaSuccess) return QLORA_ERR_CUDA;
+    return cuda_status(launch_col_reduce_fin(cb, &ca, P.Q, st));
+  }
+  cudaError_t e = cudaEventRecord(ss->fork, st);
+  if (e == cudaSuccess) e = run_dense_gemm(w, true, M, P.Q, P.Q, nullptr, dY, sU, Acat, dX, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
+  if (e == cudaSuccess) e = launch_col_reduce_fin(cb, &ca, P.Q, ss->s);
+  if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss->join, 0);
+  return cuda_status(e);
+}
+
 size_t qlora_grouped_workspace_bytes(const qlora_weight_desc* experts, int32_t E, const int32_t* offsets,
                                      int32_t rank) {
   if (validate_grouped(experts, E, offsets, rank) != QLORA_OK) return 0;

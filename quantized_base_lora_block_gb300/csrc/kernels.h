@@ -14,6 +14,8 @@ namespace qlora {
 // Fused projections that share their input (e.g. q, k, v): at most this
 // many in one call.
 constexpr int kMaxProj = 8;
+// Stacked adapters on one base: at most this many in one call.
+constexpr int kMaxAdapters = 4;
 
 void count_launch(int n);
 int* device_error_word();  // address of the device error word on the current device
@@ -86,6 +88,11 @@ struct RowReduce {
   int bd_nproj;
   int bd_r;
   int64_t bd_end[kMaxProj];
+  // stacked adapters: nseg > 0 scales out_scaled column q by seg_scale[i] for
+  // q in [seg_end[i-1], seg_end[i]) instead of `scale`
+  int nseg;
+  int seg_end[kMaxAdapters];
+  float seg_scale[kMaxAdapters];
 };
 // Column reduce out[j, q] = scale sum_p L[p, j] S[p, q], L [P x J] bf16
 // (J a multiple of 64), S given as its hi/lo bf16 split [P x 2Q] (hi in
@@ -107,7 +114,24 @@ struct ColReduce {
   int win;
   int nproj;
   int64_t proj_end[kMaxProj];
+  // stacked adapters: nseg > 0 splits the Q columns into segments [seg_end[i-1],
+  // seg_end[i]), each with its own scale and its own output array seg_out[i]
+  // ([J x w_i], or [w_i x J] transposed, w_i its width; null: not written)
+  int nseg;
+  int seg_end[kMaxAdapters];
+  float seg_scale[kMaxAdapters];
+  float* seg_out[kMaxAdapters];
 };
+// Stacked adapters: A_cat [Q x K] = the adapters' A stacked by rows, B_cat
+// [N x Q] = their B side by side (adapter i in columns [off_i, off_i + r_i)).
+struct AdapterPack {
+  int n;
+  int r[kMaxAdapters];
+  const __nv_bfloat16* A[kMaxAdapters];
+  const __nv_bfloat16* B[kMaxAdapters];
+};
+cudaError_t launch_pack_adapters(const AdapterPack& ap, int64_t N, int64_t K, __nv_bfloat16* A_cat,
+                                 __nv_bfloat16* B_cat, cudaStream_t st);
 
 cudaError_t launch_row_reduce_fin(const RowReduce& r, int Q, cudaStream_t st);
 // One launch for one or two column reductions with the same split plan (b

@@ -229,9 +229,16 @@ __global__ void __launch_bounds__(NTHR) rr_fin_kernel(const RowReduce jb) {
     const int64_t i = p0 * Q + (int64_t)it * 4;
     if (jb.out_f32) *reinterpret_cast<float4*>(jb.out_f32 + i) = v;
     if (jb.out_scaled) {
+      float sc = jb.scale;
+      if (jb.nseg > 0) {  // 4 consecutive columns lie in one segment (widths are multiples of 8)
+        const int q = (it * 4) % Q;
+        int k = 0;
+        while (k + 1 < jb.nseg && q >= jb.seg_end[k]) ++k;
+        sc = jb.seg_scale[k];
+      }
       __nv_bfloat162* o2 = reinterpret_cast<__nv_bfloat162*>(jb.out_scaled + i);
-      o2[0] = __floats2bfloat162_rn(v.x * jb.scale, v.y * jb.scale);
-      o2[1] = __floats2bfloat162_rn(v.z * jb.scale, v.w * jb.scale);
+      o2[0] = __floats2bfloat162_rn(v.x * sc, v.y * sc);
+      o2[1] = __floats2bfloat162_rn(v.z * sc, v.w * sc);
     }
     const int64_t h = (p0 + (it * 4) / Q) * (2 * Q) + (it * 4) % Q;  // [P x 2Q] position of the hi value
     if (jb.out_hilo) store_hilo(jb.out_hilo + h, v, Q);
@@ -384,10 +391,31 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
       lo.z += tl.z;
       lo.w += tl.w;
     }
-    const float4 v = make_float4((hi.x + lo.x) * jb.scale, (hi.y + lo.y) * jb.scale, (hi.z + lo.z) * jb.scale,
-                                 (hi.w + lo.w) * jb.scale);
+    float sc = jb.scale;
+    float* out = jb.out;
+    int qo = q, ow = QW;  // column within the output array, its width
+    if (jb.nseg > 0) {  // q .. q+3 lie in one segment (widths are multiples of 8)
+      int k = 0;
+      while (k + 1 < jb.nseg && q >= jb.seg_end[k]) ++k;
+      const int start = k > 0 ? jb.seg_end[k - 1] : 0;
+      sc = jb.seg_scale[k];
+      out = jb.seg_out[k];
+      qo = q - start;
+      ow = jb.seg_end[k] - start;
+      if (!out) continue;  // a frozen adapter: no gradient
+    }
+    const float4 v = make_float4((hi.x + lo.x) * sc, (hi.y + lo.y) * sc, (hi.z + lo.z) * sc, (hi.w + lo.w) * sc);
     const int64_t j = j0 + jj;
-    if (jb.transposed) {
+    if (jb.nseg > 0) {
+      if (jb.transposed) {
+        out[(int64_t)(qo + 0) * J + j] = v.x;
+        out[(int64_t)(qo + 1) * J + j] = v.y;
+        out[(int64_t)(qo + 2) * J + j] = v.z;
+        out[(int64_t)(qo + 3) * J + j] = v.w;
+      } else {
+        *reinterpret_cast<float4*>(out + j * ow + qo) = v;
+      }
+    } else if (jb.transposed) {
       jb.out[(int64_t)(q + 0) * J + j] = v.x;
       jb.out[(int64_t)(q + 1) * J + j] = v.y;
       jb.out[(int64_t)(q + 2) * J + j] = v.z;
@@ -397,6 +425,46 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
     }
   }
   cluster_sync_all();  // no CTA leaves while its tile may still be read
+}
+
+// Stacked adapters: A_cat rows and B_cat columns gathered from each
+// adapter's arrays, 8 bf16 (16 bytes) per thread and step.
+__global__ void pack_adapters_kernel(const AdapterPack ap, int64_t N, int64_t K, __nv_bfloat16* __restrict__ A_cat,
+                                     __nv_bfloat16* __restrict__ B_cat) {
+  int Q = 0;
+  for (int i = 0; i < ap.n; ++i) Q += ap.r[i];
+  const int64_t a_pieces = (int64_t)Q * (K / 8), b_pieces = N * (Q / 8);
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < a_pieces + b_pieces;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    if (t < a_pieces) {  // A_cat row q = row q - off_i of adapter i
+      const int q = (int)(t / (K / 8));
+      const int64_t c8 = (t % (K / 8)) * 8;
+      int i = 0, off = 0;
+      while (q >= off + ap.r[i]) off += ap.r[i++];
+      *reinterpret_cast<uint4*>(A_cat + (int64_t)q * K + c8) =
+          *reinterpret_cast<const uint4*>(ap.A[i] + (int64_t)(q - off) * K + c8);
+    } else {  // B_cat[n][off_i + c] = B_i[n][c]
+      const int64_t u = t - a_pieces;
+      const int64_t n = u / (Q / 8);
+      const int c8 = (int)(u % (Q / 8)) * 8;
+      int i = 0, off = 0;
+      while (c8 >= off + ap.r[i]) off += ap.r[i++];
+      *reinterpret_cast<uint4*>(B_cat + n * Q + c8) =
+          *reinterpret_cast<const uint4*>(ap.B[i] + n * ap.r[i] + (c8 - off));
+    }
+  }
+}
+
+cudaError_t launch_pack_adapters(const AdapterPack& ap, int64_t N, int64_t K, __nv_bfloat16* A_cat,
+                                 __nv_bfloat16* B_cat, cudaStream_t st) {
+  int Q = 0;
+  for (int i = 0; i < ap.n; ++i) Q += ap.r[i];
+  const int64_t pieces = (int64_t)Q * (K / 8) + N * (Q / 8);
+  int64_t blocks = (pieces + 255) / 256;
+  if (blocks > 2048) blocks = 2048;
+  count_launch(1);
+  pack_adapters_kernel<<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, st>>>(ap, N, K, A_cat, B_cat);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
