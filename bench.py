@@ -300,21 +300,24 @@ def moe_leg(q, torch, steps, stream):
     off, _, counts = syn.moe_routing(seed=0)
     lins = syn.moe_linears(mw)
     data = [syn.make_moe_linear_inputs(mw, i, off, seed=0) for i in range(len(lins))]
+    rows = int(off[-1])
+    off_dev = q.device_offsets(off)  # the router's offsets stay on the device
     dev = []
     for d in data:
         ws = [q.DeviceWeight.from_packed(w) for w in d["W"]]
         X, dY = q.bf16_from_bits(d["X"]), q.bf16_from_bits(d["dY"])
         A, B = q.bf16_from_bits(d["A"]), q.bf16_from_bits(d["B"])
-        nb = q.grouped_workspace_bytes(ws, off, mw.rank)
+        nb = q.grouped_workspace_bytes(ws, rows, mw.rank)
         dev.append({"W": ws, "X": X, "dY": dY, "A": A, "B": B, "alpha": d["alpha"], "ws": q.alloc_workspace(nb)})
 
     def step():
         Ts = []
         for d in dev:
-            _, T = q.grouped_fwd(d["W"], off, d["X"], d["A"], d["B"], d["alpha"], workspace=d["ws"], stream=stream)
+            _, T = q.grouped_fwd(d["W"], off_dev, d["X"], d["A"], d["B"], d["alpha"], workspace=d["ws"],
+                                 stream=stream)
             Ts.append(T)
         for d, T in zip(reversed(dev), reversed(Ts)):
-            q.grouped_bwd(d["W"], off, d["X"], d["A"], d["B"], T, d["dY"], d["alpha"], workspace=d["ws"],
+            q.grouped_bwd(d["W"], off_dev, d["X"], d["A"], d["B"], T, d["dY"], d["alpha"], workspace=d["ws"],
                           stream=stream)
 
     for _ in range(3):
@@ -327,7 +330,6 @@ def moe_leg(q, torch, steps, stream):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    rows = int(off[-1])
     flops = sum(syn.linear_flops(rows, l.K, l.N, mw.rank) for l in lins)
     return {"workload": "moe_q8_0: 128 experts, top-8 of 4096 tokens (32768 rows, Zipf-skewed, "
                         f"{int((counts == 0).sum())} experts empty), gate/up 2048->768, down 768->2048, rank 16",

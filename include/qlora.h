@@ -226,24 +226,43 @@ size_t qlora_noalloc_scratch_bytes(void);
 
 /* ---- grouped (mixture-of-experts) variant -------------------------------
  * The same layer for E experts (bytechap GGUF blog: fast LoRA backward for
- * linear and MoE layers).  Rows of X / dY / Y / dX / T_save are sorted by
- * expert: expert e owns rows offsets[e] .. offsets[e+1]-1 (offsets: HOST
- * int32[E+1], offsets[0] == 0, non-decreasing, offsets[E] == M_total; empty
- * experts allowed).  experts: HOST array of E weight descriptors, all with the
- * same fmt, N and K.  A: bf16 [E][rank][K], B: bf16 [E][N][rank], dA: fp32
- * [E][rank][K], dB: fp32 [E][N][rank]; experts with no rows get dA = dB = 0.
- * E <= 256.  Workspace: qlora_grouped_workspace_bytes(). */
+ * linear and MoE layers), each expert applied to its own rows.  Rows of X /
+ * dY / Y / dX / T_save are sorted by expert: expert e owns rows offsets[e] ..
+ * offsets[e+1]-1.
+ *
+ * offsets: DEVICE int32[E+1] (as a router leaves them; never read on the
+ *   host, so the call neither copies nor synchronises).  They must satisfy
+ *   offsets[0] == 0, offsets[e] <= offsets[e+1], offsets[E] == M_total;
+ *   empty experts are allowed.  This is checked on the device: offsets that
+ *   break it make the call write nothing (Y, dX, dA, dB undefined) and record
+ *   QLORA_ERR_INVALID in the device error word (qlora_last_device_error).
+ * M_total: HOST, the number of rows (0 <= M_total <= 2^30); it sizes the
+ *   workspace and the launch grids.
+ * experts: HOST array of E <= 256 weight descriptors, all with the same fmt,
+ *   N and K.  bf16 bases must lie back to back in one array [E][N][K]
+ *   (experts[e].data == experts[0].data + e N K), else
+ *   QLORA_ERR_UNSUPPORTED; quantised bases may lie anywhere.
+ * A: bf16 [E][rank][K], B: bf16 [E][N][rank], T_save: fp32 [M_total][rank],
+ * dA: fp32 [E][rank][K], dB: fp32 [E][N][rank]; an expert with no rows gets
+ * dA = dB = 0.  dX may be NULL.  Device pointers, 16-byte aligned.
+ * Workspace: qlora_grouped_workspace_bytes(experts, E, M_total, rank) (0 for
+ * invalid arguments); it holds the device-built tile lists, so the same
+ * workspace must not be in use by another call at the same time.  The
+ * backward call runs its dA / dB reduction on a second stream of the library
+ * beside its dX GEMM, joined back into `stream` before it returns. */
 size_t qlora_grouped_workspace_bytes(const qlora_weight_desc* experts, int32_t E,
-                                     const int32_t* offsets, int32_t rank);
+                                     int64_t M_total, int32_t rank);
 
 int32_t grouped_moe_qlora_fwd(const qlora_weight_desc* experts, int32_t E,
-                              const int32_t* offsets, int32_t rank, float alpha,
+                              const int32_t* offsets, int64_t M_total,
+                              int32_t rank, float alpha,
                               const void* X, const void* A, const void* B,
                               void* Y, float* T_save,
                               void* workspace, size_t ws_bytes, void* stream);
 
 int32_t grouped_moe_qlora_bwd(const qlora_weight_desc* experts, int32_t E,
-                              const int32_t* offsets, int32_t rank, float alpha,
+                              const int32_t* offsets, int64_t M_total,
+                              int32_t rank, float alpha,
                               const void* X, const void* A, const void* B,
                               const float* T_save, const void* dY,
                               void* dX, float* dA, float* dB,

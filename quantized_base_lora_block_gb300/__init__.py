@@ -29,6 +29,10 @@ STATUS = {
 }
 
 
+QLORA_OK, QLORA_ERR_INVALID, QLORA_ERR_UNSUPPORTED, QLORA_ERR_ALIGN = 0, -1, -2, -3
+QLORA_ERR_CUDA, QLORA_ERR_TIMEOUT, QLORA_ERR_WORKSPACE, QLORA_ERR_STATE = -4, -5, -6, -7
+
+
 class QloraError(RuntimeError):
     def __init__(self, fn: str, status: int):
         super().__init__(f"{fn} failed: {STATUS.get(status, status)} ({status})")
@@ -66,11 +70,10 @@ SIGNATURES = {
     "dequant_blocks": (_I32, [_WD, _P, _P]),
     "qlora_linear_fwd": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "qlora_linear_bwd": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
-    "qlora_grouped_workspace_bytes": (_SZ, [_WD, _I32, ctypes.POINTER(ctypes.c_int32), _I32]),
-    "grouped_moe_qlora_fwd": (_I32, [_WD, _I32, ctypes.POINTER(ctypes.c_int32), _I32, _F32, _P, _P, _P, _P, _P,
-                                     _P, _SZ, _P]),
-    "grouped_moe_qlora_bwd": (_I32, [_WD, _I32, ctypes.POINTER(ctypes.c_int32), _I32, _F32, _P, _P, _P, _P, _P,
-                                     _P, _P, _P, _P, _SZ, _P]),
+    "qlora_grouped_workspace_bytes": (_SZ, [_WD, _I32, _I64, _I32]),
+    "grouped_moe_qlora_fwd": (_I32, [_WD, _I32, _P, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "grouped_moe_qlora_bwd": (_I32, [_WD, _I32, _P, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                     _P]),
     "qlora_stream_create": (_I32, [_I32, _SZ, ctypes.POINTER(ctypes.c_void_p)]),
     "qlora_stream_prefetch": (_I32, [_P, _I32, _P, _SZ]),
     "qlora_stream_acquire": (_I32, [_P, _I32, _P, ctypes.POINTER(ctypes.c_void_p)]),
@@ -400,34 +403,54 @@ def multi_linear_bwd(w: DeviceWeight, n_split: Sequence[int], X, A, B, T, dY, al
 # ---------------------------------------------------------------------------
 # grouped (mixture-of-experts)
 # ---------------------------------------------------------------------------
-def _grouped_args(weights: Sequence[DeviceWeight], offsets):
+def _grouped_descs(weights: Sequence[DeviceWeight]):
     E = len(weights)
-    descs = (WeightDesc * E)(*[w.desc for w in weights])
-    off = np.ascontiguousarray(offsets, dtype=np.int32)
-    assert off.size == E + 1
-    off_c = (ctypes.c_int32 * (E + 1))(*off.tolist())
-    return E, descs, off_c, int(off[-1])
+    return E, (WeightDesc * E)(*[w.desc for w in weights])
 
 
-def grouped_workspace_bytes(weights: Sequence[DeviceWeight], offsets, rank: int) -> int:
-    E, descs, off_c, _ = _grouped_args(weights, offsets)
-    return int(load().qlora_grouped_workspace_bytes(descs, E, off_c, int(rank)))
+def device_offsets(offsets, device="cuda"):
+    """Expert row offsets [E+1] as a device int32 tensor (the grouped calls
+    read them on the device only)."""
+    torch = _torch()
+    if isinstance(offsets, torch.Tensor) and offsets.is_cuda:
+        if offsets.dtype != torch.int32 or not offsets.is_contiguous():
+            raise ValueError("device offsets must be a contiguous int32 tensor")
+        return offsets
+    return torch.from_numpy(np.ascontiguousarray(offsets, dtype=np.int32)).to(device)
+
+
+def _offsets_for_call(offsets, X, E, stream):
+    off = device_offsets(offsets, X.device)
+    if off.numel() != E + 1:
+        raise ValueError(f"offsets must have E + 1 = {E + 1} entries, got {off.numel()}")
+    if stream is not None and off is not offsets:
+        off.record_stream(stream)  # a copy made here stays alive until the call's work ran
+    return off
+
+
+def grouped_workspace_bytes(weights: Sequence[DeviceWeight], M_total: int, rank: int) -> int:
+    E, descs = _grouped_descs(weights)
+    return int(load().qlora_grouped_workspace_bytes(descs, E, int(M_total), int(rank)))
 
 
 def grouped_fwd(weights: Sequence[DeviceWeight], offsets, X, A, B, alpha: float, Y=None, T=None, workspace=None,
                 stream=None):
-    """Rows of X sorted by expert; A [E, r, K], B [E, N, r].  Returns (Y, T_save)."""
+    """Rows of X [M_total, K] sorted by expert; offsets [E+1] (a device int32
+    tensor, or host values copied to the device); A [E, r, K], B [E, N, r].
+    Returns (Y, T_save)."""
     torch = _torch()
-    E, descs, off_c, M = _grouped_args(weights, offsets)
+    E, descs = _grouped_descs(weights)
+    M = int(X.shape[0])
+    off = _offsets_for_call(offsets, X, E, stream)
     r, N = A.shape[1], weights[0].N
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
     if T is None:
         T = torch.empty((M, r), dtype=torch.float32, device=X.device)
     if workspace is None:
-        workspace = alloc_workspace(grouped_workspace_bytes(weights, offsets, r), X.device)
-    st = load().grouped_moe_qlora_fwd(descs, E, off_c, r, float(alpha), _ptr(X), _ptr(A), _ptr(B), _ptr(Y), _ptr(T),
-                                      _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+        workspace = alloc_workspace(grouped_workspace_bytes(weights, M, r), X.device)
+    st = load().grouped_moe_qlora_fwd(descs, E, _ptr(off), M, r, float(alpha), _ptr(X), _ptr(A), _ptr(B), _ptr(Y),
+                                      _ptr(T), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
     _check("grouped_moe_qlora_fwd", st)
     return Y, T
 
@@ -436,7 +459,9 @@ def grouped_bwd(weights: Sequence[DeviceWeight], offsets, X, A, B, T, dY, alpha:
                 workspace=None, stream=None, want_dx: bool = True):
     """Returns (dX, dA [E, r, K], dB [E, N, r])."""
     torch = _torch()
-    E, descs, off_c, M = _grouped_args(weights, offsets)
+    E, descs = _grouped_descs(weights)
+    M = int(X.shape[0])
+    off = _offsets_for_call(offsets, X, E, stream)
     r, N, K = A.shape[1], weights[0].N, weights[0].K
     if dX is None and want_dx:
         dX = torch.empty((M, K), dtype=torch.bfloat16, device=X.device)
@@ -445,9 +470,9 @@ def grouped_bwd(weights: Sequence[DeviceWeight], offsets, X, A, B, T, dY, alpha:
     if dB is None:
         dB = torch.empty((E, N, r), dtype=torch.float32, device=X.device)
     if workspace is None:
-        workspace = alloc_workspace(grouped_workspace_bytes(weights, offsets, r), X.device)
-    st = load().grouped_moe_qlora_bwd(descs, E, off_c, r, float(alpha), _ptr(X), _ptr(A), _ptr(B), _ptr(T), _ptr(dY),
-                                      _ptr(dX), _ptr(dA), _ptr(dB), _ptr(workspace), workspace.numel(),
+        workspace = alloc_workspace(grouped_workspace_bytes(weights, M, r), X.device)
+    st = load().grouped_moe_qlora_bwd(descs, E, _ptr(off), M, r, float(alpha), _ptr(X), _ptr(A), _ptr(B), _ptr(T),
+                                      _ptr(dY), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(workspace), workspace.numel(),
                                       _stream_ptr(stream))
     _check("grouped_moe_qlora_bwd", st)
     return dX, dA, dB

@@ -19,7 +19,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libqlora.so")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["api.cu", "dequant.cu", "gemm_tc.cu", "gemm_pair.cu", "skinny.cu", "reduce.cu", "stream.cu", "noalloc.cu", "diag.cu"]
+SOURCES = ["api.cu", "dequant.cu", "gemm_tc.cu", "gemm_pair.cu", "reduce.cu", "grouped.cu", "stream.cu", "noalloc.cu",
+           "diag.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

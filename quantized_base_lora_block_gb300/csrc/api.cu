@@ -237,29 +237,32 @@ static cudaEvent_t prof_event() {
   return e;
 }
 
-// Launch the fused GEMM, bracketed by events when instrumentation is on.
-// pair: 0 = one CTA per tile, else the pair kernel's tile configuration.
-static cudaError_t gemm_dispatch(int fmt, bool dx, int pair, const GemmMaps& maps, const GemmArgs& a,
-                                cudaStream_t st) {
-  return pair ? launch_qgemm_pair(fmt, dx, pair, maps, a, st) : launch_qgemm(fmt, dx, false, maps, a, sm_count(), st);
-}
-
-static cudaError_t gemm_launch(int fmt, bool dx, int pair, const GemmMaps& maps, const GemmArgs& a,
-                               cudaStream_t st) {
+// Run `launch` (one fused GEMM launch on st), bracketed by events when
+// instrumentation is on.
+template <class F>
+static cudaError_t timed_gemm(const GemmArgs& a, cudaStream_t st, F&& launch) {
   std::unique_lock<std::mutex> g(g_prof_mu);
   if (!g_prof_on) {
     g.unlock();
-    return gemm_dispatch(fmt, dx, pair, maps, a, st);
+    return launch();
   }
   GemmRec r;
   r.a = prof_event();
   r.b = prof_event();
   r.flops = 2.0 * (double)a.M * (double)a.n_out * (double)(a.k_red + a.rank);
   cudaEventRecord(r.a, st);
-  cudaError_t e = gemm_dispatch(fmt, dx, pair, maps, a, st);
+  cudaError_t e = launch();
   cudaEventRecord(r.b, st);
   g_prof_recs.push_back(r);
   return e;
+}
+
+// pair: 0 = one CTA per tile, else the pair kernel's tile configuration.
+static cudaError_t gemm_launch(int fmt, bool dx, int pair, const GemmMaps& maps, const GemmArgs& a,
+                               cudaStream_t st) {
+  return timed_gemm(a, st, [&] {
+    return pair ? launch_qgemm_pair(fmt, dx, pair, maps, a, st) : launch_qgemm(fmt, dx, maps, a, sm_count(), st);
+  });
 }
 
 // Output columns owned by each of P fused projections (cumulative ends).
@@ -345,151 +348,146 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
 
 
 // ------------------------------------------------------------- grouped ------
-// Schedules for the grouped (mixture-of-experts) call, built on the host from
-// the host-side offsets and copied into the workspace with one copy.
-struct GroupedPlan {
+// Workspace of a grouped call.  The tile lists are sized for their upper
+// bounds (expert e has ceil(c_e / rows) <= c_e / rows + 1 row tiles), so the
+// layout depends on E and M_total only and the lists are filled on the device
+// from the device offsets.
+constexpr int kGroupTileRows = 256;  // rows of a grouped GEMM tile
+
+struct GroupedLayout {
   int E = 0, r = 0;
   int64_t M = 0, N = 0, K = 0;
-  std::vector<WeightView> table;
-  std::vector<int4> gf, gd, rr, cr;  // GEMM fwd / dX tiles, row tiles, row chunks
-  std::vector<int> cf;               // chunk_first[E+1]
-  SplitPlan t, u;
-  size_t off_table = 0, off_gf = 0, off_gd = 0, off_rr = 0, off_cr = 0, off_cf = 0, sched_bytes = 0;
-  size_t off_act = 0, off_u = 0, off_part = 0, total = 0;
+  int nblk_f = 0, nblk_d = 0;   // GEMM column blocks, forward / dX
+  int max_gemm_rows = 0;        // bound on the GEMM row tiles of all experts
+  int max_rows64 = 0;           // bound on the 64-row reduction tiles
+  size_t off_counts = 0, off_gf = 0, off_gd = 0, off_rr = 0, off_rg = 0;
+  size_t off_act = 0, off_u2 = 0, off_t2 = 0, total = 0;
 };
 
-static int validate_grouped(const qlora_weight_desc* ex, int E, const int32_t* off, int r) {
-  if (!ex || !off || E <= 0 || E > kMaxGroups) return QLORA_ERR_INVALID;
+static int validate_grouped(const qlora_weight_desc* ex, int E, int64_t M_total, int r) {
+  if (!ex || E <= 0 || E > kMaxGroups || M_total < 0) return QLORA_ERR_INVALID;
   int v = validate_rank(r);
   if (v != QLORA_OK) return v;
   for (int e = 0; e < E; ++e) {
     if ((v = validate_weight(&ex[e])) != QLORA_OK) return v;
     if (ex[e].fmt != ex[0].fmt || ex[e].N != ex[0].N || ex[e].K != ex[0].K) return QLORA_ERR_INVALID;
   }
-  if (off[0] != 0) return QLORA_ERR_INVALID;
-  for (int e = 0; e < E; ++e)
-    if (off[e + 1] < off[e]) return QLORA_ERR_INVALID;
-  if (off[E] > (1 << 30)) return QLORA_ERR_UNSUPPORTED;
+  if (M_total > (1 << 30)) return QLORA_ERR_UNSUPPORTED;
   return QLORA_OK;
 }
 
-static void build_grouped_plan(const qlora_weight_desc* ex, int E, const int32_t* off, int r, GroupedPlan& P) {
-  P.E = E;
-  P.r = r;
-  P.M = off[E];
-  P.N = ex[0].N;
-  P.K = ex[0].K;
-  const int nb_f = (int)((P.N + kBN - 1) / kBN), nb_d = (int)((P.K + kBN - 1) / kBN);
-  constexpr int kChunkRows = 256;
-  P.table.resize(E);
-  P.cf.resize(E + 1);
-  for (int e = 0; e < E; ++e) {
-    P.table[e] = view_of(&ex[e]);
-    const int lo = off[e], c = off[e + 1] - off[e];
-    // GEMM tiles of one expert are consecutive (its weights stay in L2), row
-    // blocks fastest
-    for (int nb = 0; nb < nb_f; ++nb)
-      for (int i = 0; i < c; i += kBM) P.gf.push_back(make_int4(e, lo + i, std::min(kBM, c - i), nb));
-    for (int nb = 0; nb < nb_d; ++nb)
-      for (int i = 0; i < c; i += kBM) P.gd.push_back(make_int4(e, lo + i, std::min(kBM, c - i), nb));
-    for (int i = 0; i < c; i += 64) P.rr.push_back(make_int4(e, lo + i, std::min(64, c - i), 0));
-    P.cf[e] = (int)P.cr.size();
-    for (int i = 0; i < c; i += kChunkRows) P.cr.push_back(make_int4(e, lo + i, lo + std::min(c, i + kChunkRows), 0));
-  }
-  P.cf[E] = (int)P.cr.size();
-  P.t = plan_split_fin((int64_t)std::max<size_t>(P.rr.size(), 1), P.K);
-  P.u = plan_split_fin((int64_t)std::max<size_t>(P.rr.size(), 1), P.N);
+static GroupedLayout grouped_layout(const qlora_weight_desc* ex, int E, int64_t M, int r) {
+  GroupedLayout L;
+  L.E = E;
+  L.r = r;
+  L.M = M;
+  L.N = ex[0].N;
+  L.K = ex[0].K;
+  L.nblk_f = (int)((L.N + 255) / 256);
+  L.nblk_d = (int)((L.K + 255) / 256);
+  L.max_gemm_rows = (int)((M + kGroupTileRows - 1) / kGroupTileRows) + E;
+  L.max_rows64 = (int)((M + 63) / 64) + E;
   size_t o = 0;
-  P.off_table = o;
-  o = round256(o + sizeof(WeightView) * E);
-  P.off_gf = o;
-  o = round256(o + sizeof(int4) * P.gf.size());
-  P.off_gd = o;
-  o = round256(o + sizeof(int4) * P.gd.size());
-  P.off_rr = o;
-  o = round256(o + sizeof(int4) * P.rr.size());
-  P.off_cr = o;
-  o = round256(o + sizeof(int4) * P.cr.size());
-  P.off_cf = o;
-  o = round256(o + sizeof(int) * P.cf.size());
-  P.sched_bytes = o;
-  P.off_act = o;
-  o = round256(o + (size_t)P.M * r * 2);
-  P.off_u = o;
-  o = round256(o + (size_t)P.M * r * 4);
-  size_t part = (size_t)P.t.splits * P.M * r;
-  part = std::max(part, (size_t)P.u.splits * P.M * r);
-  part = std::max(part, P.cr.size() * (size_t)P.N * r * 2);
-  part = std::max(part, P.cr.size() * (size_t)P.K * r * 2);
-  P.off_part = o;
-  o = round256(o + std::max<size_t>(part, 1) * 4);
-  P.total = o;
+  L.off_counts = o;
+  o = round256(o + 4 * sizeof(int));
+  L.off_gf = o;
+  o = round256(o + sizeof(int4) * (size_t)L.max_gemm_rows * L.nblk_f);
+  L.off_gd = o;
+  o = round256(o + sizeof(int4) * (size_t)L.max_gemm_rows * L.nblk_d);
+  L.off_rr = o;
+  o = round256(o + sizeof(int4) * (size_t)L.max_rows64);
+  L.off_rg = o;
+  o = round256(o + sizeof(int2) * (size_t)E);
+  L.off_act = o;  // sT (forward) or sU (backward), bf16 [M x r]
+  o = round256(o + (size_t)M * r * 2);
+  L.off_u2 = o;  // U as hi/lo bf16 [M x 2r] (backward)
+  o = round256(o + (size_t)M * r * 4);
+  L.off_t2 = o;  // T as hi/lo bf16 [M x 2r] (backward)
+  o = round256(o + (size_t)M * r * 4);
+  L.total = o;
+  return L;
 }
 
-static cudaError_t upload_grouped_plan(const GroupedPlan& P, uint8_t* ws, cudaStream_t st) {
-  std::vector<uint8_t> h(P.sched_bytes, 0);
-  std::memcpy(h.data() + P.off_table, P.table.data(), sizeof(WeightView) * P.table.size());
-  if (!P.gf.empty()) std::memcpy(h.data() + P.off_gf, P.gf.data(), sizeof(int4) * P.gf.size());
-  if (!P.gd.empty()) std::memcpy(h.data() + P.off_gd, P.gd.data(), sizeof(int4) * P.gd.size());
-  if (!P.rr.empty()) std::memcpy(h.data() + P.off_rr, P.rr.data(), sizeof(int4) * P.rr.size());
-  if (!P.cr.empty()) std::memcpy(h.data() + P.off_cr, P.cr.data(), sizeof(int4) * P.cr.size());
-  std::memcpy(h.data() + P.off_cf, P.cf.data(), sizeof(int) * P.cf.size());
-  // pageable source: the copy is staged before this call returns
-  return cudaMemcpyAsync(ws, h.data(), h.size(), cudaMemcpyHostToDevice, st);
+static GroupedSched grouped_sched(const GroupedLayout& L, uint8_t* ws) {
+  GroupedSched g;
+  g.counts = reinterpret_cast<int*>(ws + L.off_counts);
+  g.gemm_f = reinterpret_cast<int4*>(ws + L.off_gf);
+  g.gemm_d = reinterpret_cast<int4*>(ws + L.off_gd);
+  g.rows64 = reinterpret_cast<int4*>(ws + L.off_rr);
+  g.ranges = reinterpret_cast<int2*>(ws + L.off_rg);
+  return g;
 }
 
 // bf16 [E][mid][inner] as a 3-D tensor (innermost first), box {64, rows, 1}
-static bool map3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t E, uint32_t box_inner,
-                  uint32_t box_rows) {
+static bool map3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid, uint64_t E, uint32_t box_rows) {
   const uint64_t dims[3] = {inner, mid, E};
   const uint64_t strides[2] = {inner * 2, inner * mid * 2};
-  const uint32_t box[3] = {box_inner, box_rows, 1};
+  const uint32_t box[3] = {64, box_rows, 1};
   return make_map(m, base, 3, dims, strides, box);
 }
 
-// bf16 expert weights must be one array [E][N][K] for the 3-D map
-static bool map3d_weights(CUtensorMap* m, const qlora_weight_desc* ex, int E, int64_t K, int64_t N,
-                          uint32_t box_rows) {
+// bf16 expert bases must be one array [E][N][K] for the 3-D map
+static bool experts_stacked(const qlora_weight_desc* ex, int E) {
   const uint8_t* b0 = static_cast<const uint8_t*>(ex[0].data);
+  const size_t stride = (size_t)ex[0].N * ex[0].K * 2;
   for (int e = 1; e < E; ++e)
-    if (static_cast<const uint8_t*>(ex[e].data) != b0 + (size_t)e * N * K * 2) return false;
-  return map3d(m, b0, K, N, E, 64, box_rows);
+    if (static_cast<const uint8_t*>(ex[e].data) != b0 + (size_t)e * stride) return false;
+  return true;
 }
 
-static GemmArgs grouped_args(const GroupedPlan& P, bool dx, int rank, void* out, uint8_t* ws) {
+// Grouped fused GEMM over the schedule's tile list: forward Y = X deq(W_e)^T
+// + sT B_e^T, dX = dY deq(W_e) + sU A_e, 256 x 256 tiles on SM pairs.
+static cudaError_t run_grouped_gemm(const qlora_weight_desc* ex, const GroupedLayout& L, bool dx,
+                                    const GroupedSched& g, const void* a_op, const void* la, const void* lb,
+                                    void* out, cudaStream_t st) {
+  const int64_t M = L.M, N = L.N, K = L.K;
+  const int E = L.E, r = L.r;
+  GemmMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  bool ok;
+  if (!dx) {
+    ok = map2d(&maps.a, a_op, K, M, 64, 128) && map2d(&maps.la, la, r, M, 64, 128) &&
+         map3d(&maps.lb, lb, r, N, E, 128);
+    if (ex[0].fmt == QLORA_FMT_BF16) ok = ok && map3d(&maps.w, ex[0].data, K, N, E, 128);
+  } else {
+    ok = map2d(&maps.a, a_op, N, M, 64, 128) && map2d(&maps.la, la, r, M, 64, 128) &&
+         map3d(&maps.lb, lb, K, r, E, 64);
+    if (ex[0].fmt == QLORA_FMT_BF16) ok = ok && map3d(&maps.w, ex[0].data, K, N, E, 64);
+  }
+  ok = ok && map2d(&maps.out, out, dx ? K : N, M, 64, 128);
+  if (!ok) return cudaErrorInvalidValue;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.M = (int)P.M;
-  a.n_out = (int)(dx ? P.K : P.N);
-  a.k_red = (int)(dx ? P.N : P.K);
-  a.rank = rank;
-  a.num_n_blk = (a.n_out + kBN - 1) / kBN;
-  a.num_tiles = (int)(dx ? P.gd.size() : P.gf.size());
-  a.w_lines_per_row = P.K / 64;
-  a.w_rows = P.N;
+  a.M = (int)M;
+  a.n_out = (int)(dx ? K : N);
+  a.k_red = (int)(dx ? N : K);
+  a.rank = r;
+  a.num_n_blk = dx ? L.nblk_d : L.nblk_f;
+  a.num_tiles = L.max_gemm_rows * a.num_n_blk;  // bound; the count is on the device
+  a.w_lines_per_row = K / 64;
+  a.w_rows = N;
   a.out = static_cast<__nv_bfloat16*>(out);
-  a.tile_sched = reinterpret_cast<const int4*>(ws + (dx ? P.off_gd : P.off_gf));
-  a.num_groups = P.E;
-  a.groups = reinterpret_cast<const GroupTable*>(ws + P.off_table);
+  a.tile_sched = dx ? g.gemm_d : g.gemm_f;
+  a.tile_count = g.counts + (dx ? 1 : 0);
+  a.wv = view_of(&ex[0]);
   a.err = device_error_word();
-  return a;
+  static thread_local GroupTable tab;  // 12 KB: kept off the stack
+  for (int e = 0; e < E; ++e) tab.w[e] = view_of(&ex[e]);
+  return timed_gemm(a, st, [&] { return launch_qgemm_pair_grouped(ex[0].fmt, dx, maps, a, tab, st); });
 }
 
-static cudaError_t gemm_launch_grouped(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& a, cudaStream_t st) {
-  std::unique_lock<std::mutex> g(g_prof_mu);
-  if (!g_prof_on) {
-    g.unlock();
-    return launch_qgemm(fmt, dx, true, maps, a, sm_count(), st);
-  }
-  GemmRec r;
-  r.a = prof_event();
-  r.b = prof_event();
-  r.flops = 2.0 * (double)a.M * (double)a.n_out * (double)(a.k_red + a.rank);
-  cudaEventRecord(r.a, st);
-  cudaError_t e = launch_qgemm(fmt, dx, true, maps, a, sm_count(), st);
-  cudaEventRecord(r.b, st);
-  g_prof_recs.push_back(r);
-  return e;
+// Splits of the grouped column reductions: one CTA per (expert, output tile)
+// already gives E (tiles) CTAs; split each expert's rows only when that is
+// far below the target.
+static SplitPlan grouped_col_split(const GroupedLayout& L, int64_t tiles) {
+  SplitPlan sp;
+  int64_t s = kSplitTargetCtas / std::max<int64_t>(tiles * L.E, 1);
+  const int64_t mean_rows64 = std::max<int64_t>((L.M + 63) / 64 / L.E, 1);
+  s = std::min<int64_t>(s, std::max<int64_t>(mean_rows64 / 2, 1));
+  s = std::min<int64_t>(std::max<int64_t>(s, 1), kMaxClusterSplits);
+  sp.splits = (int)s;
+  sp.chunk = 0;  // grouped: each expert's rows are split evenly
+  return sp;
 }
 
 }  // namespace qlora
@@ -1009,65 +1007,64 @@ int32_t qlora_stacked_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t 
   return cuda_status(e);
 }
 
-size_t qlora_grouped_workspace_bytes(const qlora_weight_desc* experts, int32_t E, const int32_t* offsets,
-                                     int32_t rank) {
-  if (validate_grouped(experts, E, offsets, rank) != QLORA_OK) return 0;
-  GroupedPlan P;
-  build_grouped_plan(experts, E, offsets, rank, P);
-  return P.total;
+size_t qlora_grouped_workspace_bytes(const qlora_weight_desc* experts, int32_t E, int64_t M_total, int32_t rank) {
+  if (validate_grouped(experts, E, M_total, rank) != QLORA_OK) return 0;
+  return grouped_layout(experts, E, M_total, rank).total;
 }
 
-int32_t grouped_moe_qlora_fwd(const qlora_weight_desc* experts, int32_t E, const int32_t* offsets, int32_t rank,
-                              float alpha, const void* X, const void* A, const void* B, void* Y, float* T_save,
-                              void* workspace, size_t ws_bytes, void* stream) {
-  int v = validate_grouped(experts, E, offsets, rank);
+int32_t grouped_moe_qlora_fwd(const qlora_weight_desc* experts, int32_t E, const int32_t* offsets, int64_t M_total,
+                              int32_t rank, float alpha, const void* X, const void* A, const void* B, void* Y,
+                              float* T_save, void* workspace, size_t ws_bytes, void* stream) {
+  int v = validate_grouped(experts, E, M_total, rank);
   if (v != QLORA_OK) return v;
-  if (!std::isfinite(alpha)) return QLORA_ERR_INVALID;
-  const int64_t M = offsets[E];
-  if (M == 0) return QLORA_OK;
+  if (!std::isfinite(alpha) || !offsets) return QLORA_ERR_INVALID;
+  if (M_total == 0) return QLORA_OK;
   if (!X || !A || !B || !Y || !T_save) return QLORA_ERR_INVALID;
   if (!aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(Y) || !aligned16(T_save)) return QLORA_ERR_ALIGN;
-  GroupedPlan P;
-  build_grouped_plan(experts, E, offsets, rank, P);
-  if (!workspace || ws_bytes < P.total) return QLORA_ERR_WORKSPACE;
+  if (experts[0].fmt == QLORA_FMT_BF16 && !experts_stacked(experts, E)) return QLORA_ERR_UNSUPPORTED;
+  const GroupedLayout L = grouped_layout(experts, E, M_total, rank);
+  if (!workspace || ws_bytes < L.total) return QLORA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (upload_grouped_plan(P, ws, st) != cudaSuccess) return QLORA_ERR_CUDA;
-  const int64_t N = P.N, K = P.K;
+  const GroupedSched g = grouped_sched(L, ws);
   const float s = alpha / (float)rank;
-  __nv_bfloat16* sT = reinterpret_cast<__nv_bfloat16*>(ws + P.off_act);
-  float* part = reinterpret_cast<float*>(ws + P.off_part);
+  __nv_bfloat16* sT = reinterpret_cast<__nv_bfloat16*>(ws + L.off_act);
 
-  // 1) T = X A_e^T per expert's rows, T_save = T, sT = bf16(s T)
-  cudaError_t e = launch_row_reduce(static_cast<const __nv_bfloat16*>(X), M, K, static_cast<const __nv_bfloat16*>(A),
-                                    rank, true, part, P.t, st, reinterpret_cast<const int4*>(ws + P.off_rr),
-                                    (int)P.rr.size(), (int64_t)rank * K);
-  if (e == cudaSuccess) e = launch_fin_rows(part, P.t.splits, M, rank, s, T_save, sT, st);
+  // 0) tile lists from the device offsets
+  cudaError_t e = launch_grouped_schedule(offsets, E, M_total, kGroupTileRows, L.nblk_f, L.nblk_d, g,
+                                          device_error_word(), st);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  // 1) T = X A_e^T over each expert's rows: T_save = T, sT = bf16(s T)
+  RowReduce rt = {};
+  rt.L = static_cast<const __nv_bfloat16*>(X);
+  rt.S = static_cast<const __nv_bfloat16*>(A);
+  rt.s_qj = 1;
+  rt.P = M_total;
+  rt.J = L.K;
+  rt.sp = plan_split_fin(L.max_rows64, L.K);
+  rt.scale = s;
+  rt.out_f32 = T_save;
+  rt.out_scaled = sT;
+  rt.tiles = g.rows64;
+  rt.tile_count = g.counts + 2;
+  rt.s_stride = (int64_t)rank * L.K;
+  rt.max_tiles = L.max_rows64;
+  if (launch_row_reduce_fin(rt, rank, st) != cudaSuccess) return QLORA_ERR_CUDA;
   // 2) Y = X deq(W_e)^T + sT B_e^T
-  GemmMaps maps;
-  std::memset(&maps, 0, sizeof(maps));
-  bool ok = map2d(&maps.a, X, K, M, 64, 128) && map2d(&maps.la, sT, rank, M, 64, 128) &&
-            map3d(&maps.lb, B, rank, N, E, 64, 256);
-  if (experts[0].fmt == QLORA_FMT_BF16) ok = ok && map3d_weights(&maps.w, experts, E, K, N, 256);
-  if (!ok) return QLORA_ERR_CUDA;
-  GemmArgs a = grouped_args(P, false, rank, Y, ws);
-  return cuda_status(gemm_launch_grouped(experts[0].fmt, false, maps, a, st));
+  return cuda_status(run_grouped_gemm(experts, L, false, g, X, sT, B, Y, st));
 }
 
-int32_t grouped_moe_qlora_bwd(const qlora_weight_desc* experts, int32_t E, const int32_t* offsets, int32_t rank,
-                              float alpha, const void* X, const void* A, const void* B, const float* T_save,
-                              const void* dY, void* dX, float* dA, float* dB, void* workspace, size_t ws_bytes,
-                              void* stream) {
-  int v = validate_grouped(experts, E, offsets, rank);
+int32_t grouped_moe_qlora_bwd(const qlora_weight_desc* experts, int32_t E, const int32_t* offsets, int64_t M_total,
+                              int32_t rank, float alpha, const void* X, const void* A, const void* B,
+                              const float* T_save, const void* dY, void* dX, float* dA, float* dB, void* workspace,
+                              size_t ws_bytes, void* stream) {
+  int v = validate_grouped(experts, E, M_total, rank);
   if (v != QLORA_OK) return v;
-  if (!std::isfinite(alpha)) return QLORA_ERR_INVALID;
-  if (!dA || !dB) return QLORA_ERR_INVALID;
-  const int64_t M = offsets[E];
+  if (!std::isfinite(alpha) || !offsets || !dA || !dB) return QLORA_ERR_INVALID;
   const int64_t N = experts[0].N, K = experts[0].K;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (M == 0) {
+  if (M_total == 0) {  // no rows: every expert's adapter gradients are zero
     if (cudaMemsetAsync(dA, 0, (size_t)E * rank * K * 4, st) != cudaSuccess) return QLORA_ERR_CUDA;
     return cuda_status(cudaMemsetAsync(dB, 0, (size_t)E * N * rank * 4, st));
   }
@@ -1075,47 +1072,80 @@ int32_t grouped_moe_qlora_bwd(const qlora_weight_desc* experts, int32_t E, const
   if (!aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(T_save) || !aligned16(dY) || !aligned16(dA) ||
       !aligned16(dB) || (dX && !aligned16(dX)))
     return QLORA_ERR_ALIGN;
-  GroupedPlan P;
-  build_grouped_plan(experts, E, offsets, rank, P);
-  if (!workspace || ws_bytes < P.total) return QLORA_ERR_WORKSPACE;
+  if (dX && experts[0].fmt == QLORA_FMT_BF16 && !experts_stacked(experts, E)) return QLORA_ERR_UNSUPPORTED;
+  const GroupedLayout L = grouped_layout(experts, E, M_total, rank);
+  if (!workspace || ws_bytes < L.total) return QLORA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (upload_grouped_plan(P, ws, st) != cudaSuccess) return QLORA_ERR_CUDA;
+  const GroupedSched g = grouped_sched(L, ws);
   const float s = alpha / (float)rank;
-  __nv_bfloat16* sU = reinterpret_cast<__nv_bfloat16*>(ws + P.off_act);
-  float* U = reinterpret_cast<float*>(ws + P.off_u);
-  float* part = reinterpret_cast<float*>(ws + P.off_part);
+  __nv_bfloat16* sU = reinterpret_cast<__nv_bfloat16*>(ws + L.off_act);
+  __nv_bfloat16* U2 = reinterpret_cast<__nv_bfloat16*>(ws + L.off_u2);
+  __nv_bfloat16* T2 = reinterpret_cast<__nv_bfloat16*>(ws + L.off_t2);
   const __nv_bfloat16* dYb = static_cast<const __nv_bfloat16*>(dY);
-  const int4* chunks = reinterpret_cast<const int4*>(ws + P.off_cr);
-  const int* chunk_first = reinterpret_cast<const int*>(ws + P.off_cf);
 
-  // 1) U = dY B_e per expert's rows: U fp32, sU = bf16(s U)
-  cudaError_t e = launch_row_reduce(dYb, M, N, static_cast<const __nv_bfloat16*>(B), rank, false, part, P.u, st,
-                                    reinterpret_cast<const int4*>(ws + P.off_rr), (int)P.rr.size(),
-                                    (int64_t)N * rank);
-  if (e == cudaSuccess) e = launch_fin_rows(part, P.u.splits, M, rank, s, U, sU, st);
-  // 2) dB_e = s dY_e^T T_e
-  SplitPlan cp;
-  cp.splits = (int)P.cr.size();
-  cp.chunk = 0;
-  if (e == cudaSuccess) e = launch_col_reduce(dYb, M, N, T_save, rank, part, cp, st, chunks);
-  if (e == cudaSuccess) e = launch_fin_cols_grouped(part, chunk_first, E, N, rank, s, dB, false, st);
+  // 0) tile lists from the device offsets
+  cudaError_t e = launch_grouped_schedule(offsets, E, M_total, kGroupTileRows, L.nblk_f, L.nblk_d, g,
+                                          device_error_word(), st);
   if (e != cudaSuccess) return QLORA_ERR_CUDA;
-  // 3) dX = dY deq(W_e) + sU A_e
-  if (dX) {
-    GemmMaps maps;
-    std::memset(&maps, 0, sizeof(maps));
-    bool ok = map2d(&maps.a, dY, N, M, 64, 128) && map2d(&maps.la, sU, rank, M, 64, 128) &&
-              map3d(&maps.lb, A, K, rank, E, 64, 64);
-    if (experts[0].fmt == QLORA_FMT_BF16) ok = ok && map3d_weights(&maps.w, experts, E, K, N, 64);
-    if (!ok) return QLORA_ERR_CUDA;
-    GemmArgs a = grouped_args(P, true, rank, dX, ws);
-    e = gemm_launch_grouped(experts[0].fmt, true, maps, a, st);
-    if (e != cudaSuccess) return QLORA_ERR_CUDA;
+  // 1) U = dY B_e over each expert's rows: sU = bf16(s U) for the dX GEMM,
+  //    U and T_save as hi/lo bf16 pairs for the dA / dB reductions
+  RowReduce ru = {};
+  ru.L = dYb;
+  ru.S = static_cast<const __nv_bfloat16*>(B);
+  ru.s_qj = 0;
+  ru.P = M_total;
+  ru.J = N;
+  ru.sp = plan_split_fin(L.max_rows64, N);
+  ru.scale = s;
+  ru.out_scaled = sU;
+  ru.out_hilo = U2;
+  ru.aux_src = T_save;
+  ru.aux_hilo = T2;
+  ru.tiles = g.rows64;
+  ru.tile_count = g.counts + 2;
+  ru.s_stride = N * rank;
+  ru.max_tiles = L.max_rows64;
+  if (launch_row_reduce_fin(ru, rank, st) != cudaSuccess) return QLORA_ERR_CUDA;
+
+  // 2) dB_e = s dY_e^T T_e and dA_e = s U_e^T X_e (one launch over (expert,
+  //    output tile)); an expert without rows gets zeros
+  const SplitPlan sp = grouped_col_split(L, N / 64 + K / 64);
+  ColReduce cb = {};
+  cb.L = dYb;
+  cb.S2 = T2;
+  cb.P = M_total;
+  cb.J = N;
+  cb.sp = sp;
+  cb.tiles = (int)(N / 64);
+  cb.scale = s;
+  cb.out = dB;
+  cb.transposed = 0;
+  cb.ranges = g.ranges;
+  cb.groups = E;
+  ColReduce ca = cb;
+  ca.L = static_cast<const __nv_bfloat16*>(X);
+  ca.S2 = U2;
+  ca.J = K;
+  ca.tiles = (int)(K / 64);
+  ca.out = dA;
+  ca.transposed = 1;
+  if (!dX) return cuda_status(launch_col_reduce_fin(cb, &ca, rank, st));
+
+  // 3) dX = dY deq(W_e) + sU A_e on the caller's stream, step 2 beside it on
+  //    the side stream
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  SideStream* ss = side_stream_locked();
+  if (!ss) {
+    if (run_grouped_gemm(experts, L, true, g, dY, sU, A, dX, st) != cudaSuccess) return QLORA_ERR_CUDA;
+    return cuda_status(launch_col_reduce_fin(cb, &ca, rank, st));
   }
-  // 4) dA_e = s U_e^T X_e
-  e = launch_col_reduce(static_cast<const __nv_bfloat16*>(X), M, K, U, rank, part, cp, st, chunks);
-  if (e == cudaSuccess) e = launch_fin_cols_grouped(part, chunk_first, E, K, rank, s, dA, true, st);
+  e = cudaEventRecord(ss->fork, st);
+  if (e == cudaSuccess) e = run_grouped_gemm(experts, L, true, g, dY, sU, A, dX, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
+  if (e == cudaSuccess) e = launch_col_reduce_fin(cb, &ca, rank, ss->s);
+  if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss->join, 0);
   return cuda_status(e);
 }
 

@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -42,18 +43,20 @@ constexpr int P_TMEM_COLS = 512;
 //   3: 512 x 256, two M256 x N256 accumulators sharing every decoded B tile,
 //      one TMEM buffer (all 512 columns): each accumulator is released as
 //      soon as the epilogue holds its values, so the next tile's MMAs into
-//      it can start while the previous tile is still being stored.
+//      it can start while the previous tile is still being stored;
+//   4: 256 x 256 with a quantised base, two TMEM buffers (grouped calls,
+//      whose experts own ~256 rows each).
 // Decoding one B tile for two accumulators halves the decode work per flop.
 template <int CFG>
 struct PairCfg {
-  static constexpr int NACC = CFG == 1 ? 1 : 2;           // accumulators per tile
+  static constexpr int NACC = (CFG == 1 || CFG == 4) ? 1 : 2;  // accumulators per tile
   static constexpr int TM = 256 * NACC;                   // output rows per pair tile
   static constexpr int TN = CFG == 2 ? 128 : 256;         // output columns per pair tile
   static constexpr int NBUF = NACC * TN <= 256 ? 2 : 1;   // TMEM buffers of NACC accumulators
   static constexpr int HALF_N = TN / 2;                   // B rows (or columns) per CTA
   static constexpr int A_BYTES = NACC * 128 * kBK * 2;    // this CTA's A rows
   static constexpr int B_BYTES = HALF_N * kBK * 2;        // this CTA's half of B
-  static constexpr int STAGES = CFG == 1 ? 6 : (CFG == 2 ? 5 : 4);
+  static constexpr int STAGES = (CFG == 1 || CFG == 4) ? 6 : (CFG == 2 ? 5 : 4);
   static constexpr int LINES = HALF_N;                    // decoded 64-wide lines per stage per CTA
   static constexpr int GROUP_WARPS = LINES / 32;          // one line per thread of a group
   static constexpr int GROUPS = CFG == 1 ? 3 : (CFG == 2 ? 5 : 2);  // groups rotate over stages
@@ -109,7 +112,7 @@ constexpr size_t p_smem_bytes() {
 }
 static_assert(p_smem_bytes<FMT_NF4, 3, false>() <= 232448 && p_smem_bytes<FMT_NF4, 3, true>() <= 232448 &&
                   p_smem_bytes<FMT_Q8_0, 3, true>() <= 232448 && p_smem_bytes<FMT_NF4, 2, true>() <= 232448 &&
-                  p_smem_bytes<FMT_BF16, 1, true>() <= 232448,
+                  p_smem_bytes<FMT_BF16, 1, true>() <= 232448 && p_smem_bytes<FMT_Q8_0, 4, true>() <= 232448,
               "shared memory per CTA");
 static_assert(PairRaw<FMT_NF4, 3, true>::BYTES % 128 == 0 && PairRaw<FMT_NF4, 3, true>::AQ_OFF % 128 == 0 &&
                   PairRaw<FMT_NF4, 3, true>::SC_OFF % 128 == 0,
@@ -124,6 +127,12 @@ constexpr int p_threads() {
 
 struct PairTile {
   int m0, n0;
+  int rows;  // grouped: rows of the tile that belong to its expert (from m0)
+  int e;     // grouped: expert
+};
+
+struct NoGroups {
+  int unused;
 };
 
 
@@ -134,9 +143,19 @@ struct PairTile {
 template <bool DX, int CFG>
 __device__ __forceinline__ PairTile pair_tile(const GemmArgs& a, int t) {
   constexpr int TM = PairCfg<CFG>::TM, TN = PairCfg<CFG>::TN;
+  PairTile p;
+  if (a.tile_sched) {  // grouped: the schedule kernel's list
+    const int4 s = a.tile_sched[t];
+    p.e = s.x;
+    p.m0 = s.y;
+    p.rows = s.z;
+    p.n0 = s.w * TN;
+    return p;
+  }
   const int num_m = (a.M + TM - 1) / TM;
   const int num_n = a.num_n_blk;
-  PairTile p;
+  p.e = 0;
+  p.rows = TM;
   if (!a.n_fastest) {
     p.m0 = (t % num_m) * TM;
     p.n0 = (t / num_m) * TN;
@@ -149,12 +168,17 @@ __device__ __forceinline__ PairTile pair_tile(const GemmArgs& a, int t) {
 
 }  // namespace
 
-template <int FMT, bool DX, int CFG>
+// GROUPED: tiles from the schedule list (args.tile_sched / tile_count), each
+// with its expert's weight view (tab) and adapter (3-D adapter and bf16
+// weight maps, expert index outermost); a pair CTA's 128-row block may hold
+// fewer rows of its expert, which are stored without the staging tile.
+template <int FMT, bool DX, int CFG, bool GROUPED>
 __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     qgemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_lb,
                       const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ CUtensorMap tm_aq,
-                      const GemmArgs args) {
+                      const GemmArgs args,
+                      const __grid_constant__ std::conditional_t<GROUPED, GroupTable, NoGroups> tab) {
   using Cfg = PairCfg<CFG>;
   using Raw = PairRaw<FMT, CFG, DX>;
   constexpr int P_STAGES = Cfg::STAGES, P_A_BYTES = Cfg::A_BYTES, P_B_BYTES = Cfg::B_BYTES;
@@ -175,7 +199,6 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
   const bool has_lora = args.rank > 0;
   const int nkb = args.k_red / kBK;
   const int nkb_total = nkb + (has_lora ? 1 : 0);
-  const int my_tiles = pair < args.num_tiles ? (args.num_tiles - pair + num_pairs - 1) / num_pairs : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < P_STAGES; ++s) {
@@ -213,6 +236,10 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
   // has finished, and the next kernel may start its own set-up
   griddep_wait();
   griddep_launch_dependents();
+  // grouped: the tile count comes from the schedule kernel (earlier in the
+  // stream, complete once griddep_wait returned)
+  const int num_tiles = GROUPED ? *args.tile_count : args.num_tiles;
+  const int my_tiles = pair < num_tiles ? (num_tiles - pair + num_pairs - 1) / num_pairs : 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -237,10 +264,14 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
             for (int a = 0; a < NACC; ++a) tma_load_2d_pair(sa + a * 16384, &tm_a, fb, kb * kBK, am + 256 * a);
             if (FMT == FMT_BF16) {
               if (!DX) {
-                tma_load_2d_pair(sb, &tm_w, fb, kb * kBK, bn);
+                if (GROUPED) tma_load_3d_pair(sb, &tm_w, fb, kb * kBK, bn, tc.e);
+                else tma_load_2d_pair(sb, &tm_w, fb, kb * kBK, bn);
               } else {
 #pragma unroll
-                for (int j = 0; j < HALF_N / 64; ++j) tma_load_2d_pair(sb + j * 8192, &tm_w, fb, bn + 64 * j, kb * kBK);
+                for (int j = 0; j < HALF_N / 64; ++j) {
+                  if (GROUPED) tma_load_3d_pair(sb + j * 8192, &tm_w, fb, bn + 64 * j, kb * kBK, tc.e);
+                  else tma_load_2d_pair(sb + j * 8192, &tm_w, fb, bn + 64 * j, kb * kBK);
+                }
               }
             }
           } else {
@@ -248,10 +279,14 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
             for (int a = 0; a < NACC; ++a)
               tma_load_2d_pair(sa + a * 16384, &tm_la, fb, adapter_col(args, tc.n0), am + 256 * a);
             if (!DX) {
-              tma_load_2d_pair(sb, &tm_lb, fb, 0, bn);
+              if (GROUPED) tma_load_3d_pair(sb, &tm_lb, fb, 0, bn, tc.e);
+              else tma_load_2d_pair(sb, &tm_lb, fb, 0, bn);
             } else {
 #pragma unroll
-              for (int j = 0; j < HALF_N / 64; ++j) tma_load_2d_pair(sb + j * 8192, &tm_lb, fb, bn + 64 * j, 0);
+              for (int j = 0; j < HALF_N / 64; ++j) {
+                if (GROUPED) tma_load_3d_pair(sb + j * 8192, &tm_lb, fb, bn + 64 * j, 0, tc.e);
+                else tma_load_2d_pair(sb + j * 8192, &tm_lb, fb, bn + 64 * j, 0);
+              }
             }
           }
         }
@@ -359,8 +394,31 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[slot]), 0));
           }
-          // the same for all 128 threads
-          const bool store = row0 < args.M && tc.n0 + 64 * c < args.n_out;
+          // the same for all 128 threads.  Grouped: rows of this 128-row block
+          // that belong to the tile's expert; a partly filled block is stored
+          // row by row from registers (the staging tile's TMA store would
+          // write the next expert's rows)
+          const int nvalid = GROUPED ? min(128, tc.rows - 256 * a - 128 * (int)rank) : 128;
+          const bool store = row0 < args.M && nvalid > 0 && tc.n0 + 64 * c < args.n_out;
+          if (GROUPED && store && nvalid < 128) {
+            if (row_in_tile < nvalid) {
+              uint4* dst = reinterpret_cast<uint4*>(args.out + (int64_t)(row0 + row_in_tile) * args.n_out + tc.n0 + 64 * c);
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const uint32_t* w = v + 8 * q;
+                dst[q] = make_uint4(pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                                    pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                                    pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                                    pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
+              }
+            }
+            if (!last) {
+              tmem_ld_32x32b_x32(tcol + 64 * (c + 1), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+              tmem_ld_32x32b_x32(tcol + 64 * (c + 1) + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+              tc_wait_ld();
+            }
+            continue;
+          }
           const uint32_t stile = sOut + (nstored % Raw::OUT_BUFS) * P_STAGE_OUT_BYTES;
           if (store) {
             ++nstored;
@@ -424,10 +482,12 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       int kb, lt;
       int64_t base;  // forward: first line of this thread's row; dX: k-line
       bool row_ok;   // forward: weight row in range; dX: k-line in range
+      const WeightView* wv;  // the tile's base weight (grouped: its expert's)
     };
     auto set_tile = [&](Cursor& c) {
       if (c.lt >= my_tiles) return;
       const PairTile tc = pair_tile<DX, CFG>(args, pair + c.lt * num_pairs);
+      if constexpr (GROUPED) c.wv = &tab.w[tc.e];
       if (!DX) {
         const int64_t row = tc.n0 + HALF_N * (int)rank + d;
         c.row_ok = row < args.w_rows;
@@ -497,7 +557,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
         } else if (Raw::ON) {
           load_nf4_scale(args.wv, ln, r);  // the code bytes come through the raw ring
         } else {
-          load_line<FMT>(args.wv, ln, r);
+          load_line<FMT>(*c.wv, ln, r);
         }
       }
       return valid;
@@ -579,7 +639,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     // next (two items ahead of cur, so two lines are in flight per thread;
     // measured on the Llama gate shape, three or four lines in flight are
     // slower)
-    Cursor cur{0, 0, 0, 0, false};
+    Cursor cur{0, 0, 0, 0, false, &args.wv};
     set_tile(cur);
     advance(cur, g);
     Cursor pre = cur;
@@ -661,9 +721,10 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
 }
 
 // ---------------------------------------------------------------------------
-template <int FMT, bool DX, int CFG>
-static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, cudaStream_t st) {
-  auto kern = qgemm_pair_kernel<FMT, DX, CFG>;
+template <int FMT, bool DX, int CFG, bool GROUPED>
+static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, const GroupTable* tab,
+                                   cudaStream_t st) {
+  auto kern = qgemm_pair_kernel<FMT, DX, CFG, GROUPED>;
   constexpr size_t P_SMEM_BYTES = p_smem_bytes<FMT, CFG, DX>();
   static int max_clusters = -1;  // per instantiation
   cudaLaunchConfig_t cfg = {};
@@ -688,11 +749,18 @@ static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, c
     if (e != cudaSuccess) return e;
     max_clusters = n > 0 ? n : 1;
   }
+  // grouped: num_tiles is the schedule's upper bound (the count itself is on
+  // the device)
   const int pairs = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
   if (pairs <= 0) return cudaSuccess;
   cfg.gridDim = dim3(2 * pairs);
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, maps.a, maps.w, maps.la, maps.lb, maps.out, maps.aq, args);
+  if constexpr (GROUPED) {
+    if (!tab) return cudaErrorInvalidValue;
+    return cudaLaunchKernelEx(&cfg, kern, maps.a, maps.w, maps.la, maps.lb, maps.out, maps.aq, args, *tab);
+  } else {
+    return cudaLaunchKernelEx(&cfg, kern, maps.a, maps.w, maps.la, maps.lb, maps.out, maps.aq, args, NoGroups{0});
+  }
 }
 
 #ifndef QLORA_PAIR_QCFG
@@ -700,8 +768,12 @@ static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, c
 #endif
 constexpr int kQuantCfg = QLORA_PAIR_QCFG;  // tile configuration for quantised bases
 
-int pair_tile_rows(int cfg) { return cfg == 1 ? PairCfg<1>::TM : (cfg == 2 ? PairCfg<2>::TM : PairCfg<3>::TM); }
-int pair_tile_cols(int cfg) { return cfg == 1 ? PairCfg<1>::TN : (cfg == 2 ? PairCfg<2>::TN : PairCfg<3>::TN); }
+int pair_tile_rows(int cfg) {
+  return cfg == 1 ? PairCfg<1>::TM : (cfg == 2 ? PairCfg<2>::TM : (cfg == 3 ? PairCfg<3>::TM : PairCfg<4>::TM));
+}
+int pair_tile_cols(int cfg) {
+  return cfg == 1 ? PairCfg<1>::TN : (cfg == 2 ? PairCfg<2>::TN : (cfg == 3 ? PairCfg<3>::TN : PairCfg<4>::TN));
+}
 
 // Quantised bases take 512 x 256 tiles (two accumulators share every decoded
 // weight tile) unless the launch has so few of them that the 512 x 128 tiling
@@ -720,12 +792,19 @@ int pair_cfg(int fmt, int64_t M, int64_t n_out, int num_sms) {
   return cost2 < 0.9 * cost3 ? 2 : 3;
 }
 
-template <int CFG>
-static cudaError_t launch_quant(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args, cudaStream_t st) {
+template <int CFG, bool G>
+static cudaError_t launch_quant(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args, const GroupTable* tab,
+                                cudaStream_t st) {
   switch (fmt) {
-    case FMT_NF4: return dx ? launch_pair_one<FMT_NF4, true, CFG>(maps, args, st) : launch_pair_one<FMT_NF4, false, CFG>(maps, args, st);
-    case FMT_Q8_0: return dx ? launch_pair_one<FMT_Q8_0, true, CFG>(maps, args, st) : launch_pair_one<FMT_Q8_0, false, CFG>(maps, args, st);
-    case FMT_Q4_0: return dx ? launch_pair_one<FMT_Q4_0, true, CFG>(maps, args, st) : launch_pair_one<FMT_Q4_0, false, CFG>(maps, args, st);
+    case FMT_NF4:
+      return dx ? launch_pair_one<FMT_NF4, true, CFG, G>(maps, args, tab, st)
+                : launch_pair_one<FMT_NF4, false, CFG, G>(maps, args, tab, st);
+    case FMT_Q8_0:
+      return dx ? launch_pair_one<FMT_Q8_0, true, CFG, G>(maps, args, tab, st)
+                : launch_pair_one<FMT_Q8_0, false, CFG, G>(maps, args, tab, st);
+    case FMT_Q4_0:
+      return dx ? launch_pair_one<FMT_Q4_0, true, CFG, G>(maps, args, tab, st)
+                : launch_pair_one<FMT_Q4_0, false, CFG, G>(maps, args, tab, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -735,11 +814,21 @@ cudaError_t launch_qgemm_pair(int fmt, bool dx, int cfg, const GemmMaps& maps, c
   count_launch(1);
   if (fmt == FMT_BF16) {
     if (cfg != 1) return cudaErrorInvalidValue;
-    return dx ? launch_pair_one<FMT_BF16, true, 1>(maps, args, st) : launch_pair_one<FMT_BF16, false, 1>(maps, args, st);
+    return dx ? launch_pair_one<FMT_BF16, true, 1, false>(maps, args, nullptr, st)
+              : launch_pair_one<FMT_BF16, false, 1, false>(maps, args, nullptr, st);
   }
-  if (cfg == 2) return launch_quant<2>(fmt, dx, maps, args, st);
-  if (cfg == 3) return launch_quant<3>(fmt, dx, maps, args, st);
+  if (cfg == 2) return launch_quant<2, false>(fmt, dx, maps, args, nullptr, st);
+  if (cfg == 3) return launch_quant<3, false>(fmt, dx, maps, args, nullptr, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_qgemm_pair_grouped(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args,
+                                      const GroupTable& tab, cudaStream_t st) {
+  count_launch(1);
+  if (fmt == FMT_BF16)
+    return dx ? launch_pair_one<FMT_BF16, true, 1, true>(maps, args, &tab, st)
+              : launch_pair_one<FMT_BF16, false, 1, true>(maps, args, &tab, st);
+  return launch_quant<4, true>(fmt, dx, maps, args, &tab, st);
 }
 
 }  // namespace qlora

@@ -7,7 +7,9 @@
 // K-loop ([X | sT] . [deq(W) | B]^T), so the LoRA up-projection costs r/16
 // extra MMAs per tile and no separate pass over Y.
 //
-// Persistent, warp-specialised, one CTA per SM:
+// Dense problems of at most 128 rows (larger ones and grouped calls run on
+// the SM-pair kernel of gemm_pair.cu).  Persistent, warp-specialised, one
+// CTA per SM:
 //   warp 0      TMA producer: A tiles (X or dY), and bf16 B tiles when the base
 //               is bf16 or for the adapter chunk
 //   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
@@ -58,32 +60,23 @@ constexpr int num_threads() {
 }
 
 struct TileCoord {
-  int m0, rows, n0, group;
+  int m0, rows, n0;
 };
 
 __device__ __forceinline__ TileCoord tile_coord(const GemmArgs& a, int t) {
+  // m fastest: concurrently running CTAs share the same weight slab
   TileCoord c;
-  if (a.tile_sched != nullptr) {
-    const int4 s = a.tile_sched[t];
-    c.group = s.x;
-    c.m0 = s.y;
-    c.rows = s.z;
-    c.n0 = s.w * kBN;
-  } else {
-    // m fastest: concurrently running CTAs share the same weight slab
-    const int num_m = (a.M + kBM - 1) / kBM;
-    const int mb = t % num_m, nb = t / num_m;
-    c.group = 0;
-    c.m0 = mb * kBM;
-    c.rows = min(kBM, a.M - c.m0);
-    c.n0 = nb * kBN;
-  }
+  const int num_m = (a.M + kBM - 1) / kBM;
+  const int mb = t % num_m, nb = t / num_m;
+  c.m0 = mb * kBM;
+  c.rows = min(kBM, a.M - c.m0);
+  c.n0 = nb * kBN;
   return c;
 }
 
 }  // namespace
 
-template <int FMT, bool DX, bool GROUPED>
+template <int FMT, bool DX>
 __global__ void __launch_bounds__(num_threads<FMT>(), 1)
     qgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                  const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_lb,
@@ -145,27 +138,19 @@ __global__ void __launch_bounds__(num_threads<FMT>(), 1)
             tma_load_2d(sa, &tm_a, fb, kb * kBK, tc.m0);
             if (FMT == FMT_BF16) {
               if (!DX) {
-                if (GROUPED) tma_load_3d(sb, &tm_w, fb, kb * kBK, tc.n0, tc.group);
-                else tma_load_2d(sb, &tm_w, fb, kb * kBK, tc.n0);
+                tma_load_2d(sb, &tm_w, fb, kb * kBK, tc.n0);
               } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  if (GROUPED) tma_load_3d(sb + j * 8192, &tm_w, fb, tc.n0 + 64 * j, kb * kBK, tc.group);
-                  else tma_load_2d(sb + j * 8192, &tm_w, fb, tc.n0 + 64 * j, kb * kBK);
-                }
+                for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &tm_w, fb, tc.n0 + 64 * j, kb * kBK);
               }
             }
           } else {
-            tma_load_2d(sa, &tm_la, fb, GROUPED ? 0 : adapter_col(args, tc.n0), tc.m0);
+            tma_load_2d(sa, &tm_la, fb, adapter_col(args, tc.n0), tc.m0);
             if (!DX) {
-              if (GROUPED) tma_load_3d(sb, &tm_lb, fb, 0, tc.n0, tc.group);
-              else tma_load_2d(sb, &tm_lb, fb, 0, tc.n0);
+              tma_load_2d(sb, &tm_lb, fb, 0, tc.n0);
             } else {
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                if (GROUPED) tma_load_3d(sb + j * 8192, &tm_lb, fb, tc.n0 + 64 * j, 0, tc.group);
-                else tma_load_2d(sb + j * 8192, &tm_lb, fb, tc.n0 + 64 * j, 0);
-              }
+              for (int j = 0; j < 4; ++j) tma_load_2d(sb + j * 8192, &tm_lb, fb, tc.n0 + 64 * j, 0);
             }
           }
         }
@@ -274,10 +259,6 @@ __global__ void __launch_bounds__(num_threads<FMT>(), 1)
       valid = row < args.w_rows && kl < args.w_lines_per_row;
       return row * args.w_lines_per_row + kl;
     };
-    auto view_of = [&](const TileCoord& tc) -> const WeightView& {
-      if (GROUPED) return args.groups->w[tc.group];
-      return args.wv;
-    };
 
     uint32_t it = 0;
     RawLine cur;
@@ -288,7 +269,7 @@ __global__ void __launch_bounds__(num_threads<FMT>(), 1)
       const TileCoord tc = tile_coord(args, t);
       if (kb < nkb) {
         const int64_t ln = line_of(tc, kb, cur_valid);
-        if (cur_valid) load_line<FMT>(view_of(tc), ln, cur);
+        if (cur_valid) load_line<FMT>(args.wv, ln, cur);
       }
     }
     while (t < args.num_tiles) {
@@ -300,7 +281,7 @@ __global__ void __launch_bounds__(num_threads<FMT>(), 1)
       if (tn < args.num_tiles && kbn < nkb) {
         const TileCoord tcn = tile_coord(args, tn);
         const int64_t ln = line_of(tcn, kbn, nxt_valid);
-        if (nxt_valid) load_line<FMT>(view_of(tcn), ln, nxt);
+        if (nxt_valid) load_line<FMT>(args.wv, ln, nxt);
       }
       const int s = it % STAGES;
       const uint32_t ph = (it / STAGES) & 1;
@@ -337,9 +318,9 @@ __global__ void __launch_bounds__(num_threads<FMT>(), 1)
 }
 
 // ---------------------------------------------------------------------------
-template <int FMT, bool DX, bool GROUPED>
+template <int FMT, bool DX>
 static cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& args, int num_sms, cudaStream_t st) {
-  auto kern = qgemm_kernel<FMT, DX, GROUPED>;
+  auto kern = qgemm_kernel<FMT, DX>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
@@ -353,22 +334,17 @@ static cudaError_t launch_one(const GemmMaps& maps, const GemmArgs& args, int nu
 }
 
 template <int FMT>
-static cudaError_t launch_fmt(bool dx, bool grouped, const GemmMaps& maps, const GemmArgs& args, int num_sms,
-                              cudaStream_t st) {
-  if (!dx) return grouped ? launch_one<FMT, false, true>(maps, args, num_sms, st)
-                          : launch_one<FMT, false, false>(maps, args, num_sms, st);
-  return grouped ? launch_one<FMT, true, true>(maps, args, num_sms, st)
-                 : launch_one<FMT, true, false>(maps, args, num_sms, st);
+static cudaError_t launch_fmt(bool dx, const GemmMaps& maps, const GemmArgs& args, int num_sms, cudaStream_t st) {
+  return dx ? launch_one<FMT, true>(maps, args, num_sms, st) : launch_one<FMT, false>(maps, args, num_sms, st);
 }
 
-cudaError_t launch_qgemm(int fmt, bool dx, bool grouped, const GemmMaps& maps, const GemmArgs& args, int num_sms,
-                         cudaStream_t st) {
+cudaError_t launch_qgemm(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args, int num_sms, cudaStream_t st) {
   count_launch(1);
   switch (fmt) {
-    case FMT_BF16: return launch_fmt<FMT_BF16>(dx, grouped, maps, args, num_sms, st);
-    case FMT_NF4: return launch_fmt<FMT_NF4>(dx, grouped, maps, args, num_sms, st);
-    case FMT_Q8_0: return launch_fmt<FMT_Q8_0>(dx, grouped, maps, args, num_sms, st);
-    case FMT_Q4_0: return launch_fmt<FMT_Q4_0>(dx, grouped, maps, args, num_sms, st);
+    case FMT_BF16: return launch_fmt<FMT_BF16>(dx, maps, args, num_sms, st);
+    case FMT_NF4: return launch_fmt<FMT_NF4>(dx, maps, args, num_sms, st);
+    case FMT_Q8_0: return launch_fmt<FMT_Q8_0>(dx, maps, args, num_sms, st);
+    case FMT_Q4_0: return launch_fmt<FMT_Q4_0>(dx, maps, args, num_sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

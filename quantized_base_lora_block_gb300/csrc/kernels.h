@@ -20,30 +20,15 @@ constexpr int kMaxAdapters = 4;
 void count_launch(int n);
 int* device_error_word();  // address of the device error word on the current device
 
-// ---- skinny adapter contractions (skinny.cu) --------------------------------
+// ---- skinny adapter contractions (reduce.cu) ---------------------------------
 struct SplitPlan {
   int splits;     // number of partial sums
   int64_t chunk;  // reduction elements per split (multiple of 64)
 };
 
 // Target number of CTAs for the split reductions.  A fixed constant (not the
-// device's SM count) so workspace sizes and summation order do not depend on
-// the device.
+// device's SM count) so the summation order does not depend on the device.
 constexpr int kSplitTargetCtas = 608;
-
-inline SplitPlan plan_split(int64_t outer_tiles, int64_t red_len) {
-  const int64_t red_tiles = (red_len + 63) / 64;
-  int64_t s = (kSplitTargetCtas + outer_tiles - 1) / (outer_tiles > 0 ? outer_tiles : 1);
-  if (s < 1) s = 1;
-  if (s > red_tiles) s = red_tiles;
-  if (s < 1) s = 1;
-  int64_t per = (red_tiles + s - 1) / s;
-  SplitPlan p;
-  p.chunk = per * 64;
-  p.splits = (int)((red_tiles + per - 1) / per);
-  if (p.splits < 1) p.splits = 1;
-  return p;
-}
 
 // Splits of the reductions that finish their sums in the kernel (reduce.cu):
 // the splits of one output tile form one thread-block cluster, so at most
@@ -88,6 +73,12 @@ struct RowReduce {
   int bd_nproj;
   int bd_r;
   int64_t bd_end[kMaxProj];
+  // grouped: CTA row x reduces tiles[x] = (expert, first row, rows) for
+  // x < *tile_count, with S + expert s_stride (the expert's adapter)
+  const int4* tiles;
+  const int* tile_count;
+  int64_t s_stride;
+  int max_tiles;  // grouped: grid rows (upper bound of the tile count)
   // stacked adapters: nseg > 0 scales out_scaled column q by seg_scale[i] for
   // q in [seg_end[i-1], seg_end[i]) instead of `scale`
   int nseg;
@@ -121,6 +112,11 @@ struct ColReduce {
   int seg_end[kMaxAdapters];
   float seg_scale[kMaxAdapters];
   float* seg_out[kMaxAdapters];
+  // grouped (groups > 0, same in both jobs of a launch): output tiles of
+  // every expert, reducing over the expert's rows ranges[e]; expert e's
+  // output is out + e J Q (zeros for an expert without rows)
+  const int2* ranges;
+  int groups;
 };
 // Stacked adapters: A_cat [Q x K] = the adapters' A stacked by rows, B_cat
 // [N x Q] = their B side by side (adapter i in columns [off_i, off_i + r_i)).
@@ -138,19 +134,6 @@ cudaError_t launch_row_reduce_fin(const RowReduce& r, int Q, cudaStream_t st);
 // may be null).
 cudaError_t launch_col_reduce_fin(const ColReduce& a, const ColReduce* b, int Q, cudaStream_t st);
 
-// tiles / chunks: optional grouped-row lists (see skinny.cu); null for dense.
-cudaError_t launch_row_reduce(const __nv_bfloat16* L, int64_t P, int64_t J, const __nv_bfloat16* S, int Q,
-                              bool s_qj, float* partial, const SplitPlan& sp, cudaStream_t st,
-                              const int4* tiles = nullptr, int ntiles = 0, int64_t s_stride = 0);
-cudaError_t launch_col_reduce(const __nv_bfloat16* L, int64_t P, int64_t J, const float* S, int Q,
-                              float* partial, const SplitPlan& sp, cudaStream_t st, const int4* chunks = nullptr);
-cudaError_t launch_fin_cols_grouped(const float* partial, const int* chunk_first, int groups, int64_t J, int Q,
-                                    float scale, float* out, bool transposed, cudaStream_t st);
-cudaError_t launch_fin_rows(const float* partial, int splits, int64_t P, int Q, float scale, float* out_f32,
-                            __nv_bfloat16* out_scaled, cudaStream_t st);
-cudaError_t launch_fin_cols(const float* partial, int splits, int64_t J, int Q, float scale, float* out,
-                            bool transposed, cudaStream_t st);
-
 // ---- standalone decode (dequant.cu) -------------------------------------------
 cudaError_t launch_dequant(int fmt, const WeightView& wv, int64_t lines, __nv_bfloat16* out, cudaStream_t st);
 
@@ -165,9 +148,28 @@ constexpr int kBK = 64;
 constexpr int kMaxGroups = 256;
 
 
+// Per-expert weight views of a grouped GEMM, passed as a kernel parameter
+// (12 KB for 256 experts), so a call uploads nothing.
 struct GroupTable {
   WeightView w[kMaxGroups];
 };
+
+// Grouped (mixture-of-experts) schedule, built on the device from the
+// experts' row offsets (device memory) by launch_grouped_schedule, so no
+// host synchronisation is needed.  Expert e owns rows [ranges[e].x,
+// ranges[e].y).  Tile lists hold (expert, first row, rows, column block);
+// counts = {GEMM forward tiles, GEMM dX tiles, 64-row tiles}.  Offsets that
+// are not a valid partition of [0, M_total) give empty lists and ranges and
+// record QLORA_ERR_INVALID in the device error word.
+struct GroupedSched {
+  int* counts;
+  int4* gemm_f;
+  int4* gemm_d;
+  int4* rows64;
+  int2* ranges;
+};
+cudaError_t launch_grouped_schedule(const int32_t* offsets, int E, int64_t M_total, int tile_rows, int nblk_f,
+                                    int nblk_d, const GroupedSched& s, int* err, cudaStream_t st);
 
 struct GemmArgs {
   int M;                 // total rows (of X / dY / output)
@@ -179,10 +181,11 @@ struct GemmArgs {
   int64_t w_lines_per_row;  // K_w / 64
   int64_t w_rows;           // N_w
   __nv_bfloat16* out;    // [M x n_out] bf16
-  // grouped schedule (device): tile -> (group, row0, rows); null for dense
-  const int4* tile_sched;   // x = group, y = row0, z = rows, w = n block
-  int num_groups;
-  const GroupTable* groups;  // device copy (grouped); dense uses wv below
+  // grouped (pair kernel): tile t = tile_sched[t] (expert, first row, rows,
+  // column block) for t < *tile_count (both device; written by the schedule
+  // kernel earlier in the stream); null for dense problems
+  const int4* tile_sched;
+  const int* tile_count;
   WeightView wv;
   int* err;              // device error word
   int n_fastest;         // pair kernel tile order: 1 = output column blocks fastest
@@ -213,8 +216,8 @@ struct GemmMaps {
   CUtensorMap aq;   // pair kernel, NF4 dX with raw_dq: int8 absmax codes [N x K/64], box [16 x 64]
 };
 
-cudaError_t launch_qgemm(int fmt, bool dx, bool grouped, const GemmMaps& maps, const GemmArgs& args,
-                         int num_sms, cudaStream_t st);
+cudaError_t launch_qgemm(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args, int num_sms,
+                         cudaStream_t st);
 
 // CTA-pair variant (gemm_pair.cu), dense problems only.  Tensor-map boxes:
 // A / adapter-A [64 x 128]; bf16 W and adapter-B [64 x tile_cols/2] forward,
@@ -229,5 +232,8 @@ cudaError_t launch_qgemm_pair(int fmt, bool dx, int cfg, const GemmMaps& maps, c
 // boxes of pair_tile_cols / 2 rows.
 int pair_tile_rows(int cfg);
 int pair_tile_cols(int cfg);
+// Grouped calls: configuration 4 (256 x 256) for quantised bases, 1 for bf16.
+cudaError_t launch_qgemm_pair_grouped(int fmt, bool dx, const GemmMaps& maps, const GemmArgs& args,
+                                      const GroupTable& tab, cudaStream_t st);
 
 }  // namespace qlora

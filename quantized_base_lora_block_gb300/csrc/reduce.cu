@@ -93,7 +93,6 @@ __global__ void __launch_bounds__(NTHR) rr_fin_kernel(const RowReduce jb) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t P = jb.P, J = jb.J;
-  const int64_t p0 = (int64_t)blockIdx.x * TP;
   const int64_t j_begin = (int64_t)blockIdx.y * jb.sp.chunk;
   const int64_t j_end = min(J, j_begin + jb.sp.chunk);
   const int nchunks = j_end > j_begin ? (int)((j_end - j_begin + TJ - 1) / TJ) : 0;
@@ -101,6 +100,17 @@ __global__ void __launch_bounds__(NTHR) rr_fin_kernel(const RowReduce jb) {
   const __nv_bfloat16* __restrict__ S = jb.S;
   griddep_wait();
   griddep_launch_dependents();
+  int64_t p0 = (int64_t)blockIdx.x * TP, p_lim = P;
+  if (jb.tiles) {
+    // grouped: the tile list comes from the schedule kernel earlier in the
+    // stream; every CTA of the cluster has the same row tile, so a cluster
+    // past the list leaves as a whole
+    if ((int)blockIdx.x >= *jb.tile_count) return;
+    const int4 t = jb.tiles[blockIdx.x];
+    p0 = t.y;
+    p_lim = (int64_t)t.y + t.z;
+    S += (int64_t)t.x * jb.s_stride;
+  }
 
   auto load_chunk = [&](int buf, int64_t j0) {
     __nv_bfloat16* dL = sL + buf * TP * LPITCH;
@@ -109,7 +119,7 @@ __global__ void __launch_bounds__(NTHR) rr_fin_kernel(const RowReduce jb) {
     for (int i = 0; i < 4; ++i) {  // 64 x 64 tile = 512 16-byte pieces
       const int piece = tid + i * NTHR;
       const int r = piece >> 3, c8 = (piece & 7) * 8;
-      const bool ok = (p0 + r) < P;
+      const bool ok = (p0 + r) < p_lim;
       cp_async16(s_addr(dL + r * LPITCH + c8), L + (ok ? (p0 + r) : 0) * J + j0 + c8, ok);
     }
     if (S_QJ) {  // Q rows x 64 columns
@@ -215,7 +225,7 @@ __global__ void __launch_bounds__(NTHR) rr_fin_kernel(const RowReduce jb) {
   // cluster in rank order
   const uint32_t splits = (uint32_t)jb.sp.splits;
   const uint32_t rank = cluster_ctarank();
-  const int rows = (int)(P - p0 < TP ? P - p0 : TP);
+  const int rows = (int)(p_lim - p0 < TP ? p_lim - p0 : TP);
   for (int it = (int)rank * NTHR + tid; it < rows * (Q / 4); it += (int)splits * NTHR) {
     const float* src = sP + it * 4;
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -264,25 +274,42 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
   __nv_bfloat16* sL = reinterpret_cast<__nv_bfloat16*>(cr_smem);  // NS x [64 x 72]
   __nv_bfloat16* sS = sL + NS * TP * LPITCH;                         // NS x [64 x (2Q + 8)]
 
-  const bool second = (int)blockIdx.x >= ja.tiles;
+  // grouped: x runs over (expert, output tile of either job)
+  int x = (int)blockIdx.x, grp = 0;
+  if (ja.groups > 0) {
+    const int per = ja.tiles + jbb.tiles;
+    grp = x / per;
+    x -= grp * per;
+  }
+  const bool second = x >= ja.tiles;
   ColReduce jb;
   if (second)
     jb = jbb;
   else
     jb = ja;
-  const int tile = second ? (int)blockIdx.x - ja.tiles : (int)blockIdx.x;
+  const int tile = second ? x - ja.tiles : x;
   const int split = (int)blockIdx.y;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t P = jb.P, J = jb.J;
   const int64_t j0 = (int64_t)tile * TJ;
-  const int64_t p_begin = (int64_t)split * jb.sp.chunk;
-  const int64_t p_end = min(P, p_begin + jb.sp.chunk);
-  const int nchunks = p_end > p_begin ? (int)((p_end - p_begin + TP - 1) / TP) : 0;
   const __nv_bfloat16* __restrict__ L = jb.L;
   const __nv_bfloat16* __restrict__ S2 = jb.S2;
   griddep_wait();
   griddep_launch_dependents();
+  int64_t p_begin = (int64_t)split * jb.sp.chunk;
+  int64_t p_end = min(P, p_begin + jb.sp.chunk);
+  if (jb.groups > 0) {
+    // the expert's rows (from the schedule kernel), split evenly over the
+    // cluster in 64-row chunks; the expert's block of the output
+    const int2 rg = jb.ranges[grp];
+    const int64_t n64 = (rg.y - rg.x + TP - 1) / TP;
+    const int64_t per = (n64 + jb.sp.splits - 1) / jb.sp.splits * TP;
+    p_begin = rg.x + (int64_t)split * per;
+    p_end = min((int64_t)rg.y, p_begin + per);
+    jb.out += (int64_t)grp * J * Q;
+  }
+  const int nchunks = p_end > p_begin ? (int)((p_end - p_begin + TP - 1) / TP) : 0;
 
   auto load_chunk = [&](int buf, int64_t pp) {
     __nv_bfloat16* dL = sL + buf * TP * LPITCH;
@@ -505,7 +532,7 @@ template <int Q>
 static cudaError_t launch_rr_fin_q(const RowReduce& r, cudaStream_t st) {
   constexpr int NS = RowStages<Q>::NS;
   const size_t smem = (size_t)NS * 2 * (TP * LPITCH + (r.s_qj ? Q * LPITCH : TJ * (Q + 8)));
-  const dim3 grid((unsigned)((r.P + TP - 1) / TP), (unsigned)r.sp.splits);
+  const dim3 grid((unsigned)(r.tiles ? r.max_tiles : (r.P + TP - 1) / TP), (unsigned)r.sp.splits);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   if (r.sp.splits > kMaxClusterSplits) return cudaErrorInvalidValue;
   static bool attr_qj = false, attr_jq = false;
@@ -517,7 +544,7 @@ template <int Q>
 static cudaError_t launch_cr_fin_q(const ColReduce& a, const ColReduce& b, cudaStream_t st) {
   constexpr int NS = kColStages;
   constexpr size_t smem = (size_t)NS * 2 * (TP * LPITCH + TP * (2 * Q + 8));
-  const dim3 grid((unsigned)(a.tiles + b.tiles), (unsigned)a.sp.splits);
+  const dim3 grid((unsigned)((a.tiles + b.tiles) * (a.groups > 0 ? a.groups : 1)), (unsigned)a.sp.splits);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   if (a.sp.splits > kMaxClusterSplits || (b.tiles > 0 && b.sp.splits != a.sp.splits)) return cudaErrorInvalidValue;
   static bool attr = false;

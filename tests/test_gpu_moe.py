@@ -1,5 +1,7 @@
-"""grouped_moe_qlora_fwd / _bwd (rows sorted by expert) against the oracle's
-per-expert loop; empty experts must get exactly zero adapter gradients."""
+"""grouped_moe_qlora_fwd / _bwd (rows sorted by expert, offsets in device
+memory) against the oracle's per-expert loop; empty experts must get exactly
+zero adapter gradients; offsets that do not partition the rows are reported
+through the device error word."""
 import numpy as np
 import pytest
 
@@ -34,10 +36,10 @@ def _run(lib, d):
         ws = [lib.DeviceWeight.from_packed(w) for w in d["W"]]
     X, dY = lib.bf16_from_bits(d["X"]), lib.bf16_from_bits(d["dY"])
     A, B = lib.bf16_from_bits(d["A"]), lib.bf16_from_bits(d["B"])
-    Y, T = lib.grouped_fwd(ws, d["off"], X, A, B, d["alpha"])
-    dX, dA, dB = lib.grouped_bwd(ws, d["off"], X, A, B, T, dY, d["alpha"])
-    torch.cuda.synchronize()
-    assert lib.device_error() == 0
+    off = lib.device_offsets(d["off"])  # device int32 [E+1], as a router leaves them
+    Y, T = lib.grouped_fwd(ws, off, X, A, B, d["alpha"])
+    dX, dA, dB = lib.grouped_bwd(ws, off, X, A, B, T, dY, d["alpha"])
+    assert lib.last_device_error() == 0
     return {"Y": lib.bits_from_bf16(Y), "T": T.cpu().numpy(), "dX": lib.bits_from_bf16(dX),
             "dA": dA.cpu().numpy(), "dB": dB.cpu().numpy()}
 
@@ -86,29 +88,89 @@ def test_grouped_all_experts_empty(lib):
     assert float(dA.abs().max()) == 0.0 and float(dB.abs().max()) == 0.0
 
 
-def test_one_expert_equals_dense(lib):
-    """E = 1 runs the same tiles as the dense call (M <= 128): Y, T and dX
-    are bitwise equal; dA / dB sum their rows in different chunks."""
-    d = _moe_inputs([100], K=256, N=256, r=16, fmt="nf4", seed=5)
+def _close_ulps(a_bits, b_bits, name, ulps=2):
+    """Elementwise |a - b| <= ulps bf16 ulps of |a| (the two calls round the
+    same sums after different split / tile orders)."""
+    a = oracle.bf16_bits_to_f64(a_bits)
+    b = oracle.bf16_bits_to_f64(b_bits.reshape(a_bits.shape))
+    tol = ulps * np.maximum(np.abs(a), 1e-30) * 2.0 ** -7
+    assert np.all(np.abs(a - b) <= tol), f"{name}: max diff {np.abs(a - b).max():.3g}"
+
+
+@pytest.mark.parametrize("rows", [100, 700])
+def test_one_expert_equals_dense(lib, rows):
+    """E = 1 computes the dense layer over the same rows (different tile
+    shapes and split orders, so compared within rounding)."""
+    d = _moe_inputs([rows], K=256, N=512, r=16, fmt="nf4", seed=5)
     got = _run(lib, d)
     inp = {"X": d["X"], "A": d["A"][0], "B": d["B"][0], "dY": d["dY"], "W": d["W"][0], "alpha": d["alpha"]}
     from gpu_helpers import run_layer
 
     dense = run_layer(inp)
-    for k in ("Y", "T", "dX"):
-        assert np.array_equal(got[k].reshape(-1), dense[k].reshape(-1)), k
-    check_f32(got["dA"][0], dense["dA"].astype(np.float64), "dA vs dense")
-    check_f32(got["dB"][0], dense["dB"].astype(np.float64), "dB vs dense")
+    _close_ulps(got["Y"], dense["Y"], "Y")
+    _close_ulps(got["dX"], dense["dX"], "dX")
+    check_f32(got["T"], dense["T"].astype(np.float64), "T vs dense", rel=1e-5)
+    check_f32(got["dA"][0], dense["dA"].astype(np.float64), "dA vs dense", rel=1e-5)
+    check_f32(got["dB"][0], dense["dB"].astype(np.float64), "dB vs dense", rel=1e-5)
+
+
+@pytest.mark.parametrize("bad", [[0, 40, 30, 100], [0, 40, 70, 90], [5, 40, 70, 100], [0, 40, 70, 130]])
+def test_invalid_offsets_reported(lib, bad):
+    """Offsets that are not a partition of [0, M_total) (decreasing, short,
+    not starting at 0, past the end) make both calls do no GEMM work and
+    record QLORA_ERR_INVALID in the device error word; the offsets are never
+    read on the host."""
+    import torch
+
+    d = _moe_inputs([40, 30, 30], K=128, N=256, r=8, fmt="q8_0", seed=9)
+    ws = [lib.DeviceWeight.from_packed(w) for w in d["W"]]
+    X, dY = lib.bf16_from_bits(d["X"]), lib.bf16_from_bits(d["dY"])
+    A, B = lib.bf16_from_bits(d["A"]), lib.bf16_from_bits(d["B"])
+    off = torch.tensor(bad, dtype=torch.int32, device="cuda")
+    assert lib.last_device_error() == 0
+    Y = torch.zeros((100, 256), dtype=torch.bfloat16, device="cuda")
+    _, T = lib.grouped_fwd(ws, off, X, A, B, d["alpha"], Y=Y)
+    assert lib.last_device_error() == lib.QLORA_ERR_INVALID
+    assert float(Y.float().abs().max()) == 0.0  # no tile was scheduled
+    dX = torch.zeros((100, 128), dtype=torch.bfloat16, device="cuda")
+    T.zero_()
+    lib.grouped_bwd(ws, off, X, A, B, T, dY, d["alpha"], dX=dX)
+    assert lib.last_device_error() == lib.QLORA_ERR_INVALID
+    assert float(dX.float().abs().max()) == 0.0
+    assert lib.last_device_error() == 0  # cleared by the read
+
+
+def test_offsets_written_on_device(lib):
+    """Offsets produced by a device computation (a prefix sum of per-expert
+    counts) feed the call directly."""
+    import torch
+
+    counts = [3, 0, 77, 200, 1]
+    d = _moe_inputs(counts, K=192, N=256, r=24, fmt="q4_0", seed=11)
+    c = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    off = torch.zeros(len(counts) + 1, dtype=torch.int32, device="cuda")
+    off[1:] = torch.cumsum(c, 0).to(torch.int32)
+    ws = [lib.DeviceWeight.from_packed(w) for w in d["W"]]
+    X, dY = lib.bf16_from_bits(d["X"]), lib.bf16_from_bits(d["dY"])
+    A, B = lib.bf16_from_bits(d["A"]), lib.bf16_from_bits(d["B"])
+    Y, T = lib.grouped_fwd(ws, off, X, A, B, d["alpha"])
+    dX, dA, dB = lib.grouped_bwd(ws, off, X, A, B, T, dY, d["alpha"])
+    assert lib.last_device_error() == 0
+    got = {"Y": lib.bits_from_bf16(Y), "T": T.cpu().numpy(), "dX": lib.bits_from_bf16(dX),
+           "dA": dA.cpu().numpy(), "dB": dB.cpu().numpy()}
+    _check(d, got, _oracle(d))
 
 
 @pytest.mark.slow
-def test_moe_workload_gate(lib):
+@pytest.mark.parametrize("lin", [0, 2], ids=["gate_2048x768", "down_768x2048"])
+def test_moe_workload(lib, lin):
     """128 experts, top-8 Zipf-skewed routing of 4096 tokens (32,768 rows,
-    4 experts empty), gate projection 2048 -> 768 in Q8_0, rank 16."""
+    4 experts empty), Q8_0 bases, rank 16: the gate projection 2048 -> 768
+    and the down projection 768 -> 2048, at full size."""
     mw = syn.MOE
     off, _, counts = syn.moe_routing()
     assert counts.min() == 0
-    d = syn.make_moe_linear_inputs(mw, 0, off, seed=0)
+    d = syn.make_moe_linear_inputs(mw, lin, off, seed=0)
     dd = {"X": d["X"], "dY": d["dY"], "A": d["A"], "B": d["B"], "W": d["W"], "off": off, "alpha": d["alpha"],
           "r": d["rank"]}
     _check(dd, _run(lib, dd), _oracle(dd))
