@@ -10,6 +10,9 @@ from .qlora_oracle import (  # noqa: F401
     bf16_round_f32,
     dequant,
     dequant_bf16_bits,
+    e2m1_value,
+    e4m3_value,
+    q4_k_scale_min,
     linear_fwd,
     linear_bwd,
     linear_fwd_rows,

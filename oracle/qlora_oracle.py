@@ -34,6 +34,26 @@ What it computes, and where it comes from:
       Q8_0  32 elements per 34-byte block {fp16 d, int8[32]}.
             value = bf16_rn( q * f32(d) )           (the product is exact)
       bf16  the stored value.
+
+  Further base formats (Surogate README: "Native GGUF" row names K-quants,
+  the quickstart quantises to q4_k_m; "LoRA & QLoRA" and "Native precision
+  recipes" rows name FP8 and NVFP4 bases; heatdrop.ai summary: FP8 E4M3 and
+  NVFP4 (E2M1) recipes).  The pages print no layout; the readings:
+      NF4 with an 8-bit map (QLoRA-style double quantisation): the absmax
+            byte is an index into a 256-entry fp32 map and a fixed offset is
+            added back:  absmax' = f32_rn( f32_rn(map[q] * scale2) + offset )
+      Q4_K  GGUF super-blocks of 256 elements, 144 bytes {fp16 d, fp16 dmin,
+            12 bytes of eight 6-bit sub-block scales sc[j] and mins m[j],
+            128 bytes of 4-bit codes}; sub-block j = 32 elements.
+            value = bf16_rn( f32_rn( (d sc[j]) q - (dmin m[j]) ) )
+            (both products are exact in fp32, so one rounding)
+      FP8   E4M3 codes (OCP 8-bit float, no infinities, S.1111.111 = NaN),
+            one per element, with one fp32 scale for the whole tensor.
+            value = bf16_rn( f32_rn( e4m3(c) * scale ) )
+      NVFP4 E2M1 codes, two per byte (element 2j in the LOW nibble of byte
+            j), an E4M3 scale per 16 consecutive elements and one fp32
+            scale for the whole tensor.
+            value = bf16_rn( f32_rn( e2m1(c) * f32_rn( e4m3(s_blk) * scale ) ) )
 """
 from __future__ import annotations
 
@@ -83,11 +103,19 @@ def _dequant_nf4(w: Dict, N: int, K: int) -> np.ndarray:
     if "absmax" in w and w["absmax"] is not None:
         amax = np.asarray(w["absmax"], dtype=np.float32).reshape(-1)
     else:
-        q = np.asarray(w["absmax_q"], dtype=np.int8).reshape(-1).astype(np.float32)
         scale2 = np.asarray(w["absmax_scale"], dtype=np.float32).reshape(-1)
         group = int(w.get("dq_group", 256))
         g = np.arange(nblk) // group
-        amax = (q * scale2[g]).astype(np.float32)          # fp32 product
+        if w.get("absmax_map") is None:
+            q = np.asarray(w["absmax_q"], dtype=np.int8).reshape(-1).astype(np.float32)
+            amax = (q * scale2[g]).astype(np.float32)          # fp32 product
+        else:
+            # the byte indexes the 8-bit map; then scale and offset, each step
+            # rounded to fp32
+            idx = np.asarray(w["absmax_q"]).reshape(-1).view(np.uint8).astype(np.int64)
+            amap = np.asarray(w["absmax_map"], dtype=np.float32).reshape(256)
+            amax = (amap[idx] * scale2[g]).astype(np.float32)
+            amax = (amax + np.float32(w["absmax_offset"])).astype(np.float32)
     assert amax.size == nblk
     prod = (NF4_LEVELS[codes] * amax[:, None]).astype(np.float32)  # fp32 product
     return bf16_round_f32(prod).astype(np.float64).reshape(N, K)
@@ -116,6 +144,89 @@ def _dequant_q8_0(w: Dict, N: int, K: int) -> np.ndarray:
     return bf16_round_f32(prod).astype(np.float64).reshape(N, K)
 
 
+def _dequant_q4_k(w: Dict, N: int, K: int) -> np.ndarray:
+    assert K % 256 == 0
+    data = np.asarray(w["data"], dtype=np.uint8).reshape(-1)
+    assert data.size == N * K // 256 * 144
+    sb = data.reshape(-1, 144)
+    d = sb[:, 0:2].copy().view("<f2").astype(np.float32).reshape(-1)
+    dmin = sb[:, 2:4].copy().view("<f2").astype(np.float32).reshape(-1)
+    sc, mn = q4_k_scale_min(sb[:, 4:16])                      # [nsb, 8] each
+    qs = sb[:, 16:144].reshape(-1, 4, 32)                     # 4 chunks of 32 bytes
+    # chunk c: low nibbles are sub-block 2c, high nibbles sub-block 2c+1
+    q = np.stack([qs & 0x0F, qs >> 4], axis=2).reshape(-1, 8, 32).astype(np.float32)
+    dsc = (d[:, None] * sc.astype(np.float32)).astype(np.float32)      # exact
+    mmn = (dmin[:, None] * mn.astype(np.float32)).astype(np.float32)   # exact
+    prod = (dsc[:, :, None] * q).astype(np.float32)                    # exact
+    val = (prod - mmn[:, :, None]).astype(np.float32)                  # one rounding
+    return bf16_round_f32(val).astype(np.float64).reshape(N, K)
+
+
+def q4_k_scale_min(b: np.ndarray):
+    """Eight 6-bit scales and mins from the 12 packed bytes of a Q4_K
+    super-block ([n, 12] uint8 -> two [n, 8] int arrays).  Sub-blocks 0..3:
+    scale = low 6 bits of byte j, min = low 6 bits of byte j+4.  Sub-blocks
+    4..7: low 4 bits from byte j+4 (scale: its low nibble, min: its high
+    nibble), top 2 bits from the top 2 bits of byte j-4 (scale) and byte j
+    (min)."""
+    b = np.asarray(b, dtype=np.uint8).astype(np.int64)
+    sc = np.empty((b.shape[0], 8), dtype=np.int64)
+    mn = np.empty((b.shape[0], 8), dtype=np.int64)
+    for j in range(4):
+        sc[:, j] = b[:, j] & 63
+        mn[:, j] = b[:, j + 4] & 63
+    for j in range(4, 8):
+        sc[:, j] = (b[:, j + 4] & 0x0F) | ((b[:, j - 4] >> 6) << 4)
+        mn[:, j] = (b[:, j + 4] >> 4) | ((b[:, j] >> 6) << 4)
+    return sc, mn
+
+
+def e4m3_value(code) -> np.ndarray:
+    """OCP 8-bit float E4M3 (bias 7, 3 mantissa bits, subnormals, no
+    infinities; exponent and mantissa all ones is NaN), as fp64."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
+    sign = np.where((c >> 7) & 1, -1.0, 1.0)
+    e = (c >> 3) & 0x0F
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    v = sign * mag
+    return np.where((e == 15) & (m == 7), np.nan, v)
+
+
+def e2m1_value(code) -> np.ndarray:
+    """4-bit float E2M1 (bias 1, 1 mantissa bit, a subnormal 0.5, no
+    infinities or NaN), as fp64; only the low 4 bits of `code` are used."""
+    c = np.asarray(code, dtype=np.uint8).astype(np.int64) & 0x0F
+    sign = np.where((c >> 3) & 1, -1.0, 1.0)
+    e = (c >> 1) & 3
+    m = (c & 1).astype(np.float64)
+    mag = np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2((e - 1).astype(np.float64)))
+    return sign * mag
+
+
+def _dequant_fp8(w: Dict, N: int, K: int) -> np.ndarray:
+    c = np.asarray(w["data"], dtype=np.uint8).reshape(-1)
+    assert c.size == N * K
+    scale = np.float32(np.asarray(w["tensor_scale"], dtype=np.float32).reshape(-1)[0])
+    prod = (e4m3_value(c).astype(np.float32) * scale).astype(np.float32)   # e4m3 is exact in fp32
+    return bf16_round_f32(prod).astype(np.float64).reshape(N, K)
+
+
+def _dequant_nvfp4(w: Dict, N: int, K: int) -> np.ndarray:
+    assert K % 16 == 0
+    packed = np.asarray(w["data"], dtype=np.uint8).reshape(-1)
+    assert packed.size == N * K // 2
+    codes = np.empty(N * K, dtype=np.uint8)
+    codes[0::2] = packed & 0x0F
+    codes[1::2] = packed >> 4
+    sblk = np.asarray(w["block_scale"], dtype=np.uint8).reshape(-1)
+    assert sblk.size == N * K // 16
+    scale = np.float32(np.asarray(w["tensor_scale"], dtype=np.float32).reshape(-1)[0])
+    b = (e4m3_value(sblk).astype(np.float32) * scale).astype(np.float32)  # block factor, fp32
+    v = (e2m1_value(codes).astype(np.float32).reshape(-1, 16) * b[:, None]).astype(np.float32)
+    return bf16_round_f32(v).astype(np.float64).reshape(N, K)
+
+
 def dequant(w: Dict) -> np.ndarray:
     """Decoded base weight deq(Wq) as fp64 [N, K] (every value a bf16 value)."""
     N, K, fmt = int(w["N"]), int(w["K"]), w["fmt"]
@@ -127,6 +238,12 @@ def dequant(w: Dict) -> np.ndarray:
         return _dequant_q4_0(w, N, K)
     if fmt == "q8_0":
         return _dequant_q8_0(w, N, K)
+    if fmt == "q4_k":
+        return _dequant_q4_k(w, N, K)
+    if fmt == "fp8_e4m3":
+        return _dequant_fp8(w, N, K)
+    if fmt == "nvfp4":
+        return _dequant_nvfp4(w, N, K)
     raise ValueError(fmt)
 
 

@@ -27,7 +27,7 @@ import numpy as np
 # Sub-stream ids, one per tensor kind.
 S_X, S_W, S_A, S_B, S_DY, S_ROUTER = 0, 1, 2, 3, 4, 5
 
-FORMATS = ("bf16", "nf4", "q8_0", "q4_0")
+FORMATS = ("bf16", "nf4", "q8_0", "q4_0", "q4_k", "fp8_e4m3", "nvfp4")
 
 
 # ----------------------------------------------------------------------------
@@ -86,7 +86,19 @@ def _nf4_midpoints() -> np.ndarray:
     return _NF4_MID
 
 
-def pack_nf4(w: np.ndarray, double_quant: bool, dq_group: int = 256) -> Dict[str, np.ndarray]:
+def float8_map() -> np.ndarray:
+    """An 8-bit float map for absmax codes (QLoRA-style double
+    quantisation): the values of the 256 E4M3 codes divided by the largest
+    (448), the two NaN codes standing in for +1 and -1.  Computed with the
+    E4M3 conversion of PyTorch."""
+    import torch
+
+    v = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    v[0x7F], v[0xFF] = 448.0, -448.0
+    return (v / 448.0).astype(np.float32)
+
+
+def pack_nf4(w: np.ndarray, double_quant: bool, dq_group: int = 256, dq_map: bool = False) -> Dict[str, np.ndarray]:
     """w: fp32 [N, K], K % 64 == 0.  Blocks of 64 consecutive K-elements.
 
     absmax = max|w| over the block (fp32).  code = the nearest NF4 level to
@@ -97,6 +109,11 @@ def pack_nf4(w: np.ndarray, double_quant: bool, dq_group: int = 256) -> Dict[str
     block order); scale2 = max(absmax in group)/127 (fp32) and
     absmax_q = clamp(round_half_even(absmax/scale2), 0, 127) as int8.  Codes
     are chosen with the exact fp32 absmax (codes first, then the constants).
+
+    dq_map (QLoRA style): offset = mean of all absmax values (fp32); per group
+    scale2 = max |absmax - offset| (fp32); the code is the index of the
+    float8_map() entry nearest to (absmax - offset) / scale2 (lowest index on
+    ties); stored as bytes in absmax_q with the map and the offset.
     """
     w = np.ascontiguousarray(w, dtype=np.float32)
     N, K = w.shape
@@ -117,7 +134,28 @@ def pack_nf4(w: np.ndarray, double_quant: bool, dq_group: int = 256) -> Dict[str
     flat = codes.reshape(-1)
     packed = ((flat[0::2] << 4) | flat[1::2]).astype(np.uint8)
     out = {"fmt": "nf4", "N": N, "K": K, "data": packed}
-    if double_quant:
+    if double_quant and dq_map:
+        nb = amax.shape[0]
+        ng = (nb + dq_group - 1) // dq_group
+        offset = np.float32(amax.astype(np.float64).mean())
+        cen = amax.astype(np.float64) - float(offset)
+        pad = np.zeros(ng * dq_group)
+        pad[:nb] = np.abs(cen)
+        scale2 = pad.reshape(ng, dq_group).max(axis=1).astype(np.float32)
+        s_rep = np.repeat(scale2, dq_group)[:nb].astype(np.float64)
+        x = np.where(s_rep > 0, cen / np.where(s_rep > 0, s_rep, 1.0), 0.0)
+        amap = float8_map().astype(np.float64)
+        order = np.argsort(amap, kind="stable")
+        sv = amap[order]
+        j = np.clip(np.searchsorted(sv, x), 1, 255)
+        pick = np.where(np.abs(x - sv[j - 1]) <= np.abs(sv[j] - x), j - 1, j)
+        code = order[pick].astype(np.uint8)
+        out["absmax_q"] = code.view(np.int8)
+        out["absmax_scale"] = scale2
+        out["absmax_map"] = amap.astype(np.float32)
+        out["absmax_offset"] = float(offset)
+        out["dq_group"] = dq_group
+    elif double_quant:
         nb = amax.shape[0]
         ng = (nb + dq_group - 1) // dq_group
         pad = np.zeros(ng * dq_group, dtype=np.float32)
@@ -188,6 +226,112 @@ def pack_q8_0(w: np.ndarray) -> Dict[str, np.ndarray]:
     return {"fmt": "q8_0", "N": N, "K": K, "data": rec.reshape(-1)}
 
 
+def pack_q4_k(w: np.ndarray) -> Dict[str, np.ndarray]:
+    """GGUF Q4_K: super-blocks of 256 along K, 144 bytes each: fp16 d, fp16
+    dmin, 12 bytes of eight 6-bit (scale, min) pairs, 128 bytes of codes.
+
+    Sub-block j (32 elements): lo = min(0, min w), hi = max w,
+    scale_j = (hi - lo)/15, min_j = -lo.  d = fp16(max scale_j / 63),
+    dmin = fp16(max min_j / 63); sc_j = clamp(rint(scale_j/d), 0, 63),
+    m_j = clamp(rint(min_j/dmin), 0, 63); q = clamp(rint((w + dmin m_j) /
+    (d sc_j)), 0, 15).  Chunk c of 64 elements takes bytes 32c..32c+31 of the
+    codes: sub-block 2c in the low nibbles, 2c+1 in the high nibbles.
+    Scale bytes: sub-blocks 0..3 in the low 6 bits of bytes j (scale) and
+    j+4 (min); sub-blocks 4..7 keep their low 4 bits in byte j+4 (scale low
+    nibble, min high nibble) and their top 2 bits in the top bits of bytes
+    j-4 (scale) and j (min).
+    """
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    assert K % 256 == 0
+    sb = w.reshape(-1, 8, 32).astype(np.float64)
+    lo = np.minimum(sb.min(axis=2), 0.0)
+    hi = sb.max(axis=2)
+    scale = (hi - lo) / 15.0
+    mins = -lo
+    d16 = (scale.max(axis=1) / 63.0).astype(np.float16)
+    m16 = (mins.max(axis=1) / 63.0).astype(np.float16)
+    d, dm = d16.astype(np.float64), m16.astype(np.float64)
+    sc = np.clip(np.rint(scale / np.where(d > 0, d, 1.0)[:, None]), 0, 63).astype(np.int64)
+    mn = np.clip(np.rint(mins / np.where(dm > 0, dm, 1.0)[:, None]), 0, 63).astype(np.int64)
+    sc[d == 0] = 0
+    mn[dm == 0] = 0
+    step = d[:, None] * sc
+    q = np.rint((sb + (dm[:, None] * mn)[:, :, None]) / np.where(step > 0, step, 1.0)[:, :, None])
+    q = np.clip(q, 0, 15)
+    q[np.broadcast_to((step == 0)[:, :, None], q.shape)] = 0
+    q = q.astype(np.uint8)
+    nsb = sb.shape[0]
+    rec = np.zeros((nsb, 144), dtype=np.uint8)
+    rec[:, 0:2] = d16.view(np.uint8).reshape(-1, 2)
+    rec[:, 2:4] = m16.view(np.uint8).reshape(-1, 2)
+    b = np.zeros((nsb, 12), dtype=np.int64)
+    for j in range(4):
+        b[:, j] = sc[:, j] | ((sc[:, j + 4] >> 4) << 6)
+        b[:, j + 4] = mn[:, j] | ((mn[:, j + 4] >> 4) << 6)
+        b[:, j + 8] = (sc[:, j + 4] & 0x0F) | ((mn[:, j + 4] & 0x0F) << 4)
+    rec[:, 4:16] = b.astype(np.uint8)
+    qc = q.reshape(nsb, 4, 2, 32)
+    rec[:, 16:] = (qc[:, :, 0, :] | (qc[:, :, 1, :] << 4)).reshape(nsb, 128)
+    return {"fmt": "q4_k", "N": N, "K": K, "data": rec.reshape(-1)}
+
+
+def _to_e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """Round to E4M3 codes (nearest, ties to even; saturated to +-448) with
+    PyTorch's conversion."""
+    import torch
+
+    t = torch.from_numpy(np.clip(np.ascontiguousarray(x, dtype=np.float32), -448.0, 448.0))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+
+
+def _e4m3_codes_to_f32(c: np.ndarray) -> np.ndarray:
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(c, dtype=np.uint8)).view(torch.float8_e4m3fn).float().numpy()
+
+
+def pack_fp8_e4m3(w: np.ndarray) -> Dict[str, np.ndarray]:
+    """FP8 E4M3 codes with one fp32 scale for the tensor: scale =
+    max|w| / 448 (1 if the tensor is zero), code = E4M3(w / scale)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    amax = np.float32(np.abs(w).max()) if w.size else np.float32(0)
+    scale = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+    codes = _to_e4m3_codes((w / scale).astype(np.float32))
+    return {"fmt": "fp8_e4m3", "N": N, "K": K, "data": codes.reshape(-1),
+            "tensor_scale": np.array([scale], dtype=np.float32)}
+
+
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def pack_nvfp4(w: np.ndarray) -> Dict[str, np.ndarray]:
+    """NVFP4: E2M1 codes in blocks of 16 along K, an E4M3 scale per block
+    and one fp32 scale for the tensor.  scale = max|w| / (6 * 448);
+    block scale = E4M3(max|w in block| / 6 / scale); with the block factor
+    b = f32(E4M3 value) * scale, each element takes the E2M1 magnitude
+    nearest to |w| / b (lower one on ties) and the sign of w.  Element 2j in
+    the low nibble of byte j."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    N, K = w.shape
+    assert K % 16 == 0
+    amax = np.float32(np.abs(w).max()) if w.size else np.float32(0)
+    ts = np.float32(amax / np.float32(6.0 * 448.0)) if amax > 0 else np.float32(1.0)
+    blk = w.reshape(-1, 16)
+    bmax = np.abs(blk).max(axis=1).astype(np.float32)
+    sc = _to_e4m3_codes((bmax / np.float32(6.0) / ts).astype(np.float32))
+    b = (_e4m3_codes_to_f32(sc) * ts).astype(np.float32).astype(np.float64)
+    x = np.abs(blk.astype(np.float64)) / np.where(b > 0, b, 1.0)[:, None]
+    mid = (_E2M1_MAG[:-1] + _E2M1_MAG[1:]) / 2
+    mag = np.searchsorted(mid, x, side="left")
+    mag[np.broadcast_to((b == 0)[:, None], mag.shape)] = 0
+    code = (mag | np.where(blk < 0, 8, 0)).astype(np.uint8).reshape(-1)
+    packed = (code[0::2] | (code[1::2] << 4)).astype(np.uint8)
+    return {"fmt": "nvfp4", "N": N, "K": K, "data": packed, "block_scale": sc.reshape(-1),
+            "tensor_scale": np.array([ts], dtype=np.float32)}
+
+
 def pack(w_f32: np.ndarray, fmt: str, double_quant: bool = False) -> Dict[str, np.ndarray]:
     if fmt == "bf16":
         N, K = w_f32.shape
@@ -198,12 +342,20 @@ def pack(w_f32: np.ndarray, fmt: str, double_quant: bool = False) -> Dict[str, n
         return pack_q8_0(w_f32)
     if fmt == "q4_0":
         return pack_q4_0(w_f32)
+    if fmt == "q4_k":
+        return pack_q4_k(w_f32)
+    if fmt == "fp8_e4m3":
+        return pack_fp8_e4m3(w_f32)
+    if fmt == "nvfp4":
+        return pack_nvfp4(w_f32)
+    if fmt == "nf4_dqmap":
+        return pack_nf4(w_f32, True, dq_map=True)
     raise ValueError(fmt)
 
 
 def weight_nbytes(qw: Dict) -> int:
     n = qw["data"].nbytes
-    for k in ("absmax", "absmax_q", "absmax_scale"):
+    for k in ("absmax", "absmax_q", "absmax_scale", "absmax_map", "block_scale", "tensor_scale"):
         if k in qw:
             n += qw[k].nbytes
     return n
