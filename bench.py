@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--stream-layers", type=int, default=32,
                    help="layers for the streamed leg (0 = skip); Llama workload only")
     p.add_argument("--no-moe", action="store_true", help="skip the grouped MoE leg")
+    p.add_argument("--only-moe", action="store_true",
+                   help="run the grouped MoE leg alone and print its result (for profiling)")
     p.add_argument("--no-configs", action="store_true",
                    help="skip the layer legs of the other configurations (Qwen3-0.6B bf16, Qwen3-8B Q4_0 / Q8_0)")
     return p.parse_args()
@@ -330,11 +332,21 @@ def moe_leg(q, torch, steps, stream):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    # a second pass with every grouped GEMM launch bracketed by events
+    q.profile_gemm(True)
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    q.profile_gemm(False)
+    gemm_ms, gemm_n, gemm_flops = q.profile_gemm_read()
     flops = sum(syn.linear_flops(rows, l.K, l.N, mw.rank) for l in lins)
     return {"workload": "moe_q8_0: 128 experts, top-8 of 4096 tokens (32768 rows, Zipf-skewed, "
                         f"{int((counts == 0).sum())} experts empty), gate/up 2048->768, down 768->2048, rank 16",
             "ms_per_step": ms, "tokens_per_s": mw.tokens / (ms / 1e3), "rows_per_s": rows / (ms / 1e3),
-            "tflops": flops / (ms / 1e3) / 1e12}
+            "tflops": flops / (ms / 1e3) / 1e12,
+            "gemm": {"ms_per_step": gemm_ms / steps, "launches_per_step": gemm_n / steps,
+                     "tflops": gemm_flops / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None,
+                     "kernel": "qgemm_pair_kernel grouped (256x256 tiles, Q8_0 decode in the producer)"}}
 
 
 def fused_groups(wl):
@@ -466,6 +478,15 @@ def config_of(wl):
 def main():
     args = parse_args()
     wl = syn.WORKLOADS[args.workload]
+    if args.only_moe:
+        import torch
+
+        import quantized_base_lora_block_gb300 as q
+
+        q.load()
+        stream = torch.cuda.Stream()
+        print(json.dumps(moe_leg(q, torch, args.steps, stream)))
+        return
     if args.impl == "reference":
         return run_reference(args, wl)
 

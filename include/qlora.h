@@ -25,12 +25,34 @@
  *             bf16_rn( f32_rn( level[c] * absmax' ) ),
  *             absmax' = absmax or f32_rn( f32(absmax_q) * absmax_scale ).
  *         level[] = the 16 NormalFloat-4 levels (normal quantiles incl. an
- *         exact 0, scaled to [-1, 1]) as fp32.
+ *         exact 0, scaled to [-1, 1]) as fp32.  QLoRA-style double
+ *         quantisation (absmax_map set): the absmax byte indexes a 256-entry
+ *         fp32 map and an offset is added back:
+ *             absmax' = f32_rn( f32_rn( map[(uint8)absmax_q] * absmax_scale )
+ *                               + absmax_offset ).
  *   Q8_0  GGUF: blocks of 32 along K, 34 bytes {fp16 d; int8 q[32]};
  *         value = bf16_rn( q * f32(d) ).
  *   Q4_0  GGUF: blocks of 32 along K, 18 bytes {fp16 d; uint8 qs[16]};
  *         element i < 16 = low nibble of qs[i], element i+16 = high nibble;
  *         value = bf16_rn( (nib - 8) * f32(d) ).
+ *   Q4_K  GGUF K-quant (Surogate README, "Native GGUF" row; quickstart
+ *         "--type q4_k_m"): super-blocks of 256 along K (K % 256 == 0), 144
+ *         bytes {fp16 d; fp16 dmin; 12 bytes: eight 6-bit sub-block scales
+ *         sc[j] and mins m[j]; 128 code bytes}; sub-block j = 32 elements.
+ *         Sub-blocks 0..3: sc = byte j & 63, m = byte j+4 & 63; 4..7:
+ *         sc = (byte j+4 & 15) | (byte j-4 >> 6) << 4,
+ *         m = (byte j+4 >> 4) | (byte j >> 6) << 4.  Code bytes 32c..32c+31
+ *         hold sub-block 2c in their low nibbles and 2c+1 in their high.
+ *         value = bf16_rn( f32_rn( f32(d) sc q - f32(dmin) m ) ).
+ *   FP8_E4M3  (Surogate README, "LoRA & QLoRA" and "Native precision
+ *         recipes" rows; heatdrop.ai summary: E4M3 recipe) one E4M3 code
+ *         per element [N*K] (OCP 8-bit float: bias 7, no infinities,
+ *         S.1111.111 = NaN) and one fp32 tensor_scale;
+ *         value = bf16_rn( f32_rn( e4m3(c) * tensor_scale ) ).
+ *   NVFP4 E2M1 codes, two per byte [N*K/2] (element 2j in the LOW nibble of
+ *         byte j), one E4M3 block_scale per 16 consecutive K-elements
+ *         [N*K/16] and one fp32 tensor_scale;
+ *         value = bf16_rn( f32_rn( e2m1(c) * f32_rn( e4m3(s) * tensor_scale ) ) ).
  *
  * Conventions for every call:
  *   - All tensor pointers are DEVICE pointers unless stated otherwise, owned
@@ -65,7 +87,10 @@ typedef enum {
   QLORA_FMT_BF16 = 0,
   QLORA_FMT_NF4 = 1,
   QLORA_FMT_Q8_0 = 2,
-  QLORA_FMT_Q4_0 = 3
+  QLORA_FMT_Q4_0 = 3,
+  QLORA_FMT_Q4_K = 4,     /* GGUF K-quant, super-blocks of 256 */
+  QLORA_FMT_FP8_E4M3 = 5, /* OCP E4M3 codes with one fp32 tensor scale */
+  QLORA_FMT_NVFP4 = 6     /* E2M1 codes, E4M3 scale per 16, fp32 tensor scale */
 } qlora_format;
 
 typedef enum {
@@ -79,8 +104,8 @@ typedef enum {
   QLORA_ERR_STATE = -7        /* streaming pool used out of order */
 } qlora_status;
 
-/* Frozen base weight W [N x K] in one of the four formats.  Every pointer is
- * a read-only device pointer; unused ones must be NULL. */
+/* Frozen base weight W [N x K] in one of the formats above.  Every pointer
+ * is a read-only device pointer; unused ones must be NULL. */
 typedef struct {
   int32_t fmt;                /* qlora_format */
   int32_t dq_group;           /* NF4 double quantisation group (256), else 0 */
@@ -88,11 +113,19 @@ typedef struct {
   int64_t K;                  /* input features (columns of W) */
   const void* data;           /* BF16: bf16[N*K]; NF4: uint8[N*K/2];
                                  Q8_0: 34-byte blocks [N*K/32];
-                                 Q4_0: 18-byte blocks [N*K/32] */
+                                 Q4_0: 18-byte blocks [N*K/32];
+                                 Q4_K: 144-byte super-blocks [N*K/256];
+                                 FP8_E4M3: uint8[N*K]; NVFP4: uint8[N*K/2] */
   const float* absmax;        /* NF4 without double quantisation: fp32[N*K/64] */
   const int8_t* absmax_q;     /* NF4 with double quantisation: int8[N*K/64] */
   const float* absmax_scale;  /* NF4 with double quantisation:
                                  fp32[ceil(N*K/64 / dq_group)] */
+  const float* absmax_map;    /* NF4 with double quantisation through an 8-bit
+                                 map: fp32[256]; NULL = plain int8 codes */
+  const float* tensor_scale;  /* FP8_E4M3, NVFP4: fp32[1] */
+  const uint8_t* block_scale; /* NVFP4: E4M3 codes [N*K/16], 16-byte aligned */
+  float absmax_offset;        /* NF4 with absmax_map: added to every absmax */
+  int32_t reserved;           /* must be 0 */
 } qlora_weight_desc;
 
 /* Human-readable name of a status code (static string, never NULL). */

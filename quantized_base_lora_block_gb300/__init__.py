@@ -20,7 +20,7 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libqlora.so")
 
-FMT = {"bf16": 0, "nf4": 1, "q8_0": 2, "q4_0": 3}
+FMT = {"bf16": 0, "nf4": 1, "q8_0": 2, "q4_0": 3, "q4_k": 4, "fp8_e4m3": 5, "nvfp4": 6}
 
 STATUS = {
     0: "ok", -1: "invalid argument", -2: "unsupported", -3: "pointer not 16-byte aligned",
@@ -53,6 +53,11 @@ class WeightDesc(ctypes.Structure):
         ("absmax", ctypes.c_void_p),
         ("absmax_q", ctypes.c_void_p),
         ("absmax_scale", ctypes.c_void_p),
+        ("absmax_map", ctypes.c_void_p),
+        ("tensor_scale", ctypes.c_void_p),
+        ("block_scale", ctypes.c_void_p),
+        ("absmax_offset", ctypes.c_float),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -159,24 +164,38 @@ class DeviceWeight:
     """A frozen base weight resident on the GPU plus its C descriptor."""
 
     def __init__(self, fmt: str, N: int, K: int, data, absmax=None, absmax_q=None, absmax_scale=None,
-                 dq_group: int = 0):
+                 dq_group: int = 0, absmax_map=None, absmax_offset: float = 0.0, tensor_scale=None,
+                 block_scale=None):
         self.fmt, self.N, self.K = fmt, int(N), int(K)
         self.data, self.absmax, self.absmax_q, self.absmax_scale = data, absmax, absmax_q, absmax_scale
+        self.absmax_map, self.tensor_scale, self.block_scale = absmax_map, tensor_scale, block_scale
         self.desc = WeightDesc(FMT[fmt], int(dq_group), self.N, self.K, _ptr(data), _ptr(absmax), _ptr(absmax_q),
-                               _ptr(absmax_scale))
+                               _ptr(absmax_scale), _ptr(absmax_map), _ptr(tensor_scale), _ptr(block_scale),
+                               float(absmax_offset), 0)
 
     @classmethod
     def from_packed(cls, p: Dict, device="cuda") -> "DeviceWeight":
         torch = _torch()
+
+        def f32(key):
+            return torch.from_numpy(np.ascontiguousarray(p[key], np.float32).reshape(-1)).to(device)
+
         data = _bytes_to_device(p["data"], device)
-        absmax = absmax_q = absmax_scale = None
+        kw = {}
         if p["fmt"] == "nf4":
             if "absmax" in p:
-                absmax = torch.from_numpy(np.ascontiguousarray(p["absmax"], np.float32)).to(device)
+                kw["absmax"] = f32("absmax")
             else:
-                absmax_q = torch.from_numpy(np.ascontiguousarray(p["absmax_q"], np.int8)).to(device)
-                absmax_scale = torch.from_numpy(np.ascontiguousarray(p["absmax_scale"], np.float32)).to(device)
-        return cls(p["fmt"], p["N"], p["K"], data, absmax, absmax_q, absmax_scale, p.get("dq_group", 0))
+                kw["absmax_q"] = torch.from_numpy(np.ascontiguousarray(p["absmax_q"]).view(np.int8)).to(device)
+                kw["absmax_scale"] = f32("absmax_scale")
+                if p.get("absmax_map") is not None:
+                    kw["absmax_map"] = f32("absmax_map")
+                    kw["absmax_offset"] = float(p["absmax_offset"])
+        if p["fmt"] in ("fp8_e4m3", "nvfp4"):
+            kw["tensor_scale"] = f32("tensor_scale")
+        if p["fmt"] == "nvfp4":
+            kw["block_scale"] = _bytes_to_device(p["block_scale"], device)
+        return cls(p["fmt"], p["N"], p["K"], data, dq_group=p.get("dq_group", 0), **kw)
 
     @classmethod
     def from_pointers(cls, fmt: str, N: int, K: int, data: int, absmax: int = 0, absmax_q: int = 0,
@@ -186,13 +205,15 @@ class DeviceWeight:
         self.fmt, self.N, self.K = fmt, int(N), int(K)
         self.data = self.absmax = self.absmax_q = self.absmax_scale = None
         self._keepalive = keepalive
+        self.absmax_map = self.tensor_scale = self.block_scale = None
         self.desc = WeightDesc(FMT[fmt], int(dq_group), self.N, self.K, data or None, absmax or None,
-                               absmax_q or None, absmax_scale or None)
+                               absmax_q or None, absmax_scale or None, None, None, None, 0.0, 0)
         return self
 
     def nbytes(self) -> int:
         n = 0
-        for t in (self.data, self.absmax, self.absmax_q, self.absmax_scale):
+        for t in (self.data, self.absmax, self.absmax_q, self.absmax_scale, self.absmax_map, self.tensor_scale,
+                  self.block_scale):
             if t is not None:
                 n += t.numel() * t.element_size()
         return n

@@ -38,6 +38,7 @@ int* device_error_word() {
 
 // ---------------------------------------------------------------- helpers ---
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 static int sm_count() {
   static int cached[64] = {0};
@@ -118,16 +119,35 @@ static int validate_weight(const qlora_weight_desc* w) {
   if (w->N > (1ll << 30) || w->K > (1ll << 30)) return QLORA_ERR_UNSUPPORTED;
   if (!w->data) return QLORA_ERR_INVALID;
   if (!aligned16(w->data)) return QLORA_ERR_ALIGN;
+  if (w->reserved != 0) return QLORA_ERR_INVALID;
+  if (w->fmt != QLORA_FMT_NF4 && (w->absmax || w->absmax_q || w->absmax_scale || w->absmax_map))
+    return QLORA_ERR_INVALID;
+  if (w->fmt != QLORA_FMT_FP8_E4M3 && w->fmt != QLORA_FMT_NVFP4 && w->tensor_scale) return QLORA_ERR_INVALID;
+  if (w->fmt != QLORA_FMT_NVFP4 && w->block_scale) return QLORA_ERR_INVALID;
   switch (w->fmt) {
     case QLORA_FMT_BF16:
     case QLORA_FMT_Q8_0:
     case QLORA_FMT_Q4_0:
       break;
+    case QLORA_FMT_Q4_K:
+      if (w->K % 256) return QLORA_ERR_INVALID;
+      break;
+    case QLORA_FMT_FP8_E4M3:
+      if (!w->tensor_scale) return QLORA_ERR_INVALID;
+      if (!aligned4(w->tensor_scale)) return QLORA_ERR_ALIGN;
+      break;
+    case QLORA_FMT_NVFP4:
+      if (!w->tensor_scale || !w->block_scale) return QLORA_ERR_INVALID;
+      if (!aligned4(w->tensor_scale) || !aligned16(w->block_scale)) return QLORA_ERR_ALIGN;
+      break;
     case QLORA_FMT_NF4:
       if (w->absmax) {
         if (!aligned16(w->absmax)) return QLORA_ERR_ALIGN;
+        if (w->absmax_q || w->absmax_scale || w->absmax_map) return QLORA_ERR_INVALID;
       } else {
         if (!w->absmax_q || !w->absmax_scale || w->dq_group <= 0) return QLORA_ERR_INVALID;
+        if (w->absmax_map && !aligned4(w->absmax_map)) return QLORA_ERR_ALIGN;
+        if (w->absmax_map && !std::isfinite(w->absmax_offset)) return QLORA_ERR_INVALID;
       }
       break;
     default:
@@ -147,6 +167,10 @@ static WeightView view_of(const qlora_weight_desc* w) {
   v.absmax = w->absmax;
   v.absmax_q = w->absmax_q;
   v.absmax_scale = w->absmax_scale;
+  v.amap = w->fmt == QLORA_FMT_NF4 && !w->absmax ? w->absmax_map : nullptr;
+  v.aoff = w->absmax_offset;
+  v.tscale = w->tensor_scale;
+  v.bscale = w->block_scale;
   v.dq_group = w->dq_group > 0 ? w->dq_group : 1;
   v.aq_align8 = (reinterpret_cast<uintptr_t>(w->absmax_q) & 7u) == 0 ? 1 : 0;
   v.dq_shift = -1;
@@ -511,7 +535,7 @@ const char* qlora_status_string(int32_t s) {
   }
 }
 
-int32_t qlora_version(void) { return 100; }
+int32_t qlora_version(void) { return 200; }
 
 int64_t qlora_launch_count(void) { return g_launches.load(); }
 

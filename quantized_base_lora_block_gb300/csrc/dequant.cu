@@ -17,7 +17,7 @@ __global__ void __launch_bounds__(256) dequant_kernel(const WeightView wv, int64
     RawLine r;
     load_line<FMT>(wv, ln, r);
     uint4 o[8];
-    decode_line<FMT>(r, o);
+    decode_line<FMT>(r, wv, o);
     uint4* dst = out + ln * 8;
 #pragma unroll
     for (int c = 0; c < 8; ++c) dst[c] = o[c];
@@ -38,6 +38,9 @@ cudaError_t launch_dequant(int fmt, const WeightView& wv, int64_t lines, __nv_bf
     case FMT_NF4: dequant_kernel<FMT_NF4><<<(unsigned)blocks, 256, 0, st>>>(wv, lines, o); break;
     case FMT_Q8_0: dequant_kernel<FMT_Q8_0><<<(unsigned)blocks, 256, 0, st>>>(wv, lines, o); break;
     case FMT_Q4_0: dequant_kernel<FMT_Q4_0><<<(unsigned)blocks, 256, 0, st>>>(wv, lines, o); break;
+    case FMT_Q4_K: dequant_kernel<FMT_Q4_K><<<(unsigned)blocks, 256, 0, st>>>(wv, lines, o); break;
+    case FMT_FP8: dequant_kernel<FMT_FP8><<<(unsigned)blocks, 256, 0, st>>>(wv, lines, o); break;
+    case FMT_NVFP4: dequant_kernel<FMT_NVFP4><<<(unsigned)blocks, 256, 0, st>>>(wv, lines, o); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

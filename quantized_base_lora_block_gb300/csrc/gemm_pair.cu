@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
         if (valid) {
           if (dq_cache) resolve_dq(r);
           uint4 out[8];
-          decode_line<FMT>(r, out);
+          decode_line<FMT>(r, *c.wv, out);
 #pragma unroll
           for (int q = 0; q < 8; ++q) sts_v4(dst + ((q ^ swz) << 4), out[q]);
         } else {
@@ -805,6 +805,15 @@ static cudaError_t launch_quant(int fmt, bool dx, const GemmMaps& maps, const Ge
     case FMT_Q4_0:
       return dx ? launch_pair_one<FMT_Q4_0, true, CFG, G>(maps, args, tab, st)
                 : launch_pair_one<FMT_Q4_0, false, CFG, G>(maps, args, tab, st);
+    case FMT_Q4_K:
+      return dx ? launch_pair_one<FMT_Q4_K, true, CFG, G>(maps, args, tab, st)
+                : launch_pair_one<FMT_Q4_K, false, CFG, G>(maps, args, tab, st);
+    case FMT_FP8:
+      return dx ? launch_pair_one<FMT_FP8, true, CFG, G>(maps, args, tab, st)
+                : launch_pair_one<FMT_FP8, false, CFG, G>(maps, args, tab, st);
+    case FMT_NVFP4:
+      return dx ? launch_pair_one<FMT_NVFP4, true, CFG, G>(maps, args, tab, st)
+                : launch_pair_one<FMT_NVFP4, false, CFG, G>(maps, args, tab, st);
     default: return cudaErrorInvalidValue;
   }
 }

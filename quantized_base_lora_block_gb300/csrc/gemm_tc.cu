@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(num_threads<FMT>(), 1)
         const uint32_t dst = sB0 + s * B_BYTES + soff;
         if (cur_valid) {
           uint4 out[8];
-          decode_line<FMT>(cur, out);
+          decode_line<FMT>(cur, args.wv, out);
 #pragma unroll
           for (int c = 0; c < 8; ++c) sts_v4(dst + ((c ^ swz) << 4), out[c]);
         } else {
@@ -345,6 +345,9 @@ cudaError_t launch_qgemm(int fmt, bool dx, const GemmMaps& maps, const GemmArgs&
     case FMT_NF4: return launch_fmt<FMT_NF4>(dx, maps, args, num_sms, st);
     case FMT_Q8_0: return launch_fmt<FMT_Q8_0>(dx, maps, args, num_sms, st);
     case FMT_Q4_0: return launch_fmt<FMT_Q4_0>(dx, maps, args, num_sms, st);
+    case FMT_Q4_K: return launch_fmt<FMT_Q4_K>(dx, maps, args, num_sms, st);
+    case FMT_FP8: return launch_fmt<FMT_FP8>(dx, maps, args, num_sms, st);
+    case FMT_NVFP4: return launch_fmt<FMT_NVFP4>(dx, maps, args, num_sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -356,6 +356,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Two E4M3 codes (low byte: first) to two fp16 values (low half: first);
+// every E4M3 value, NaN included, is exact in fp16.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}" : "=r"(r) : "r"(two_codes));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings(lib):
     for s in range(-7, 1):
         assert lib.qlora_status_string(s).decode() == q.STATUS[s]
-    assert lib.qlora_version() == 100
+    assert lib.qlora_version() == 200
 
 
 def _desc(fmt="nf4", N=256, K=256, data=0x1000, absmax=0x2000):
@@ -77,6 +77,44 @@ def test_validation_rejects_before_any_launch(lib):
     # backward needs dA and dB
     b = lib.qlora_linear_bwd
     assert b(ctypes.byref(d), 64, 8, 16.0, *bufs[:5], bufs[5], None, None, bufs[6], ws, None) == -1
+
+
+def test_descriptor_fields_of_each_format_checked(lib):
+    """Per-format descriptor fields: required ones present and aligned,
+    fields of other formats NULL, reserved zero (all checked before any
+    launch; the pointers here are never dereferenced)."""
+    bufs = [0x10000 * (i + 1) for i in range(8)]
+    f = lib.qlora_linear_fwd
+
+    def call(d):
+        return f(ctypes.byref(d), 64, 8, 16.0, *bufs[:5], bufs[5], 1 << 30, None)
+
+    def desc(fmt, K=256, **kw):
+        d = q.WeightDesc(q.FMT[fmt], kw.pop("dq_group", 0), 256, K, 0x1000)
+        for k, v in kw.items():
+            setattr(d, k, v)
+        return d
+
+    # FP8 / NVFP4 need their scales
+    assert call(desc("fp8_e4m3")) == -1
+    assert call(desc("nvfp4", tensor_scale=0x3000)) == -1
+    assert call(desc("fp8_e4m3", tensor_scale=0x3002)) == -3
+    assert call(desc("nvfp4", tensor_scale=0x3000, block_scale=0x4008)) == -3
+    # scales of another format
+    assert call(desc("q8_0", tensor_scale=0x3000)) == -1
+    assert call(desc("fp8_e4m3", tensor_scale=0x3000, block_scale=0x4000)) == -1
+    assert call(desc("q4_0", absmax=0x2000)) == -1
+    # Q4_K super-blocks need K % 256 == 0
+    assert call(desc("q4_k", K=192)) == -1
+    # the map variant of NF4 needs a finite offset; reserved must stay 0
+    nan_off = desc("nf4", absmax_q=0x2000, absmax_scale=0x3000, absmax_map=0x4000, dq_group=256,
+                   absmax_offset=float("nan"))
+    assert call(nan_off) == -1
+    assert call(desc("q8_0", reserved=1)) == -1
+    # workspace queries agree (0 on an invalid descriptor)
+    assert lib.qlora_workspace_bytes(ctypes.byref(desc("q4_k", K=192)), 64, 8) == 0
+    assert lib.qlora_workspace_bytes(ctypes.byref(desc("nvfp4", tensor_scale=0x3000, block_scale=0x4000)),
+                                     64, 8) > 0
 
 
 def test_workspace_size_is_deterministic(lib):

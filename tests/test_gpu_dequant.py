@@ -22,7 +22,7 @@ def _assert_bits_equal(got, want, name):
     # compare by value so that -0 == +0 (bf16 bits 0x8000 vs 0x0000)
     gv = oracle.bf16_bits_to_f64(got)
     wv = oracle.bf16_bits_to_f64(want)
-    bad = gv != wv
+    bad = (gv != wv) & ~(np.isnan(gv) & np.isnan(wv))  # NaN codes decode to some NaN
     assert not bad.any(), f"{name}: {int(bad.sum())} mismatches, first at {np.argwhere(bad)[0]}"
 
 
@@ -78,8 +78,65 @@ def test_q8_0_every_code_bit_exact(lib):
     _assert_bits_equal(_gpu_dequant(lib, p), oracle.dequant_bf16_bits(p), "q8_0")
 
 
+def test_fp8_every_code_bit_exact(lib):
+    """All 256 E4M3 codes (NaN included) under several tensor scales, one
+    per launch: a normal, a power of two, a large and a tiny one."""
+    rng = np.random.default_rng(5)
+    N, K = 64, 512
+    codes = np.tile(np.arange(256, dtype=np.uint8), N * K // 256)
+    rng.shuffle(codes)
+    for ts in (0.0173, 0.25, 3.0e4, 1.0e-30):
+        p = {"fmt": "fp8_e4m3", "N": N, "K": K, "data": codes, "tensor_scale": np.array([ts], np.float32)}
+        _assert_bits_equal(_gpu_dequant(lib, p), oracle.dequant_bf16_bits(p), f"fp8 scale {ts}")
+
+
+def test_nvfp4_every_code_bit_exact(lib):
+    """All 16 E2M1 codes in every block, block scales over every finite E4M3
+    code of either sign (subnormals and zero included)."""
+    rng = np.random.default_rng(6)
+    N, K = 128, 512
+    nblk = N * K // 16
+    codes = np.tile(np.arange(16, dtype=np.uint8), N * K // 16)
+    for b in range(nblk):
+        rng.shuffle(codes[16 * b:16 * (b + 1)])
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    bsc = np.resize(finite, nblk)
+    rng.shuffle(bsc)
+    for ts in (1.0, 0.0123, 2.0 ** -100):
+        p = {"fmt": "nvfp4", "N": N, "K": K, "data": (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8),
+             "block_scale": bsc, "tensor_scale": np.array([ts], np.float32)}
+        _assert_bits_equal(_gpu_dequant(lib, p), oracle.dequant_bf16_bits(p), f"nvfp4 scale {ts}")
+
+
+def test_q4_k_random_bytes_bit_exact(lib):
+    """Super-blocks of random bytes (every scale/min bit pattern and code)
+    with finite fp16 d and dmin of either sign, zero and subnormal ones."""
+    rng = np.random.default_rng(7)
+    N, K = 64, 1024
+    nsb = N * K // 256
+    rec = rng.integers(0, 256, (nsb, 144), dtype=np.uint8)
+    d = (rng.standard_normal((nsb, 2)) * 0.01).astype(np.float16)
+    d[:4] = [[0.0, 0.0], [-0.0, 1.0], [6.0e-8, -3.0e-5], [65000.0, -0.5]]
+    rec[:, 0:4] = d.view(np.uint8).reshape(nsb, 4)
+    p = {"fmt": "q4_k", "N": N, "K": K, "data": rec.reshape(-1)}
+    _assert_bits_equal(_gpu_dequant(lib, p), oracle.dequant_bf16_bits(p), "q4_k")
+
+
+def test_nf4_absmax_map_bit_exact(lib):
+    """NF4 with an 8-bit absmax map and offset: every absmax byte, every
+    NF4 code."""
+    rng = np.random.default_rng(8)
+    p = _nf4_all_codes(N=128, K=512, dq=True)
+    nb = 128 * 512 // 64
+    p["absmax_q"] = np.resize(np.arange(256, dtype=np.uint8), nb).view(np.int8)
+    p["absmax_map"] = (rng.standard_normal(256) * 0.5).astype(np.float32)
+    p["absmax_offset"] = 0.0371
+    _assert_bits_equal(_gpu_dequant(lib, p), oracle.dequant_bf16_bits(p), "nf4 map")
+
+
 @pytest.mark.parametrize("fmt,dq", [("nf4", False), ("nf4", True), ("q4_0", False), ("q8_0", False),
-                                    ("bf16", False)])
+                                    ("bf16", False), ("q4_k", False), ("fp8_e4m3", False), ("nvfp4", False),
+                                    ("nf4_dqmap", False)])
 def test_packed_normal_weights_bit_exact(lib, fmt, dq):
     rng = np.random.default_rng(3)
     w = (rng.standard_normal((192, 1024)) * 0.02).astype(np.float32)
@@ -90,7 +147,8 @@ def test_packed_normal_weights_bit_exact(lib, fmt, dq):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("fmt,dq,N,K", [("nf4", True, 14336, 4096), ("q4_0", False, 12288, 4096),
-                                        ("q8_0", False, 4096, 12288)])
+                                        ("q8_0", False, 4096, 12288), ("q4_k", False, 12288, 4096),
+                                        ("fp8_e4m3", False, 14336, 4096), ("nvfp4", False, 4096, 14336)])
 def test_full_size_layer_weight_bit_exact(lib, fmt, dq, N, K):
     """A full gate/down projection of the 8B-class layers."""
     rng = np.random.default_rng(4)

@@ -46,11 +46,24 @@ SHAPES = [
 
 
 @pytest.mark.parametrize("fmt,dq", [("bf16", False), ("nf4", False), ("nf4", True), ("q8_0", False),
-                                    ("q4_0", False)])
+                                    ("q4_0", False), ("fp8_e4m3", False), ("nvfp4", False),
+                                    ("nf4_dqmap", False)])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_formats_and_shapes(lib, fmt, dq, shape):
     M, K, N, r = shape
     inp = make(M, K, N, r, fmt, dq, seed=M + K + N + r)
+    check_all(inp, run_layer(inp), oracle_layer(inp))
+
+
+# Q4_K needs K % 256 == 0
+Q4_K_SHAPES = [(64, 256, 256, 8), (200, 512, 320, 16), (1, 256, 64, 32), (300, 1024, 768, 64),
+               (130, 768, 448, 24), (600, 512, 1280, 16)]
+
+
+@pytest.mark.parametrize("shape", Q4_K_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_q4_k_shapes(lib, shape):
+    M, K, N, r = shape
+    inp = make(M, K, N, r, "q4_k", False, seed=M + K + N + r)
     check_all(inp, run_layer(inp), oracle_layer(inp))
 
 

@@ -23,7 +23,7 @@ def _moe_inputs(counts, K, N, r, fmt, seed=0, alpha=None):
     A = syn.normal_bf16(rng(syn.S_A), (E, r, K), 1.0 / np.sqrt(K))
     B = syn.normal_bf16(rng(syn.S_B), (E, N, r), 0.01)
     W = [syn.pack(syn.normal_f32(syn.rng_for(seed, 78 + e, 0, syn.S_W), (N, K), 0.02), fmt,
-                  double_quant=(fmt == "nf4")) for e in range(E)]
+                  double_quant=(fmt in ("nf4", "nf4_dqmap"))) for e in range(E)]
     return {"X": X, "dY": dY, "A": A, "B": B, "W": W, "off": off, "alpha": float(alpha or 2 * r), "r": r}
 
 
@@ -66,7 +66,7 @@ def _check(d, got, ref):
             check_f32(got["dB"][e], ref["dB"][e], f"dB[{e}]")
 
 
-@pytest.mark.parametrize("fmt", ["q8_0", "nf4", "q4_0", "bf16"])
+@pytest.mark.parametrize("fmt", ["q8_0", "nf4", "q4_0", "bf16", "q4_k", "fp8_e4m3", "nvfp4", "nf4_dqmap"])
 def test_grouped_mixed_counts(lib, fmt):
     d = _moe_inputs([0, 5, 130, 1, 0, 260, 64], K=256, N=320, r=16, fmt=fmt, seed=3)
     _check(d, _run(lib, d), _oracle(d))
