@@ -306,7 +306,7 @@ def moe_leg(q, torch, steps, stream):
     off_dev = q.device_offsets(off)  # the router's offsets stay on the device
     dev = []
     for d in data:
-        ws = [q.DeviceWeight.from_packed(w) for w in d["W"]]
+        ws = q.upload_experts(d["W"])  # expert bases back to back (one tensor map)
         X, dY = q.bf16_from_bits(d["X"]), q.bf16_from_bits(d["dY"])
         A, B = q.bf16_from_bits(d["A"]), q.bf16_from_bits(d["B"])
         nb = q.grouped_workspace_bytes(ws, rows, mw.rank)

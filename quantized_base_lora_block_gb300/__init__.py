@@ -367,9 +367,16 @@ def stack_weights(packed: Sequence[Dict]) -> Dict:
     K = packed[0]["K"]
     out = {"fmt": fmt, "N": sum(p["N"] for p in packed), "K": K,
            "data": np.concatenate([np.asarray(p["data"]).reshape(-1) for p in packed])}
-    for k in ("absmax", "absmax_q", "absmax_scale"):
+    for k in ("absmax", "absmax_q", "absmax_scale", "block_scale"):
         if k in packed[0]:
             out[k] = np.concatenate([np.asarray(p[k]).reshape(-1) for p in packed])
+    # per-tensor constants must agree to describe the stack with one set
+    for k in ("absmax_map", "absmax_offset", "tensor_scale"):
+        if packed[0].get(k) is not None:
+            v = np.asarray(packed[0][k])
+            if not all(np.array_equal(np.asarray(p[k]), v) for p in packed):
+                raise ValueError(f"stacked weights need the same {k}")
+            out[k] = packed[0][k]
     if "dq_group" in packed[0]:
         g = packed[0]["dq_group"]
         assert all((p["N"] * K // 64) % g == 0 for p in packed), "a quantisation group spans two projections"
@@ -499,17 +506,21 @@ def grouped_bwd(weights: Sequence[DeviceWeight], offsets, X, A, B, T, dY, alpha:
     return dX, dA, dB
 
 
-def stack_bf16_weights(weights: Sequence[Dict], device="cuda") -> List[DeviceWeight]:
-    """bf16 expert bases must live in one [E][N][K] array (grouped calls read
-    them through one 3-D tensor map); returns per-expert views of it."""
-    torch = _torch()
-    E = len(weights)
-    N, K = weights[0]["N"], weights[0]["K"]
-    big = torch.from_numpy(np.stack([np.asarray(w["data"], np.uint16).reshape(N, K) for w in weights])
-                           .view(np.int16)).to(device)
+def upload_experts(weights: Sequence[Dict], device="cuda") -> List[DeviceWeight]:
+    """Expert bases with their bytes back to back in one device array
+    [E][N][row bytes] (grouped calls read such a stack through one 3-D tensor
+    map: required for bf16 bases, the fast path for quantised ones); each
+    expert's other arrays (absmax, scales) are uploaded on their own.
+    Returns per-expert descriptors over views of the stack."""
+    big = _bytes_to_device(np.concatenate([np.ascontiguousarray(w["data"]).view(np.uint8).reshape(-1)
+                                           for w in weights]), device)
+    per = big.numel() // len(weights)
     out = []
-    for e in range(E):
-        out.append(DeviceWeight("bf16", N, K, big[e]))
+    for e, w in enumerate(weights):
+        one = DeviceWeight.from_packed(dict(w, data=np.zeros(16, np.uint8)), device)
+        one.data = big[e * per:(e + 1) * per]
+        one.desc.data = one.data.data_ptr()
+        out.append(one)
     out[0]._stack = big
     return out
 

@@ -356,6 +356,7 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
   a.wv = view_of(w);
   a.err = device_error_word();
   a.raw_dq = raw_dq;
+  a.raw_on = (pair == 3 && w->fmt == QLORA_FMT_NF4) ? 1 : 0;
   // Tile order.  Forward: row blocks fastest while the activation fits in L2
   // next to the streamed weight slabs (measured: gate 133 MB of DRAM traffic
   // this way vs 234 MB the other way); beyond ~64 MB (e.g. the 14336-wide
@@ -450,13 +451,28 @@ static bool map3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t mid
   return make_map(m, base, 3, dims, strides, box);
 }
 
-// bf16 expert bases must be one array [E][N][K] for the 3-D map
+// Expert bases back to back in one array [E][N][row bytes] (read through
+// one 3-D map: required for bf16, the fast path for quantised bases)
 static bool experts_stacked(const qlora_weight_desc* ex, int E) {
   const uint8_t* b0 = static_cast<const uint8_t*>(ex[0].data);
-  const size_t stride = (size_t)ex[0].N * ex[0].K * 2;
+  const size_t stride = (size_t)ex[0].N * (size_t)row_bytes_of(ex[0].fmt, ex[0].K);
   for (int e = 1; e < E; ++e)
     if (static_cast<const uint8_t*>(ex[e].data) != b0 + (size_t)e * stride) return false;
   return true;
+}
+
+// Byte tensor [E][N][row_bytes] (row_bytes a multiple of 16), box
+// {box_bytes, box_rows, 1}, no swizzle
+static bool map3d_u8(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t E,
+                     uint32_t box_bytes, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[3] = {row_bytes, rows, E}, s[2] = {row_bytes, row_bytes * rows};
+  cuuint32_t b[3] = {box_bytes, box_rows, 1}, e[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), d, s, b, e,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 // Grouped fused GEMM over the schedule's tile list: forward Y = X deq(W_e)^T
@@ -479,6 +495,16 @@ static cudaError_t run_grouped_gemm(const qlora_weight_desc* ex, const GroupedLa
     if (ex[0].fmt == QLORA_FMT_BF16) ok = ok && map3d(&maps.w, ex[0].data, K, N, E, 64);
   }
   ok = ok && map2d(&maps.out, out, dx ? K : N, M, 64, 128);
+  // quantised bases back to back with 16-byte multiple rows: their bytes
+  // through the raw ring (one 3-D byte box per item; Q4_K headers as a second)
+  const int fmt = ex[0].fmt;
+  const int64_t rb = row_bytes_of(fmt, K);
+  int raw_on = 0;
+  if (ok && fmt != QLORA_FMT_BF16 && rb % 16 == 0 && experts_stacked(ex, E)) {
+    const uint32_t rows = dx ? 64 : 128;
+    raw_on = map3d_u8(&maps.w, ex[0].data, rb, N, E, raw_box_bytes(fmt, dx), rows) ? 1 : 0;
+    if (raw_on && fmt == QLORA_FMT_Q4_K) raw_on = map3d_u8(&maps.aq, ex[0].data, rb, N, E, 16, rows) ? 1 : 0;
+  }
   if (!ok) return cudaErrorInvalidValue;
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -493,6 +519,7 @@ static cudaError_t run_grouped_gemm(const qlora_weight_desc* ex, const GroupedLa
   a.out = static_cast<__nv_bfloat16*>(out);
   a.tile_sched = dx ? g.gemm_d : g.gemm_f;
   a.tile_count = g.counts + (dx ? 1 : 0);
+  a.raw_on = raw_on;
   a.wv = view_of(&ex[0]);
   a.err = device_error_word();
   static thread_local GroupTable tab;  // 12 KB: kept off the stack

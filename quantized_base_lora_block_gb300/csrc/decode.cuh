@@ -446,6 +446,23 @@ __device__ __forceinline__ void load_nf4_scale(const WeightView& v, int64_t line
   }
 }
 
+// The fields of a line that do not come with its code bytes (the code bytes
+// arrive through a shared-memory ring): NF4 absmax, FP8 / NVFP4 tensor scale,
+// NVFP4 block scales, Q4_K chunk index.
+template <int FMT>
+__device__ __forceinline__ void load_line_side(const WeightView& v, int64_t line, RawLine& r) {
+  if constexpr (FMT == FMT_NF4) {
+    load_nf4_scale(v, line, r);
+  } else if constexpr (FMT == FMT_FP8) {
+    r.scale = __ldg(v.tscale);
+  } else if constexpr (FMT == FMT_NVFP4) {
+    r.w[8] = ldg_nc_u32(v.bscale + line * 4);
+    r.scale = __ldg(v.tscale);
+  } else if constexpr (FMT == FMT_Q4_K) {
+    r.q = (int32_t)(line & 3);
+  }
+}
+
 // Only for the quantised formats.
 template <int FMT>
 __device__ __forceinline__ void decode_line(const RawLine& r, const WeightView& v, uint4 (&out)[8]) {

@@ -45,7 +45,8 @@ constexpr int P_TMEM_COLS = 512;
 //      soon as the epilogue holds its values, so the next tile's MMAs into
 //      it can start while the previous tile is still being stored;
 //   4: 256 x 256 with a quantised base, two TMEM buffers (grouped calls,
-//      whose experts own ~256 rows each).
+//      whose experts own ~256 rows each); four stages, leaving room for the
+//      raw ring.
 // Decoding one B tile for two accumulators halves the decode work per flop.
 template <int CFG>
 struct PairCfg {
@@ -56,7 +57,7 @@ struct PairCfg {
   static constexpr int HALF_N = TN / 2;                   // B rows (or columns) per CTA
   static constexpr int A_BYTES = NACC * 128 * kBK * 2;    // this CTA's A rows
   static constexpr int B_BYTES = HALF_N * kBK * 2;        // this CTA's half of B
-  static constexpr int STAGES = (CFG == 1 || CFG == 4) ? 6 : (CFG == 2 ? 5 : 4);
+  static constexpr int STAGES = CFG == 1 ? 6 : (CFG == 2 ? 5 : 4);
   static constexpr int LINES = HALF_N;                    // decoded 64-wide lines per stage per CTA
   static constexpr int GROUP_WARPS = LINES / 32;          // one line per thread of a group
   static constexpr int GROUPS = CFG == 1 ? 3 : (CFG == 2 ? 5 : 2);  // groups rotate over stages
@@ -65,25 +66,37 @@ struct PairCfg {
   static_assert(NBUF * NACC * TN == 512, "accumulators fill TMEM");
 };
 
-// NF4 bases on 512 x 256 tiles take their code bytes through a TMA ring
-// ("raw" ring, filled by a warp of its own) instead of per-thread global
-// loads: each item's codes are one 2-D box (forward: 128 rows x 32 bytes; dX:
-// 64 rows x 64 bytes), and the decode warps read them from shared memory.
-// In dX the slot also holds the item's int8 absmax codes (a 16-byte wide box
-// of the 64 rows, x rounded down to 16 bytes) and the range of group scales
-// its lines use (a 1-D bulk copy), when the host finds the layout allows it
-// (GemmArgs::raw_dq).  The ring's shared memory comes from the second
-// epilogue staging tile.
+// Quantised bytes through a TMA ring ("raw" ring, filled by a warp of its
+// own) instead of per-thread global loads, whose one-row-per-lane pattern
+// touches a separate cache line per lane and load: each item's bytes are one
+// 2-D (grouped: 3-D, expert outermost) byte box per CTA (forward: the CTA's
+// weight rows x one line; dX: 64 weight rows x the CTA's two lines; the box
+// starts at the line's 16-byte aligned address, raw_box_bytes wide), and the
+// decode warps read their lines from shared memory.  Q4_K adds a second box
+// with the 16-byte super-block headers.  Used by NF4 on 512 x 256 tiles and
+// by every quantised format on grouped 256 x 256 tiles, where the host finds
+// the layout allows it (GemmArgs::raw_on: 16-byte multiple row length;
+// grouped: experts back to back in one array).  In NF4 dX on 512 x 256 tiles
+// the slot also holds the item's int8 absmax codes (a 16-byte wide box of
+// the 64 rows, x rounded down to 16 bytes) and the range of group scales its
+// lines use (a 1-D bulk copy), when the host finds the layout allows it
+// (GemmArgs::raw_dq).  On 512 x 256 tiles the ring's shared memory comes from
+// the second epilogue staging tile.
 template <int FMT, int CFG, bool DX>
 struct PairRaw {
-  static constexpr bool ON = FMT == FMT_NF4 && CFG == 3;
-  static constexpr int STAGES = DX ? 3 : 4;
-  static constexpr int CODE_BYTES = 32 * PairCfg<CFG>::HALF_N;  // code bytes of one item for this CTA
-  static constexpr int AQ_OFF = CODE_BYTES;                     // dX: [64 rows x 16] absmax codes
-  static constexpr int SC_OFF = CODE_BYTES + 1024;              // dX: group scales
-  static constexpr int SC_CAP = 64;                             // dX: group scales a slot holds
-  static constexpr int BYTES = !ON ? 0 : (DX ? SC_OFF + 4 * SC_CAP : CODE_BYTES);
-  static constexpr int OUT_BUFS = (CFG == 2 || ON) ? 1 : 2;     // epilogue staging tiles
+  static constexpr bool ON = FMT != FMT_BF16 && ((FMT == FMT_NF4 && CFG == 3) || CFG == 4);
+  static constexpr int STAGES = (CFG == 3 && DX) ? 3 : 4;
+  static constexpr int ROWS = DX ? 64 : PairCfg<CFG>::HALF_N;   // weight rows of one item's box
+  static constexpr int BOX = raw_box_bytes(FMT, DX);           // bytes per row of the box
+  static constexpr int LINE = raw_line_bytes(FMT);              // bytes of one line
+  static constexpr int CODE_BYTES = ROWS * BOX;                 // main box of one item for this CTA
+  static constexpr int HDR_BYTES = FMT == FMT_Q4_K ? ROWS * 16 : 0;  // Q4_K: [ROWS x 16] headers after the box
+  static constexpr int AQ_OFF = CODE_BYTES;                     // NF4 dX: [64 rows x 16] absmax codes
+  static constexpr int SC_OFF = CODE_BYTES + 1024;              // NF4 dX: group scales
+  static constexpr int SC_CAP = 64;                             // NF4 dX: group scales a slot holds
+  static constexpr int RAW_DQ = FMT == FMT_NF4 && CFG == 3 && DX;
+  static constexpr int BYTES = !ON ? 0 : ((RAW_DQ ? SC_OFF + 4 * SC_CAP : CODE_BYTES + HDR_BYTES) + 127) / 128 * 128;
+  static constexpr int OUT_BUFS = (CFG == 2 || (ON && CFG == 3)) ? 1 : 2;  // epilogue staging tiles
 };
 
 template <int CFG>
@@ -110,12 +123,25 @@ constexpr size_t p_smem_bytes() {
   return 1024 + (size_t)PairCfg<CFG>::STAGES * (PairCfg<CFG>::A_BYTES + PairCfg<CFG>::B_BYTES) +
          (size_t)Raw::OUT_BUFS * P_STAGE_OUT_BYTES + (size_t)Raw::STAGES * Raw::BYTES + sizeof(PairBarriers<CFG>);
 }
-static_assert(p_smem_bytes<FMT_NF4, 3, false>() <= 232448 && p_smem_bytes<FMT_NF4, 3, true>() <= 232448 &&
-                  p_smem_bytes<FMT_Q8_0, 3, true>() <= 232448 && p_smem_bytes<FMT_NF4, 2, true>() <= 232448 &&
-                  p_smem_bytes<FMT_BF16, 1, true>() <= 232448 && p_smem_bytes<FMT_Q8_0, 4, true>() <= 232448,
+template <int FMT>
+constexpr bool smem_fits_all() {
+  return p_smem_bytes<FMT, 2, false>() <= 232448 && p_smem_bytes<FMT, 2, true>() <= 232448 &&
+         p_smem_bytes<FMT, 3, false>() <= 232448 && p_smem_bytes<FMT, 3, true>() <= 232448 &&
+         p_smem_bytes<FMT, 4, false>() <= 232448 && p_smem_bytes<FMT, 4, true>() <= 232448;
+}
+static_assert(smem_fits_all<FMT_NF4>() && smem_fits_all<FMT_Q8_0>() && smem_fits_all<FMT_Q4_0>() &&
+                  smem_fits_all<FMT_Q4_K>() && smem_fits_all<FMT_FP8>() && smem_fits_all<FMT_NVFP4>() &&
+                  p_smem_bytes<FMT_BF16, 1, true>() <= 232448,
               "shared memory per CTA");
-static_assert(PairRaw<FMT_NF4, 3, true>::BYTES % 128 == 0 && PairRaw<FMT_NF4, 3, true>::AQ_OFF % 128 == 0 &&
-                  PairRaw<FMT_NF4, 3, true>::SC_OFF % 128 == 0,
+template <int FMT, int CFG, bool DX>
+constexpr bool raw_aligned() {
+  using R = PairRaw<FMT, CFG, DX>;
+  return R::BYTES % 128 == 0 && R::AQ_OFF % 128 == 0 && R::SC_OFF % 128 == 0 && R::CODE_BYTES % 128 == 0;
+}
+static_assert(raw_aligned<FMT_NF4, 3, true>() && raw_aligned<FMT_NF4, 3, false>() &&
+                  raw_aligned<FMT_Q8_0, 4, true>() && raw_aligned<FMT_Q8_0, 4, false>() &&
+                  raw_aligned<FMT_Q4_0, 4, true>() && raw_aligned<FMT_Q4_0, 4, false>() &&
+                  raw_aligned<FMT_Q4_K, 4, true>() && raw_aligned<FMT_Q4_K, 4, false>(),
               "raw ring slots keep TMA destinations 128-byte aligned");
 
 // warps: 0 TMA producer, 1 TMEM / MMA issuer, 2-5 epilogue, then the decode
@@ -123,6 +149,34 @@ static_assert(PairRaw<FMT_NF4, 3, true>::BYTES % 128 == 0 && PairRaw<FMT_NF4, 3,
 template <int FMT, int CFG>
 constexpr int p_threads() {
   return (FMT == FMT_BF16) ? 6 * 32 : (6 + PairCfg<CFG>::DQ_WARPS + (PairRaw<FMT, CFG, false>::ON ? 1 : 0)) * 32;
+}
+
+// One line's bytes from its raw ring row (line starts `addr`, 4-byte
+// aligned) into RawLine words 0 .. LINE/4-1: 16-byte loads from the aligned
+// address at or below, shifted down by the (warp-uniform) word offset.
+template <int FMT, int LINE>
+__device__ __forceinline__ void read_raw_line(uint32_t addr, RawLine& r) {
+  constexpr int NW = LINE / 4;                 // words of the line
+  constexpr int NC = (LINE % 16) ? (LINE + 12 + 15) / 16 : LINE / 16;  // 16-byte loads
+  uint32_t u[4 * (NC > 0 ? NC : 1)];
+  const uint32_t base = addr & ~15u;
+#pragma unroll
+  for (int i = 0; i < NC; ++i) {
+    const uint4 v = lds_v4(base + 16 * i);
+    u[4 * i] = v.x; u[4 * i + 1] = v.y; u[4 * i + 2] = v.z; u[4 * i + 3] = v.w;
+  }
+  if constexpr (LINE % 16 == 0) {
+#pragma unroll
+    for (int i = 0; i < NW; ++i) r.w[i] = u[i];
+  } else {
+    const uint32_t sh = (addr & 15u) >> 2;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      const uint32_t a = sh & 1 ? u[i + 1] : u[i];
+      const uint32_t b = sh & 1 ? u[i + 3] : u[i + 2];
+      r.w[i] = sh & 2 ? b : a;
+    }
+  }
 }
 
 struct PairTile {
@@ -219,8 +273,8 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
   if (warp == 2 && lane == 0) prefetch_tmap(&tm_out);
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_a);
-    if (FMT == FMT_BF16 || Raw::ON) prefetch_tmap(&tm_w);
-    if (Raw::ON && DX && args.raw_dq) prefetch_tmap(&tm_aq);
+    if (FMT == FMT_BF16 || (Raw::ON && args.raw_on)) prefetch_tmap(&tm_w);
+    if (Raw::ON && args.raw_on && ((DX && args.raw_dq) || FMT == FMT_Q4_K)) prefetch_tmap(&tm_aq);
     if (has_lora) {
       prefetch_tmap(&tm_la);
       prefetch_tmap(&tm_lb);
@@ -522,7 +576,9 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     // new one and kept with the one before it; a line records which word
     // and group it needs (low 32 bits of their indices) and picks them at
     // decode time, when the load issued for it has had an item to land.
-    const bool dq_cache = Raw::ON && !DX && args.wv.absmax == nullptr && args.wv.aq_align8;
+    const bool raw = Raw::ON && args.raw_on;
+    const bool dq_cache = FMT == FMT_NF4 && raw && !DX && !GROUPED && args.wv.absmax == nullptr &&
+                          args.wv.aq_align8;
     int64_t aq_base = -1, sc_grp = -1;
     uint32_t aq_new_lo = 0, aq_new_hi = 0, aq_old_lo = 0, aq_old_hi = 0, aq_old_base = 0xffffffffu;
     float sc_new = 0.f, sc_old = 0.f;
@@ -552,10 +608,10 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
           r.w[8] = (uint32_t)wb;
           r.w[9] = (uint32_t)grp;
           r.q = (int32_t)(ln & 7);
-        } else if (Raw::ON && DX && args.raw_dq) {
+        } else if (raw && DX && args.raw_dq) {
           // everything this line needs arrives through the raw ring
-        } else if (Raw::ON) {
-          load_nf4_scale(args.wv, ln, r);  // the code bytes come through the raw ring
+        } else if (raw) {
+          load_line_side<FMT>(*c.wv, ln, r);  // the code bytes come through the raw ring
         } else {
           load_line<FMT>(*c.wv, ln, r);
         }
@@ -577,7 +633,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       const int s = c.it % P_STAGES;
       const uint32_t ph = (c.it / P_STAGES) & 1;
       bool ok = true;
-      if (Raw::ON) {
+      if (raw) {
         // this item's code bytes: wait for them (every lane, for its own
         // acquire) and copy them to registers; the slot is handed back after
         // the line's stores (below)
@@ -586,10 +642,23 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
         if (!__all_sync(0xffffffffu, ok)) return false;
         if (valid) {
           const uint32_t slot = sRaw + rs * Raw::BYTES;
-          const uint32_t src = slot + (DX ? (uint32_t)((d & 63) * 64 + (d >> 6) * 32) : (uint32_t)(d * 32));
-          const uint4 a = lds_v4(src), b = lds_v4(src + 16);
-          r.w[0] = a.x; r.w[1] = a.y; r.w[2] = a.z; r.w[3] = a.w;
-          r.w[4] = b.x; r.w[5] = b.y; r.w[6] = b.z; r.w[7] = b.w;
+          const int row = DX ? (d & 63) : d;
+          // the line's first byte within its box row: the box starts at the
+          // 16-byte aligned address at or below the CTA's first line
+          int off;
+          if constexpr (FMT == FMT_Q4_K) {
+            off = DX ? 32 * (d >> 6) : 0;
+          } else if (!DX) {
+            off = (Raw::LINE * c.kb) & 15;
+          } else {
+            const int64_t kl0 = c.base - (d >> 6);
+            off = Raw::LINE * (d >> 6) + (int)((Raw::LINE * kl0) & 15);
+          }
+          read_raw_line<FMT, Raw::LINE>(slot + (uint32_t)(row * Raw::BOX + off), r);
+          if constexpr (FMT == FMT_Q4_K) {
+            const uint4 h = lds_v4(slot + Raw::CODE_BYTES + (uint32_t)(row * 16));
+            r.w[8] = h.x; r.w[9] = h.y; r.w[10] = h.z; r.w[11] = h.w;
+          }
           if (DX && args.raw_dq) {
             // absmax code of (row, block) and the group scale of its line
             const int kblk = (int)c.base;  // this thread's k-block
@@ -630,7 +699,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_cluster_after_smem_writes(bready0 + s * 8);
-        if (Raw::ON) mbar_arrive(smem_u32(&bars->raw_empty[c.it % Raw::STAGES]));
+        if (raw) mbar_arrive(smem_u32(&bars->raw_empty[c.it % Raw::STAGES]));
       }
       return true;
     };
@@ -661,7 +730,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     }
   }
 
-  if (Raw::ON && warp == 6 + Cfg::DQ_WARPS && lane == 0) {
+  if (Raw::ON && args.raw_on && warp == 6 + Cfg::DQ_WARPS && lane == 0) {
     // ---------------------------------------------------- raw code producer
     // the same item sequence as the decode warps: every (tile, k-block) of
     // this pair, the adapter chunk included (no bytes: a plain arrive)
@@ -679,12 +748,27 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
         const uint32_t bar = smem_u32(&bars->raw_full[rs]);
         const uint32_t slot = sRaw + rs * Raw::BYTES;
         if (kb < nkb) {
-          if (!DX) {
-            mbar_arrive_expect_tx(bar, Raw::CODE_BYTES);
-            tma_load_2d(slot, &tm_w, bar, kb * 32, ncol);
-          } else if (!args.raw_dq) {
-            mbar_arrive_expect_tx(bar, Raw::CODE_BYTES);
-            tma_load_2d(slot, &tm_w, bar, ncol / 2, kb * kBK);
+          // the box: first weight row, and the byte x of the first line in
+          // its row rounded down to 16 (Q4_K: the chunk's code bytes, and
+          // the super-block's header as a second box)
+          const int64_t line0 = DX ? ncol / 64 : kb;
+          const int32_t row0 = DX ? kb * kBK : ncol;
+          int32_t x, xh = 0;
+          if constexpr (FMT == FMT_Q4_K) {
+            x = (int32_t)((line0 >> 2) * 144 + 16 + 32 * (line0 & 3));
+            xh = (int32_t)((line0 >> 2) * 144);
+          } else {
+            x = (int32_t)((Raw::LINE * line0) & ~int64_t(15));
+          }
+          if (!(DX && args.raw_dq)) {
+            mbar_arrive_expect_tx(bar, Raw::CODE_BYTES + Raw::HDR_BYTES);
+            if constexpr (GROUPED) {
+              tma_load_3d(slot, &tm_w, bar, x, row0, tc.e);
+              if constexpr (FMT == FMT_Q4_K) tma_load_3d(slot + Raw::CODE_BYTES, &tm_aq, bar, xh, row0, tc.e);
+            } else {
+              tma_load_2d(slot, &tm_w, bar, x, row0);
+              if constexpr (FMT == FMT_Q4_K) tma_load_2d(slot + Raw::CODE_BYTES, &tm_aq, bar, xh, row0);
+            }
           } else {
             // codes, the 64 rows' absmax codes from block (kblk0 & ~15) on,
             // and the group scales from (g_lo & ~3) to g_hi rounded up to

@@ -171,6 +171,25 @@ struct GroupedSched {
 cudaError_t launch_grouped_schedule(const int32_t* offsets, int E, int64_t M_total, int tile_rows, int nblk_f,
                                     int nblk_d, const GroupedSched& s, int* err, cudaStream_t st);
 
+// Raw ring geometry (pair kernel): the quantised bytes of one item reach
+// shared memory as one byte box per CTA: forward, one 64-element line of each
+// of the CTA's weight rows; dX, the CTA's two consecutive lines of each of 64
+// weight rows.  raw_line_bytes: bytes of one line in a weight row (Q4_K: the
+// code bytes of one 64-element chunk, its 16-byte super-block header comes
+// as a second box).  raw_box_bytes: inner box width, the line's bytes from a
+// 16-byte aligned start (a Q8_0 / Q4_0 line starts up to 12 bytes past one).
+__host__ __device__ constexpr int raw_line_bytes(int fmt) {
+  return fmt == 1 ? 32 : fmt == 2 ? 68 : fmt == 3 ? 36 : fmt == 4 ? 32 : fmt == 5 ? 64 : fmt == 6 ? 32 : 0;
+}
+__host__ __device__ constexpr int raw_box_bytes(int fmt, bool dx) {
+  return fmt == 2 ? (dx ? 160 : 80) : fmt == 3 ? (dx ? 96 : 48) : (dx ? 2 : 1) * raw_line_bytes(fmt);
+}
+// Bytes of one weight row of a format (K elements).
+__host__ __device__ constexpr int64_t row_bytes_of(int fmt, int64_t K) {
+  return fmt == 0 ? 2 * K : fmt == 1 ? K / 2 : fmt == 2 ? K / 32 * 34 : fmt == 3 ? K / 32 * 18
+       : fmt == 4 ? K / 256 * 144 : fmt == 5 ? K : K / 2;
+}
+
 struct GemmArgs {
   int M;                 // total rows (of X / dY / output)
   int n_out;             // output columns (N forward, K for dX)
@@ -189,6 +208,7 @@ struct GemmArgs {
   WeightView wv;
   int* err;              // device error word
   int n_fastest;         // pair kernel tile order: 1 = output column blocks fastest
+  int raw_on;            // pair kernel: quantised bytes through the TMA raw ring (maps.w / maps.aq)
   int raw_dq;            // pair kernel, NF4 dX: absmax codes and group scales through the raw ring
   // Fused projections (forward): projection p owns output columns
   // [proj_end[p-1], proj_end[p]) and adapter columns [p rank, (p+1) rank) of

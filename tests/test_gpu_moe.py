@@ -27,11 +27,12 @@ def _moe_inputs(counts, K, N, r, fmt, seed=0, alpha=None):
     return {"X": X, "dY": dY, "A": A, "B": B, "W": W, "off": off, "alpha": float(alpha or 2 * r), "r": r}
 
 
-def _run(lib, d):
-    import torch
-
-    if d["W"][0]["fmt"] == "bf16":
-        ws = lib.stack_bf16_weights(d["W"])
+def _run(lib, d, stacked=True):
+    """stacked: expert bases back to back in one array (the tensor-map path);
+    else each expert uploaded on its own (per-thread loads; bf16 bases must
+    be stacked)."""
+    if stacked or d["W"][0]["fmt"] == "bf16":
+        ws = lib.upload_experts(d["W"])
     else:
         ws = [lib.DeviceWeight.from_packed(w) for w in d["W"]]
     X, dY = lib.bf16_from_bits(d["X"]), lib.bf16_from_bits(d["dY"])
@@ -66,9 +67,22 @@ def _check(d, got, ref):
             check_f32(got["dB"][e], ref["dB"][e], f"dB[{e}]")
 
 
+@pytest.mark.parametrize("stacked", [True, False], ids=["stacked", "separate"])
 @pytest.mark.parametrize("fmt", ["q8_0", "nf4", "q4_0", "bf16", "q4_k", "fp8_e4m3", "nvfp4", "nf4_dqmap"])
-def test_grouped_mixed_counts(lib, fmt):
+def test_grouped_mixed_counts(lib, fmt, stacked):
+    if fmt == "bf16" and not stacked:
+        pytest.skip("bf16 expert bases are always stacked")
     d = _moe_inputs([0, 5, 130, 1, 0, 260, 64], K=256, N=320, r=16, fmt=fmt, seed=3)
+    _check(d, _run(lib, d, stacked), _oracle(d))
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_0", "nf4", "q4_k"])
+def test_grouped_wide_and_ragged(lib, fmt):
+    """More column blocks than one (N = 1280 forward, K = 768 dX), K whose
+    Q8_0 / Q4_0 rows are not a multiple of 16 bytes (raw ring off) where
+    the format allows it, and an expert spanning several row tiles."""
+    K = 768 if fmt == "q4_k" else 832
+    d = _moe_inputs([700, 3, 0, 300], K=K, N=1280, r=8, fmt=fmt, seed=12)
     _check(d, _run(lib, d), _oracle(d))
 
 
