@@ -45,8 +45,7 @@ constexpr int P_TMEM_COLS = 512;
 //      soon as the epilogue holds its values, so the next tile's MMAs into
 //      it can start while the previous tile is still being stored;
 //   4: 256 x 256 with a quantised base, two TMEM buffers (grouped calls,
-//      whose experts own ~256 rows each); four stages, leaving room for the
-//      raw ring.
+//      whose experts own ~256 rows each).
 // Decoding one B tile for two accumulators halves the decode work per flop.
 template <int CFG>
 struct PairCfg {
@@ -57,7 +56,7 @@ struct PairCfg {
   static constexpr int HALF_N = TN / 2;                   // B rows (or columns) per CTA
   static constexpr int A_BYTES = NACC * 128 * kBK * 2;    // this CTA's A rows
   static constexpr int B_BYTES = HALF_N * kBK * 2;        // this CTA's half of B
-  static constexpr int STAGES = CFG == 1 ? 6 : (CFG == 2 ? 5 : 4);
+  static constexpr int STAGES = (CFG == 1 || CFG == 4) ? 6 : (CFG == 2 ? 5 : 4);
   static constexpr int LINES = HALF_N;                    // decoded 64-wide lines per stage per CTA
   static constexpr int GROUP_WARPS = LINES / 32;          // one line per thread of a group
   static constexpr int GROUPS = CFG == 1 ? 3 : (CFG == 2 ? 5 : 2);  // groups rotate over stages
@@ -81,11 +80,18 @@ struct PairCfg {
 // the 64 rows, x rounded down to 16 bytes) and the range of group scales its
 // lines use (a 1-D bulk copy), when the host finds the layout allows it
 // (GemmArgs::raw_dq).  On 512 x 256 tiles the ring's shared memory comes from
-// the second epilogue staging tile.
+// the second epilogue staging tile and a warp of its own fills it.  On
+// grouped 256 x 256 tiles the box lands in the stage's B slot itself
+// (INPLACE), loaded by the operand producer with the stage's A rows: the
+// decode group reads its lines into registers, meets at a named barrier,
+// and writes the decoded tile over them; no ring of its own, so the six
+// operand stages still fit.
 template <int FMT, int CFG, bool DX>
 struct PairRaw {
   static constexpr bool ON = FMT != FMT_BF16 && ((FMT == FMT_NF4 && CFG == 3) || CFG == 4);
-  static constexpr int STAGES = (CFG == 3 && DX) ? 3 : 4;
+  static constexpr bool INPLACE = ON && CFG == 4;
+  static constexpr bool RING = ON && !INPLACE;
+  static constexpr int STAGES = DX ? 3 : 4;                     // ring slots (RING)
   static constexpr int ROWS = DX ? 64 : PairCfg<CFG>::HALF_N;   // weight rows of one item's box
   static constexpr int BOX = raw_box_bytes(FMT, DX);           // bytes per row of the box
   static constexpr int LINE = raw_line_bytes(FMT);              // bytes of one line
@@ -95,7 +101,8 @@ struct PairRaw {
   static constexpr int SC_OFF = CODE_BYTES + 1024;              // NF4 dX: group scales
   static constexpr int SC_CAP = 64;                             // NF4 dX: group scales a slot holds
   static constexpr int RAW_DQ = FMT == FMT_NF4 && CFG == 3 && DX;
-  static constexpr int BYTES = !ON ? 0 : ((RAW_DQ ? SC_OFF + 4 * SC_CAP : CODE_BYTES + HDR_BYTES) + 127) / 128 * 128;
+  static constexpr int BYTES = !RING ? 0 : ((RAW_DQ ? SC_OFF + 4 * SC_CAP : CODE_BYTES + HDR_BYTES) + 127) / 128 * 128;
+  static_assert(!INPLACE || CODE_BYTES + HDR_BYTES <= PairCfg<CFG>::B_BYTES, "the box fits the B slot");
   static constexpr int OUT_BUFS = (CFG == 2 || (ON && CFG == 3)) ? 1 : 2;  // epilogue staging tiles
 };
 
@@ -106,8 +113,8 @@ struct __align__(8) PairBarriers {
   uint64_t empty[PairCfg<CFG>::STAGES];   // both: MMA completion (multicast)
   uint64_t acc_full[4];                   // per (buffer, accumulator): MMA completion (multicast)
   uint64_t acc_empty[4];                  // CTA 0, per (buffer, accumulator): epilogue warps of both CTAs
-  uint64_t raw_full[4];                   // raw ring: code bytes landed (TMA, this CTA)
-  uint64_t raw_empty[4];                  // raw ring: the decode group has read them (this CTA)
+  uint64_t raw_full[8];                   // raw ring: code bytes landed (TMA, this CTA)
+  uint64_t raw_empty[8];                  // raw ring: the decode group has read them (this CTA)
   uint32_t tmem_base;
   int abort;
   int ep_ok;  // epilogue: result of the "accumulator full" wait, for all 4 warps
@@ -148,7 +155,7 @@ static_assert(raw_aligned<FMT_NF4, 3, true>() && raw_aligned<FMT_NF4, 3, false>(
 // warps, then (raw ring) the code-byte producer
 template <int FMT, int CFG>
 constexpr int p_threads() {
-  return (FMT == FMT_BF16) ? 6 * 32 : (6 + PairCfg<CFG>::DQ_WARPS + (PairRaw<FMT, CFG, false>::ON ? 1 : 0)) * 32;
+  return (FMT == FMT_BF16) ? 6 * 32 : (6 + PairCfg<CFG>::DQ_WARPS + (PairRaw<FMT, CFG, false>::RING ? 1 : 0)) * 32;
 }
 
 // One line's bytes from its raw ring row (line starts `addr`, 4-byte
@@ -176,6 +183,23 @@ __device__ __forceinline__ void read_raw_line(uint32_t addr, RawLine& r) {
       const uint32_t b = sh & 1 ? u[i + 3] : u[i + 2];
       r.w[i] = sh & 2 ? b : a;
     }
+  }
+}
+
+// Coordinates of an item's raw box: the first weight row, and the byte x of
+// the CTA's first line in its row rounded down to 16 (Q4_K: the chunk's
+// code bytes, and xh the super-block's header).  bn: this CTA's first weight
+// row (forward) or output column (dX).
+template <int FMT, bool DX>
+__device__ __forceinline__ void raw_box_coords(int bn, int kb, int32_t& x, int32_t& xh, int32_t& row0) {
+  const int64_t line0 = DX ? bn / 64 : kb;
+  row0 = DX ? kb * kBK : bn;
+  xh = 0;
+  if constexpr (FMT == FMT_Q4_K) {
+    x = (int32_t)((line0 >> 2) * 144 + 16 + 32 * (line0 & 3));
+    xh = (int32_t)((line0 >> 2) * 144);
+  } else {
+    x = (int32_t)((raw_line_bytes(FMT) * line0) & ~int64_t(15));
   }
 }
 
@@ -263,6 +287,8 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     for (int b = 0; b < 4; ++b) {
       mbar_init(smem_u32(&bars->acc_full[b]), 1);
       mbar_init(smem_u32(&bars->acc_empty[b]), 8);
+    }
+    for (int b = 0; b < (Raw::INPLACE ? P_STAGES : Raw::STAGES); ++b) {
       mbar_init(smem_u32(&bars->raw_full[b]), 1);
       mbar_init(smem_u32(&bars->raw_empty[b]), Cfg::GROUP_WARPS);
     }
@@ -313,6 +339,26 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
           // CTA 0 expects both CTAs' bytes; every copy completes on CTA 0's barrier
           if (rank == 0) mbar_arrive_expect_tx(smem_u32(&bars->full[s]), 2 * bytes);
           const uint32_t fb = mapa_shared(smem_u32(&bars->full[s]), 0);
+          if constexpr (Raw::INPLACE) {
+            // this CTA's quantised bytes into its B slot (decoded there)
+            if (args.raw_on) {
+              const uint32_t rb = smem_u32(&bars->raw_full[s]);
+              if (!lora) {
+                int32_t x, xh, row0;
+                raw_box_coords<FMT, DX>(bn, kb, x, xh, row0);
+                mbar_arrive_expect_tx(rb, Raw::CODE_BYTES + Raw::HDR_BYTES);
+                if constexpr (GROUPED) {
+                  tma_load_3d(sb, &tm_w, rb, x, row0, tc.e);
+                  if constexpr (FMT == FMT_Q4_K) tma_load_3d(sb + Raw::CODE_BYTES, &tm_aq, rb, xh, row0, tc.e);
+                } else {
+                  tma_load_2d(sb, &tm_w, rb, x, row0);
+                  if constexpr (FMT == FMT_Q4_K) tma_load_2d(sb + Raw::CODE_BYTES, &tm_aq, rb, xh, row0);
+                }
+              } else {
+                mbar_arrive(rb);  // the adapter chunk: no bytes, keeps the phases in step
+              }
+            }
+          }
           if (!lora) {
 #pragma unroll
             for (int a = 0; a < NACC; ++a) tma_load_2d_pair(sa + a * 16384, &tm_a, fb, kb * kBK, am + 256 * a);
@@ -351,6 +397,10 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       if (rank == 0)
         for (uint32_t k = (it >= P_STAGES ? it - P_STAGES : 0); k < it; ++k)
           mbar_drain(smem_u32(&bars->full[k % P_STAGES]), (k / P_STAGES) & 1);
+      // and each CTA for its own in-place raw boxes
+      if (Raw::INPLACE && args.raw_on)
+        for (uint32_t k = (it >= P_STAGES ? it - P_STAGES : 0); k < it; ++k)
+          mbar_drain(smem_u32(&bars->raw_full[k % P_STAGES]), (k / P_STAGES) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
@@ -635,13 +685,16 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       bool ok = true;
       if (raw) {
         // this item's code bytes: wait for them (every lane, for its own
-        // acquire) and copy them to registers; the slot is handed back after
-        // the line's stores (below)
-        const uint32_t rs = c.it % Raw::STAGES;
-        ok = mbar_wait(smem_u32(&bars->raw_full[rs]), (c.it / Raw::STAGES) & 1, abort, args.err);
-        if (!__all_sync(0xffffffffu, ok)) return false;
-        if (valid) {
-          const uint32_t slot = sRaw + rs * Raw::BYTES;
+        // acquire) and copy them to registers; a ring slot is handed back
+        // after the line's stores (below)
+        const uint32_t rs = Raw::INPLACE ? (uint32_t)s : c.it % Raw::STAGES;
+        const uint32_t rph = Raw::INPLACE ? ph : (c.it / Raw::STAGES) & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->raw_full[rs]), rph, abort, args.err));
+        // in place, a failure is only acted on at the group's barrier below,
+        // which every warp of the group must reach
+        if (!ok && !Raw::INPLACE) return false;
+        if (ok && valid && c.kb < nkb) {
+          const uint32_t slot = Raw::INPLACE ? sB0 + s * P_B_BYTES : sRaw + rs * Raw::BYTES;
           const int row = DX ? (d & 63) : d;
           // the line's first byte within its box row: the box starts at the
           // 16-byte aligned address at or below the CTA's first line
@@ -673,8 +726,12 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
           }
         }
       }
-      if (lane == 0) ok = mbar_wait_cluster(smem_u32(&bars->empty[s]), ph ^ 1, abort, args.err);
-      if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0) == 0) return false;
+      if (lane == 0 && ok) ok = mbar_wait_cluster(smem_u32(&bars->empty[s]), ph ^ 1, abort, args.err);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      // in place: every line of the group has been read before any decoded
+      // line overwrites the box (and the group leaves together on a failure)
+      if (Raw::INPLACE && raw) ok = named_bar_and(2 + g, 32 * Cfg::GROUP_WARPS, ok);
+      if (!ok) return false;
       if (c.kb < nkb) {
         const uint32_t dst = sB0 + s * P_B_BYTES + soff;
         if (valid) {
@@ -699,7 +756,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_cluster_after_smem_writes(bready0 + s * 8);
-        if (raw) mbar_arrive(smem_u32(&bars->raw_empty[c.it % Raw::STAGES]));
+        if (Raw::RING && raw) mbar_arrive(smem_u32(&bars->raw_empty[c.it % Raw::STAGES]));
       }
       return true;
     };
@@ -730,7 +787,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     }
   }
 
-  if (Raw::ON && args.raw_on && warp == 6 + Cfg::DQ_WARPS && lane == 0) {
+  if (Raw::RING && args.raw_on && warp == 6 + Cfg::DQ_WARPS && lane == 0) {
     // ---------------------------------------------------- raw code producer
     // the same item sequence as the decode warps: every (tile, k-block) of
     // this pair, the adapter chunk included (no bytes: a plain arrive)
@@ -748,18 +805,8 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
         const uint32_t bar = smem_u32(&bars->raw_full[rs]);
         const uint32_t slot = sRaw + rs * Raw::BYTES;
         if (kb < nkb) {
-          // the box: first weight row, and the byte x of the first line in
-          // its row rounded down to 16 (Q4_K: the chunk's code bytes, and
-          // the super-block's header as a second box)
-          const int64_t line0 = DX ? ncol / 64 : kb;
-          const int32_t row0 = DX ? kb * kBK : ncol;
-          int32_t x, xh = 0;
-          if constexpr (FMT == FMT_Q4_K) {
-            x = (int32_t)((line0 >> 2) * 144 + 16 + 32 * (line0 & 3));
-            xh = (int32_t)((line0 >> 2) * 144);
-          } else {
-            x = (int32_t)((Raw::LINE * line0) & ~int64_t(15));
-          }
+          int32_t x, xh, row0;
+          raw_box_coords<FMT, DX>(ncol, kb, x, xh, row0);
           if (!(DX && args.raw_dq)) {
             mbar_arrive_expect_tx(bar, Raw::CODE_BYTES + Raw::HDR_BYTES);
             if constexpr (GROUPED) {
