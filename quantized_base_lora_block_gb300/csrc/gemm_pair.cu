@@ -59,7 +59,7 @@ struct PairCfg {
   static constexpr int STAGES = (CFG == 1 || CFG == 4) ? 6 : (CFG == 2 ? 5 : 4);
   static constexpr int LINES = HALF_N;                    // decoded 64-wide lines per stage per CTA
   static constexpr int GROUP_WARPS = LINES / 32;          // one line per thread of a group
-  static constexpr int GROUPS = CFG == 1 ? 3 : (CFG == 2 ? 5 : 2);  // groups rotate over stages
+  static constexpr int GROUPS = (CFG == 1 || CFG == 4) ? 3 : (CFG == 2 ? 5 : 2);  // groups rotate over stages
   static constexpr int DQ_WARPS = GROUP_WARPS * GROUPS;
   static_assert(STAGES % GROUPS == 0, "a stage must always be decoded by the same group");
   static_assert(NBUF * NACC * TN == 512, "accumulators fill TMEM");
