@@ -50,6 +50,13 @@ def parse_args():
     p.add_argument("--stream-layers", type=int, default=32,
                    help="layers for the streamed leg (0 = skip); Llama workload only")
     p.add_argument("--no-moe", action="store_true", help="skip the grouped MoE leg")
+    p.add_argument("--no-context", action="store_true",
+                   help="skip the dequant_blocks GB/s and library-composition baseline legs")
+    p.add_argument("--case", default=None, choices=["gemm_m128", "dequant", "linear_m4096"],
+                   help="run one small case of a kernel family --steps times and print its time (for profiling): "
+                        "gemm_m128 = Llama gate fwd+bwd at 128 rows (one-CTA GEMM), dequant = dequant_blocks of "
+                        "the Llama gate base, linear_m4096 = Llama gate fwd+bwd at 4096 rows (reductions and pair "
+                        "GEMM)")
     p.add_argument("--only-moe", action="store_true",
                    help="run the grouped MoE leg alone and print its result (for profiling)")
     p.add_argument("--no-configs", action="store_true",
@@ -349,6 +356,116 @@ def moe_leg(q, torch, steps, stream):
                      "kernel": "qgemm_pair_kernel grouped (256x256 tiles, Q8_0 decode in the producer)"}}
 
 
+def dequant_leg(q, torch, L, wl, peaks, reps=20):
+    """dequant_blocks on every distinct base weight of the layer: the
+    standalone block decode to bf16 in HBM (HBM-bound): bytes read (codes
+    and scales) + bytes written (bf16), per second."""
+    out, seen = [], set()
+    stream = torch.cuda.current_stream()
+    for lin, d in zip(wl.linears, L):
+        key = (d["N"], d["K"])
+        if key in seen:
+            continue
+        seen.add(key)
+        w = d["W"]
+        Wd = torch.empty((w.N, w.K), dtype=torch.bfloat16, device=w.data.device)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=w.data.device)  # > L2
+        for _ in range(3):
+            q.dequant_blocks(w, out=Wd, stream=stream)
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            q.dequant_blocks(w, out=Wd, stream=stream)
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = sorted(ts)[len(ts) // 2]
+        nbytes = w.nbytes() + Wd.numel() * 2
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out.append({"linear": lin.name, "N": w.N, "K": w.K, "us": ms * 1e3, "bytes": nbytes, "GBps": gbs,
+                    "frac_of_measured_hbm": gbs / peaks["hbm"]})
+    return {"kernel": "dequant_kernel (dequant_blocks)", "format": wl.fmt + ("+dq" if wl.double_quant else ""),
+            "l2": "flushed before each timed launch (256 MB write)", "per_weight": out}
+
+
+def library_leg(q, torch, L, wl, steps):
+    """Context baseline: the same layer composed from library pieces, as a
+    framework without fused kernels would run it: each linear decodes its
+    base to bf16 in HBM with dequant_blocks (forward and again for dX), then
+    cuBLAS bf16 GEMMs (torch.matmul) and PyTorch ops for the adapter terms
+    and gradients."""
+    M, r, alpha = wl.M, wl.rank, wl.alpha
+    s = alpha / r
+    stream = torch.cuda.current_stream()
+    Wd = torch.empty(max(d["N"] * d["K"] for d in L), dtype=torch.bfloat16, device=L[0]["X"].device)
+
+    def step():
+        for d in L:
+            w = q.dequant_blocks(d["W"], out=Wd[: d["N"] * d["K"]].view(d["N"], d["K"]), stream=stream)
+            T = d["X"] @ d["A"].t()
+            d["Y"].copy_(d["X"] @ w.t() + (s * T) @ d["B"].t())
+            d["T"].copy_(T.float())
+        for d in reversed(L):
+            w = q.dequant_blocks(d["W"], out=Wd[: d["N"] * d["K"]].view(d["N"], d["K"]), stream=stream)
+            U = d["dY"] @ d["B"]
+            d["dX"].copy_(d["dY"] @ w + (s * U) @ d["A"])
+            d["dA"].copy_(s * (U.t().float() @ d["X"].float()))
+            d["dB"].copy_(s * (d["dY"].t().float() @ d["T"]))
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    flops = sum(syn.linear_flops(M, l.K, l.N, r) for l in wl.linears)
+    return {"ms_per_step": ms, "value": M / (ms / 1e3), "unit": "tokens/s", "tflops": flops / (ms / 1e3) / 1e12,
+            "kind": "context (library composition, not the product path)",
+            "note": "dequant_blocks to bf16 in HBM + torch.matmul (cuBLAS bf16) + PyTorch adapter ops; dA, dB "
+                    "in fp32"}
+
+
+def run_case(args):
+    """One small case of a kernel family, --steps times (for ncu captures)."""
+    import torch
+
+    import quantized_base_lora_block_gb300 as q
+
+    q.load()
+    wl = syn.WORKLOADS["llama31_8b_nf4dq"]
+    M = {"gemm_m128": 128, "dequant": 1, "linear_m4096": 4096}[args.case]
+    gate = [i for i, l in enumerate(wl.linears) if l.name == "gate_proj"][0]
+    inp = syn.make_linear_inputs(wl, gate, seed=0, M=M)
+    w = q.DeviceWeight.from_packed(inp["W"])
+    X, A, B, dY = (q.bf16_from_bits(inp[k]) for k in ("X", "A", "B", "dY"))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if args.case == "dequant":
+        out = torch.empty((w.N, w.K), dtype=torch.bfloat16, device="cuda")
+        f = lambda: q.dequant_blocks(w, out=out)  # noqa: E731
+    else:
+        ws = q.alloc_workspace(q.workspace_bytes(w, M, wl.rank))
+        Y, T = q.linear_fwd(w, X, A, B, wl.alpha, workspace=ws)
+
+        def f():
+            q.linear_fwd(w, X, A, B, wl.alpha, Y=Y, T=T, workspace=ws)
+            q.linear_bwd(w, X, A, B, T, dY, wl.alpha, workspace=ws)
+    f()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(args.steps):
+        f()
+    e1.record()
+    torch.cuda.synchronize()
+    assert q.device_error() == 0
+    print(json.dumps({"case": args.case, "rows": M, "ms_per_iter": e0.elapsed_time(e1) / args.steps}))
+
+
 def fused_groups(wl):
     """Linears of a decoder layer that share their input and run as one fused
     launch (q|k|v, gate|up), where the fused call supports them (widths
@@ -478,6 +595,8 @@ def config_of(wl):
 def main():
     args = parse_args()
     wl = syn.WORKLOADS[args.workload]
+    if args.case:
+        return run_case(args)
     if args.only_moe:
         import torch
 
@@ -726,6 +845,10 @@ def main():
     moe_res = None
     if not args.no_moe and rank == 0:
         moe_res = moe_leg(q, torch, 10, stream)
+    deq_res = lib_res = None
+    if rank == 0 and not args.no_context:
+        deq_res = dequant_leg(q, torch, L, wl, peaks)
+        lib_res = library_leg(q, torch, L, wl, 5)
     cfg_res = None
     if not args.no_configs and rank == 0:
         cfg_res = [config_leg(q, torch, name, 10, dev)
@@ -761,6 +884,7 @@ def main():
                        "met": flops_step / t_step / 1e12 >= 0.6 * NOMINAL_BF16_TFLOPS},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clk, "stream": stream_res, "moe": moe_res, "configs": cfg_res,
+            "dequant_blocks": deq_res, "library_baseline": lib_res,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

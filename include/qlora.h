@@ -171,6 +171,22 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
                          void* dX, float* dA, float* dB,
                          void* workspace, size_t ws_bytes, void* stream);
 
+/* Debug forms of the two calls above: identical, except that the GEMM
+ * output is written as its fp32 accumulator values (Y32 [M x N], resp.
+ * dX32 [M x K], fp32, device, 16-byte aligned) instead of bf16, so that a
+ * test can see the error of the computation without the bf16 output
+ * rounding.  dX32 may not be NULL.  Slower (no staged output stores); for
+ * tests only. */
+int32_t qlora_debug_linear_fwd_f32(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha,
+                                   const void* X, const void* A, const void* B,
+                                   float* Y32, float* T_save,
+                                   void* workspace, size_t ws_bytes, void* stream);
+int32_t qlora_debug_linear_bwd_f32(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha,
+                                   const void* X, const void* A, const void* B,
+                                   const float* T_save, const void* dY,
+                                   float* dX32, float* dA, float* dB,
+                                   void* workspace, size_t ws_bytes, void* stream);
+
 /* ---- fused projections that share their input ------------------------------
  * The P LoRA linears that read the same X in a decoder layer (q, k, v of the
  * attention block; gate and up of the MLP) as one call each way: one pass of

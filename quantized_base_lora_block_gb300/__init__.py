@@ -98,6 +98,8 @@ SIGNATURES = {
     "qlora_multi_linear_bwd": (_I32, [_WD, _I32, ctypes.POINTER(ctypes.c_int64), _I64, _I32, _F32, _P, _P, _P, _P,
                                       _P, _P, _P, _P, _P, _SZ, _P]),
     "qlora_noalloc_scratch_bytes": (_SZ, []),
+    "qlora_debug_linear_fwd_f32": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "qlora_debug_linear_bwd_f32": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "qlora_profile_gemm": (_I32, [_I32]),
     "qlora_profile_gemm_read": (_I32, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
                                        ctypes.POINTER(ctypes.c_double)]),
@@ -229,6 +231,36 @@ def workspace_bytes(w: DeviceWeight, M: int, rank: int) -> int:
 def alloc_workspace(nbytes: int, device="cuda"):
     torch = _torch()
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def debug_linear_fwd_f32(w: DeviceWeight, X, A, B, alpha: float, workspace=None, stream=None):
+    """The forward with Y returned as the fp32 accumulator values (tests)."""
+    torch = _torch()
+    M, r = X.shape[0], A.shape[0]
+    Y = torch.empty((M, w.N), dtype=torch.float32, device=X.device)
+    T = torch.empty((M, r), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_bytes(w, M, r), X.device)
+    st = load().qlora_debug_linear_fwd_f32(ctypes.byref(w.desc), M, r, float(alpha), _ptr(X), _ptr(A), _ptr(B),
+                                           _ptr(Y), _ptr(T), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check("qlora_debug_linear_fwd_f32", st)
+    return Y, T
+
+
+def debug_linear_bwd_f32(w: DeviceWeight, X, A, B, T, dY, alpha: float, workspace=None, stream=None):
+    """The backward with dX returned as the fp32 accumulator values (tests)."""
+    torch = _torch()
+    M, r = X.shape[0], A.shape[0]
+    dX = torch.empty((M, w.K), dtype=torch.float32, device=X.device)
+    dA = torch.empty((r, w.K), dtype=torch.float32, device=X.device)
+    dB = torch.empty((w.N, r), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_bytes(w, M, r), X.device)
+    st = load().qlora_debug_linear_bwd_f32(ctypes.byref(w.desc), M, r, float(alpha), _ptr(X), _ptr(A), _ptr(B),
+                                           _ptr(T), _ptr(dY), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(workspace),
+                                           workspace.numel(), _stream_ptr(stream))
+    _check("qlora_debug_linear_bwd_f32", st)
+    return dX, dA, dB
 
 
 def dequant_blocks(w: DeviceWeight, out=None, stream=None):

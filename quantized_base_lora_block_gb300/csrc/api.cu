@@ -300,9 +300,12 @@ struct ProjSplit {
 // la lb with A_op = dY [M x N], la = sU, lb = A [r x K].  la has la_cols
 // columns; with fused projections (forward, ps->P > 1) a tile's adapter chunk
 // takes the `rank` columns of its projection.
+// out_f32 (debug): when set, the fp32 accumulators are written there
+// ([M x n_out]) instead of bf16 to `out`.
 static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M, int rank, int la_cols,
                                   const ProjSplit* ps, const void* a_op, const void* la, const void* lb, void* out,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, float* out_f32 = nullptr) {
+  if (out_f32) out = out_f32;  // the bf16 store map is then built but never used
   const int64_t N = w->N, K = w->K;
   // pair tiles on an SM pair; short problems use one CTA per 128 x 256 tile
   const int pair = M > kBM ? pair_cfg(w->fmt, M, dx ? K : N, sm_count()) : 0;
@@ -353,6 +356,7 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
   a.w_lines_per_row = K / 64;
   a.w_rows = N;
   a.out = static_cast<__nv_bfloat16*>(out);
+  a.out_f32 = out_f32;
   a.wv = view_of(w);
   a.err = device_error_word();
   a.raw_dq = raw_dq;
@@ -669,9 +673,10 @@ static size_t multi_workspace(const qlora_weight_desc* w, const ProjSplit& ps, i
   return dense_layout(M, w->N, w->K, ps.P * rank).total;
 }
 
+// Y32 (debug): when set, Y is written there as fp32 instead of bf16 to Y.
 static int32_t linear_fwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, int64_t M, int32_t rank,
                                float alpha, const void* X, const void* A, const void* B, void* Y, float* T_save,
-                               void* workspace, size_t ws_bytes, void* stream) {
+                               void* workspace, size_t ws_bytes, void* stream, float* Y32 = nullptr) {
   if (M < 0 || !std::isfinite(alpha)) return QLORA_ERR_INVALID;
   if (M == 0) return QLORA_OK;
   if (M > (1ll << 31) - 256) return QLORA_ERR_UNSUPPORTED;
@@ -703,13 +708,14 @@ static int32_t linear_fwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, 
   if (launch_row_reduce_fin(rt, Q, st) != cudaSuccess) return QLORA_ERR_CUDA;
 
   // 2) Y = X deq(W)^T + sT B^T, each tile's adapter chunk from its projection
-  return cuda_status(run_dense_gemm(w, false, M, rank, Q, &ps, X, sT, B, Y, st));
+  return cuda_status(run_dense_gemm(w, false, M, rank, Q, &ps, X, sT, B, Y, st, Y32));
 }
 
+// dX32 (debug): when set, dX is written there as fp32 instead of bf16 to dX.
 static int32_t linear_bwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, int64_t M, int32_t rank,
                                float alpha, const void* X, const void* A, const void* B, const float* T_save,
                                const void* dY, void* dX, float* dA, float* dB, void* workspace, size_t ws_bytes,
-                               void* stream) {
+                               void* stream, float* dX32 = nullptr) {
   if (M < 0 || !std::isfinite(alpha)) return QLORA_ERR_INVALID;
   if (!dA || !dB) return QLORA_ERR_INVALID;
   const int64_t N = w->N, K = w->K;
@@ -794,11 +800,11 @@ static int32_t linear_bwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, 
   std::lock_guard<std::mutex> g(g_side_mu);
   SideStream* ss = side_stream_locked();
   if (!ss) {
-    if (run_dense_gemm(w, true, M, Q, Q, nullptr, dY, sU, A, dX, st) != cudaSuccess) return QLORA_ERR_CUDA;
+    if (run_dense_gemm(w, true, M, Q, Q, nullptr, dY, sU, A, dX, st, dX32) != cudaSuccess) return QLORA_ERR_CUDA;
     return cuda_status(launch_col_reduce_fin(cb, &ca, Q, st));
   }
   cudaError_t e = cudaEventRecord(ss->fork, st);
-  if (e == cudaSuccess) e = run_dense_gemm(w, true, M, Q, Q, nullptr, dY, sU, A, dX, st);
+  if (e == cudaSuccess) e = run_dense_gemm(w, true, M, Q, Q, nullptr, dY, sU, A, dX, st, dX32);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->fork, 0);
   if (e == cudaSuccess) e = launch_col_reduce_fin(cb, &ca, Q, ss->s);
   if (e == cudaSuccess) e = cudaEventRecord(ss->join, ss->s);
@@ -830,6 +836,33 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   ProjSplit ps;
   ps.end[0] = w->N;
   return linear_bwd_impl(w, ps, M, rank, alpha, X, A, B, T_save, dY, dX, dA, dB, workspace, ws_bytes, stream);
+}
+
+// Debug: the same calls with the GEMM output (Y, resp. dX) written as the
+// fp32 accumulator values instead of bf16.
+int32_t qlora_debug_linear_fwd_f32(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha, const void* X,
+                                   const void* A, const void* B, float* Y32, float* T_save, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+  int v = validate_weight(w);
+  if (v != QLORA_OK) return v;
+  if ((v = validate_rank(rank)) != QLORA_OK) return v;
+  if (!Y32) return QLORA_ERR_INVALID;
+  ProjSplit ps;
+  ps.end[0] = w->N;
+  return linear_fwd_impl(w, ps, M, rank, alpha, X, A, B, Y32, T_save, workspace, ws_bytes, stream, Y32);
+}
+
+int32_t qlora_debug_linear_bwd_f32(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha, const void* X,
+                                   const void* A, const void* B, const float* T_save, const void* dY, float* dX32,
+                                   float* dA, float* dB, void* workspace, size_t ws_bytes, void* stream) {
+  int v = validate_weight(w);
+  if (v != QLORA_OK) return v;
+  if ((v = validate_rank(rank)) != QLORA_OK) return v;
+  if (!dX32) return QLORA_ERR_INVALID;
+  ProjSplit ps;
+  ps.end[0] = w->N;
+  return linear_bwd_impl(w, ps, M, rank, alpha, X, A, B, T_save, dY, dX32, dA, dB, workspace, ws_bytes, stream,
+                         dX32);
 }
 
 size_t qlora_multi_workspace_bytes(const qlora_weight_desc* w, int32_t P, const int64_t* n_split, int64_t M,

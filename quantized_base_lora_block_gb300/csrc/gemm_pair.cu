@@ -504,6 +504,23 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
           // write the next expert's rows)
           const int nvalid = GROUPED ? min(128, tc.rows - 256 * a - 128 * (int)rank) : 128;
           const bool store = row0 < args.M && nvalid > 0 && tc.n0 + 64 * c < args.n_out;
+          if (args.out_f32 != nullptr) {
+            // debug: the fp32 accumulator values, row by row from registers
+            if (store && row_in_tile < nvalid && row0 + row_in_tile < args.M) {
+              float4* dst = reinterpret_cast<float4*>(args.out_f32 + (int64_t)(row0 + row_in_tile) * args.n_out +
+                                                      tc.n0 + 64 * c);
+#pragma unroll
+              for (int q = 0; q < 16; ++q)
+                dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                     __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            }
+            if (!last) {
+              tmem_ld_32x32b_x32(tcol + 64 * (c + 1), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+              tmem_ld_32x32b_x32(tcol + 64 * (c + 1) + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+              tc_wait_ld();
+            }
+            continue;
+          }
           if (GROUPED && store && nvalid < 128) {
             if (row_in_tile < nvalid) {
               uint4* dst = reinterpret_cast<uint4*>(args.out + (int64_t)(row0 + row_in_tile) * args.n_out + tc.n0 + 64 * c);

@@ -221,7 +221,14 @@ __global__ void __launch_bounds__(num_threads<FMT>(), 1)
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + ab * kBN + c * 32, v);
         tc_wait_ld();
-        if (row_ok && tc.n0 + c * 32 < args.n_out) {
+        if (row_ok && tc.n0 + c * 32 < args.n_out && args.out_f32 != nullptr) {
+          float4* dst = reinterpret_cast<float4*>(args.out_f32 + (int64_t)(tc.m0 + row_in_tile) * args.n_out +
+                                                  tc.n0 + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                 __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        } else if (row_ok && tc.n0 + c * 32 < args.n_out) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {

@@ -200,6 +200,7 @@ struct GemmArgs {
   int64_t w_lines_per_row;  // K_w / 64
   int64_t w_rows;           // N_w
   __nv_bfloat16* out;    // [M x n_out] bf16
+  float* out_f32;        // debug: when set, the fp32 accumulators are written here instead of `out`
   // grouped (pair kernel): tile t = tile_sched[t] (expert, first row, rows,
   // column block) for t < *tile_count (both device; written by the schedule
   // kernel earlier in the stream); null for dense problems
