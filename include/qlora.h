@@ -142,6 +142,11 @@ int32_t qlora_version(void);
  * calls; calls that may overlap on the GPU need separate workspaces. */
 size_t qlora_workspace_bytes(const qlora_weight_desc* w, int64_t M, int32_t rank);
 
+/* Bytes of workspace qlora_linear_fwd alone needs (the scaled activation
+ * s*T, bf16 [M x rank], 256-byte rounded); at most qlora_workspace_bytes.
+ * 0 on invalid arguments. */
+size_t qlora_forward_workspace_bytes(const qlora_weight_desc* w, int64_t M, int32_t rank);
+
 /* Decode the whole base weight to bf16: W_bf16[N*K] (device, caller-owned)
  * receives deq(Wq) bit-exactly as defined above.  For QLORA_FMT_BF16 it is a
  * copy. */
@@ -262,7 +267,8 @@ int32_t qlora_stacked_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t 
  * workspace is a fixed 16 MiB array kept in device memory by the library
  * (qlora_noalloc_scratch_bytes()), reserved on every GPU that loads the
  * library until the process exits.  Returns QLORA_ERR_WORKSPACE, launching
- * nothing, when qlora_workspace_bytes(w, M, rank) exceeds that size.  The
+ * nothing, when qlora_forward_workspace_bytes(w, M, rank) exceeds that size
+ * (2 M rank bytes: M rank <= 8 Mi, e.g. 524,288 rows at rank 16).  The
  * first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  All calls on a device share the array: calls whose GPU work

@@ -98,6 +98,7 @@ SIGNATURES = {
     "qlora_multi_linear_bwd": (_I32, [_WD, _I32, ctypes.POINTER(ctypes.c_int64), _I64, _I32, _F32, _P, _P, _P, _P,
                                       _P, _P, _P, _P, _P, _SZ, _P]),
     "qlora_noalloc_scratch_bytes": (_SZ, []),
+    "qlora_forward_workspace_bytes": (_SZ, [_WD, _I64, _I32]),
     "qlora_debug_linear_fwd_f32": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "qlora_debug_linear_bwd_f32": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "qlora_profile_gemm": (_I32, [_I32]),

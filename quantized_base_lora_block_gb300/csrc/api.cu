@@ -632,6 +632,13 @@ size_t qlora_workspace_bytes(const qlora_weight_desc* w, int64_t M, int32_t rank
   return dense_layout(M, w->N, w->K, rank).total;
 }
 
+size_t qlora_forward_workspace_bytes(const qlora_weight_desc* w, int64_t M, int32_t rank) {
+  if (validate_weight(w) != QLORA_OK || validate_rank(rank) != QLORA_OK || M < 0) return 0;
+  if (M == 0) return 256;
+  const DenseLayout L = dense_layout(M, w->N, w->K, rank);
+  return L.act_off + L.act_bytes;
+}
+
 int32_t dequant_blocks(const qlora_weight_desc* w, void* W_bf16, void* stream) {
   int v = validate_weight(w);
   if (v != QLORA_OK) return v;
@@ -686,7 +693,8 @@ static int32_t linear_fwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, 
   const int64_t N = w->N, K = w->K;
   const int Q = ps.P * rank;  // adapter columns of all projections
   const DenseLayout L = dense_layout(M, N, K, Q);
-  if (!workspace || ws_bytes < multi_workspace(w, ps, M, rank)) return QLORA_ERR_WORKSPACE;
+  // the forward uses only the scaled-activation region of the layout
+  if (!workspace || ws_bytes < L.act_off + L.act_bytes) return QLORA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);

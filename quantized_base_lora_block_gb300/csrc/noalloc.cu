@@ -57,7 +57,7 @@ size_t qlora_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 int32_t qlora_linear_fwd_noalloc(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha, const void* X,
                                  const void* A, const void* B, void* Y, float* T_save, void* stream) {
-  const size_t need = qlora_workspace_bytes(w, M, rank);
+  const size_t need = qlora_forward_workspace_bytes(w, M, rank);
   // invalid arguments: let the regular entry point report the precise status
   // (it validates everything before it would look at the workspace)
   if (need == 0) return qlora_linear_fwd(w, M, rank, alpha, X, A, B, Y, T_save, nullptr, 0, stream);

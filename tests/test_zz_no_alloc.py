@@ -52,11 +52,37 @@ def test_noalloc_rejects_problems_larger_than_its_scratch(lib):
     c = lib.load()
     cap = c.qlora_noalloc_scratch_bytes()
     assert cap == 16 << 20
-    # a Llama-sized gate projection over 262144 tokens needs more than 16 MiB
+    # a Llama-sized gate projection over 1,048,576 tokens: its forward needs
+    # 32 MiB of scaled activation, more than the 16 MiB array
     desc = lib.WeightDesc(lib.FMT["nf4"], 0, 14336, 4096, 0x1000, 0x2000, None, None)
-    assert c.qlora_workspace_bytes(ctypes.byref(desc), 262144, 16) > cap
+    assert c.qlora_forward_workspace_bytes(ctypes.byref(desc), 1 << 20, 16) > cap
     n0 = c.qlora_launch_count()
-    st = c.qlora_linear_fwd_noalloc(ctypes.byref(desc), 262144, 16, 16.0, 0x10000, 0x20000, 0x30000, 0x40000,
+    st = c.qlora_linear_fwd_noalloc(ctypes.byref(desc), 1 << 20, 16, 16.0, 0x10000, 0x20000, 0x30000, 0x40000,
                                     0x50000, None)
     assert st == -6  # QLORA_ERR_WORKSPACE, nothing launched
     assert c.qlora_launch_count() == n0
+
+
+def test_noalloc_serves_forwards_whose_backward_workspace_is_larger(lib):
+    """131,072 rows at rank 16: the forward needs 4 MiB (fits the array), the
+    forward+backward layout 20 MiB (does not)."""
+    import torch
+
+    c = lib.load()
+    M, K, N, r = 131072, 256, 256, 16
+    inp = _inputs(M, K, N, r, "q8_0", False, 13)
+    d = to_device(inp)
+    w = d["W"]
+    assert c.qlora_forward_workspace_bytes(ctypes.byref(w.desc), M, r) <= c.qlora_noalloc_scratch_bytes()
+    assert c.qlora_workspace_bytes(ctypes.byref(w.desc), M, r) > c.qlora_noalloc_scratch_bytes()
+    Y_ref, T_ref = lib.linear_fwd(w, d["X"], d["A"], d["B"], inp["alpha"])
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    T = torch.empty((M, r), dtype=torch.float32, device="cuda")
+    st = c.qlora_linear_fwd_noalloc(ctypes.byref(w.desc), M, r, inp["alpha"], d["X"].data_ptr(), d["A"].data_ptr(),
+                                    d["B"].data_ptr(), Y.data_ptr(), T.data_ptr(),
+                                    torch.cuda.current_stream().cuda_stream)
+    assert st == 0, lib.STATUS.get(st, st)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    assert torch.equal(Y, Y_ref) and torch.equal(T, T_ref)
+
