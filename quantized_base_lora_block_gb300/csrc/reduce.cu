@@ -36,7 +36,7 @@ constexpr int TP = 64;      // rows of L per tile
 constexpr int TJ = 64;      // columns of L per tile
 constexpr int LPITCH = 72;  // padded smem row pitch of an L tile (elements)
 constexpr int NTHR = 128;
-constexpr int kColStages = 3;
+constexpr int kColStages = 4;  // measured: 3 and 5 stages slower (fewer bytes in flight / fewer CTAs per SM)
 using namespace wmma16;
 
 template <int Q>
