@@ -24,4 +24,7 @@ from .qlora_oracle import (  # noqa: F401
     multi_linear_bwd,
     stacked_linear_fwd,
     stacked_linear_bwd,
+    swiglu_fwd,
+    swiglu_bwd,
+    swiglu_grad_gate_up,
 )

@@ -406,3 +406,43 @@ def stacked_linear_bwd(X, Wd, As: Sequence[np.ndarray], Bs: Sequence[np.ndarray]
         dA.append(s * (U.T @ X))
         dB.append(s * (dY.T @ T))
     return {"dX": dX, "dA": dA, "dB": dB}
+
+
+# ----------------------------------------------------------------------------
+# gate / up projections with the SwiGLU activation (the MLP of the Llama and
+# Qwen3 layers the workloads are shaped after): two LoRA linears over the same
+# X, G = X Wg^T + s Tg Bg^T and U = X Wu^T + s Tu Bu^T, and
+#     H = silu(G) * U,   silu(g) = g * sigmoid(g).
+# Backward from dH: dG = dH * U * sigmoid(G) * (1 + G (1 - sigmoid(G))),
+# dU = dH * silu(G), then the fused-projection backward with dY = [dG | dU]
+# (the input gradient summed over both projections).
+# ----------------------------------------------------------------------------
+def _sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def swiglu_fwd(X, Wg, Wu, Ag, Au, Bg, Bu, alpha: float):
+    """Returns (H [M, I], G [M, I], U [M, I], T [M, 2r] = [Tg | Tu])."""
+    G, Tg = linear_fwd(X, Wg, Ag, Bg, alpha)
+    U, Tu = linear_fwd(X, Wu, Au, Bu, alpha)
+    H = G * _sigmoid(G) * U
+    return H, G, U, np.concatenate([Tg, Tu], axis=1)
+
+
+def swiglu_grad_gate_up(G, U, dH):
+    """(dG, dU) of H = silu(G) * U."""
+    G, U, dH = _f64(G), _f64(U), _f64(dH)
+    sg = _sigmoid(G)
+    return dH * U * sg * (1.0 + G * (1.0 - sg)), dH * G * sg
+
+
+def swiglu_bwd(X, Wg, Wu, Ag, Au, Bg, Bu, dH, alpha: float, G=None, U=None):
+    """dX (summed over gate and up), dA [2, r, K], dB [2 I, r] (gate rows, then
+    up rows).  G, U: the pre-activations the backward starts from (default:
+    recomputed exactly)."""
+    if G is None or U is None:
+        _, G, U, _ = swiglu_fwd(X, Wg, Wu, Ag, Au, Bg, Bu, alpha)
+    dG, dU = swiglu_grad_gate_up(G, U, dH)
+    g = multi_linear_bwd(X, [Wg, Wu], [Ag, Au], [Bg, Bu], np.concatenate([dG, dU], axis=1), alpha)
+    return {"dX": g["dX"], "dA": g["dA"], "dB": g["dB"], "dG": dG, "dU": dU}
+

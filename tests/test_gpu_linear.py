@@ -136,3 +136,34 @@ def test_full_size_layer_sampled_rows(lib, wl_name, lin):
     check_f32(got["T"], ref["T_all"], "T")
     check_f32(got["dA"], ref["dA"], "dA")
     check_f32(got["dB"], ref["dB"], "dB")
+
+
+@pytest.mark.parametrize("shape", [(128, 64, 64, 8), (129, 64, 64, 8), (513, 128, 192, 8), (1, 64, 64, 64)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_edge_shapes(lib, shape):
+    """Smallest K and N (one decode line, one 64-wide chunk), the last size of
+    the one-CTA path (128 rows) and the first of the pair path (129), one row
+    past a 512-row pair tile, a single row at the largest rank."""
+    M, K, N, r = shape
+    inp = make(M, K, N, r, "nf4", True, seed=M + K + N + r)
+    check_all(inp, run_layer(inp), oracle_layer(inp))
+
+
+def test_zero_rows(lib):
+    """M = 0: the forward writes nothing; the backward sets dA and dB to zero."""
+    import torch
+
+    inp = make(64, 256, 320, 16, "q8_0", seed=3)
+    d = {k: lib.bf16_from_bits(inp[k]) for k in ("A", "B")}
+    w = lib.DeviceWeight.from_packed(inp["W"])
+    X = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    dY = torch.empty((0, 320), dtype=torch.bfloat16, device="cuda")
+    Y = torch.empty((0, 320), dtype=torch.bfloat16, device="cuda")
+    T = torch.empty((0, 16), dtype=torch.float32, device="cuda")
+    lib.linear_fwd(w, X, d["A"], d["B"], inp["alpha"], Y=Y, T=T)
+    dA = torch.full((16, 256), 5.0, device="cuda")
+    dB = torch.full((320, 16), 5.0, device="cuda")
+    lib.linear_bwd(w, X, d["A"], d["B"], T, dY, inp["alpha"], dA=dA, dB=dB, want_dx=False)
+    torch.cuda.synchronize()
+    assert lib.device_error() == 0
+    assert float(dA.abs().max()) == 0.0 and float(dB.abs().max()) == 0.0

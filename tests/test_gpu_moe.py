@@ -188,3 +188,18 @@ def test_moe_workload(lib, lin):
     dd = {"X": d["X"], "dY": d["dY"], "A": d["A"], "B": d["B"], "W": d["W"], "off": off, "alpha": d["alpha"],
           "r": d["rank"]}
     _check(dd, _run(lib, dd), _oracle(dd))
+
+
+def test_largest_expert_count(lib):
+    """256 experts (the limit), most with a handful of rows, some empty; 257
+    experts are rejected before anything is launched."""
+    import ctypes
+
+    rng = np.random.default_rng(21)
+    counts = rng.integers(0, 12, size=256)
+    counts[::17] = 0
+    d = _moe_inputs(list(counts), K=128, N=192, r=8, fmt="q4_0", seed=21)
+    _check(d, _run(lib, d), _oracle(d))
+    ws = [lib.DeviceWeight.from_packed(w) for w in d["W"]]
+    descs = (lib.WeightDesc * 257)(*([w.desc for w in ws] + [ws[0].desc]))
+    assert lib.load().qlora_grouped_workspace_bytes(descs, 257, int(counts.sum()), 8) == 0

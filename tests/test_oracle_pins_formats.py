@@ -266,3 +266,58 @@ def test_dq_map_pack_decode_error_bound():
     # value), then the decoded value is read back through bf16 (2^-9)
     assert np.all(np.abs(dec_amax - amax) <= 0.07 * np.abs(amax - p["absmax_offset"]) + 2.0 ** -8 * amax)
     assert np.abs(oracle.dequant(p) - x).max() < 0.25 * amax.max()
+
+
+# ---------------------------------------------------------------------------
+# gate / up with SwiGLU
+# ---------------------------------------------------------------------------
+def test_swiglu_hand_worked():
+    # G = [0, 2, -1], U = [3, 1, 2]: H = silu(G) U = [0, 2 s(2), -2 s(-1)]
+    G = np.array([[0.0, 2.0, -1.0]])
+    U = np.array([[3.0, 1.0, 2.0]])
+    dH = np.array([[1.0, 1.0, 0.5]])
+    dG, dU = oracle.swiglu_grad_gate_up(G, U, dH)
+    s = lambda x: 1.0 / (1.0 + np.exp(-x))  # noqa: E731
+    # d silu / dg at 0 is 1/2; at g: s(g) + g s(g) (1 - s(g))
+    assert dG[0, 0] == 1.5
+    assert np.isclose(dG[0, 1], 1.0 * (s(2.0) + 2.0 * s(2.0) * (1 - s(2.0))), rtol=1e-15)
+    assert np.isclose(dG[0, 2], 0.5 * 2.0 * (s(-1.0) - s(-1.0) * (1 - s(-1.0))), rtol=1e-15)
+    assert dU.tolist() == [[0.0, 2.0 * s(2.0), -0.5 * s(-1.0)]]
+
+
+def test_swiglu_gradients_by_finite_differences():
+    """<dH, H> is smooth in X, A, B: central differences (fp64) match the
+    analytic gradients of the oracle to ~1e-7 relative."""
+    rng = np.random.default_rng(14)
+    M, K, I, r = 3, 64, 8, 8
+    X = rng.standard_normal((M, K))
+    Wg, Wu = rng.standard_normal((I, K)) * 0.1, rng.standard_normal((I, K)) * 0.1
+    Ag, Au = rng.standard_normal((r, K)) * 0.1, rng.standard_normal((r, K)) * 0.1
+    Bg, Bu = rng.standard_normal((I, r)) * 0.1, rng.standard_normal((I, r)) * 0.1
+    dH = rng.standard_normal((M, I))
+    alpha = 4.0
+    g = oracle.swiglu_bwd(X, Wg, Wu, Ag, Au, Bg, Bu, dH, alpha)
+
+    def loss(X_=X, Ag_=Ag, Bu_=Bu):
+        H = oracle.swiglu_fwd(X_, Wg, Wu, Ag_, Au, Bg, Bu_, alpha)[0]
+        return float(np.sum(dH * H))
+
+    eps = 1e-5
+    for (i, j) in [(0, 3), (2, 40), (1, 63)]:
+        Xp, Xm = X.copy(), X.copy()
+        Xp[i, j] += eps
+        Xm[i, j] -= eps
+        fd = (loss(X_=Xp) - loss(X_=Xm)) / (2 * eps)
+        assert np.isclose(g["dX"][i, j], fd, rtol=1e-6, atol=1e-9)
+    for (i, j) in [(0, 0), (5, 17)]:
+        Ap, Am = Ag.copy(), Ag.copy()
+        Ap[i, j] += eps
+        Am[i, j] -= eps
+        fd = (loss(Ag_=Ap) - loss(Ag_=Am)) / (2 * eps)
+        assert np.isclose(g["dA"][0][i, j], fd, rtol=1e-6, atol=1e-9)
+    for (i, j) in [(2, 1), (7, 6)]:
+        Bp, Bm = Bu.copy(), Bu.copy()
+        Bp[i, j] += eps
+        Bm[i, j] -= eps
+        fd = (loss(Bu_=Bp) - loss(Bu_=Bm)) / (2 * eps)
+        assert np.isclose(g["dB"][I + i, j], fd, rtol=1e-6, atol=1e-9)
