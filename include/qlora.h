@@ -192,6 +192,34 @@ int32_t qlora_debug_linear_bwd_f32(const qlora_weight_desc* w, int64_t M, int32_
                                    float* dX32, float* dA, float* dB,
                                    void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- gate / up projections with the SwiGLU activation ------------------------
+ * The MLP input side of the Llama / Qwen3 layers: two LoRA linears over the
+ * same X (gate and up) fused as one call (see the fused projections below),
+ * with the activation H = silu(G) * U, silu(g) = g sigmoid(g), computed in
+ * the forward GEMM's epilogue from the fp32 accumulators (launches of more
+ * than 128 rows; an elementwise pass over G | U otherwise).
+ *   w: the two bases stacked by rows, [gate rows; up rows], N = 2 I with
+ *      I % 256 == 0; A: bf16 [2][rank][K] (gate, up); B: bf16 [2I][rank]
+ *      (gate rows, then up rows); 2 rank <= 64.
+ *   forward outputs: H bf16 [M][I]; GU bf16 [M][2I] = G | U (the
+ *      pre-activations, kept for the backward); T_save fp32 [M][2 rank].
+ *   backward: from dH bf16 [M][I] and GU, dG = dH U sigmoid(G) (1 + G (1 -
+ *      sigmoid(G))) and dU = dH silu(G) (fp32, stored bf16 in the
+ *      workspace), then the fused two-projection backward: dX bf16 [M][K]
+ *      (gate's and up's input gradients summed; may be NULL), dA fp32
+ *      [2][rank][K], dB fp32 [2I][rank].
+ *   workspace: qlora_swiglu_workspace_bytes (covers both calls). */
+size_t qlora_swiglu_workspace_bytes(const qlora_weight_desc* w, int64_t M, int32_t rank);
+int32_t qlora_swiglu_fwd(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha,
+                         const void* X, const void* A, const void* B,
+                         void* H, void* GU, float* T_save,
+                         void* workspace, size_t ws_bytes, void* stream);
+int32_t qlora_swiglu_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha,
+                         const void* X, const void* A, const void* B,
+                         const float* T_save, const void* GU, const void* dH,
+                         void* dX, float* dA, float* dB,
+                         void* workspace, size_t ws_bytes, void* stream);
+
 /* ---- fused projections that share their input ------------------------------
  * The P LoRA linears that read the same X in a decoder layer (q, k, v of the
  * attention block; gate and up of the MLP) as one call each way: one pass of

@@ -98,6 +98,9 @@ SIGNATURES = {
     "qlora_multi_linear_bwd": (_I32, [_WD, _I32, ctypes.POINTER(ctypes.c_int64), _I64, _I32, _F32, _P, _P, _P, _P,
                                       _P, _P, _P, _P, _P, _SZ, _P]),
     "qlora_noalloc_scratch_bytes": (_SZ, []),
+    "qlora_swiglu_workspace_bytes": (_SZ, [_WD, _I64, _I32]),
+    "qlora_swiglu_fwd": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "qlora_swiglu_bwd": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "qlora_forward_workspace_bytes": (_SZ, [_WD, _I64, _I32]),
     "qlora_debug_linear_fwd_f32": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "qlora_debug_linear_bwd_f32": (_I32, [_WD, _I64, _I32, _F32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -261,6 +264,49 @@ def debug_linear_bwd_f32(w: DeviceWeight, X, A, B, T, dY, alpha: float, workspac
                                            _ptr(T), _ptr(dY), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(workspace),
                                            workspace.numel(), _stream_ptr(stream))
     _check("qlora_debug_linear_bwd_f32", st)
+    return dX, dA, dB
+
+
+def swiglu_workspace_bytes(w: DeviceWeight, M: int, rank: int) -> int:
+    return int(load().qlora_swiglu_workspace_bytes(ctypes.byref(w.desc), int(M), int(rank)))
+
+
+def swiglu_fwd(w: DeviceWeight, X, A, B, alpha: float, H=None, GU=None, T=None, workspace=None, stream=None):
+    """Gate / up with SwiGLU over w = [gate rows; up rows]; A [2, r, K], B
+    [2I, r].  Returns (H [M, I], GU [M, 2I], T_save [M, 2r])."""
+    torch = _torch()
+    M, r, I = X.shape[0], A.shape[-2], w.N // 2
+    if H is None:
+        H = torch.empty((M, I), dtype=torch.bfloat16, device=X.device)
+    if GU is None:
+        GU = torch.empty((M, 2 * I), dtype=torch.bfloat16, device=X.device)
+    if T is None:
+        T = torch.empty((M, 2 * r), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(swiglu_workspace_bytes(w, M, r), X.device)
+    st = load().qlora_swiglu_fwd(ctypes.byref(w.desc), M, r, float(alpha), _ptr(X), _ptr(A), _ptr(B), _ptr(H),
+                                 _ptr(GU), _ptr(T), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check("qlora_swiglu_fwd", st)
+    return H, GU, T
+
+
+def swiglu_bwd(w: DeviceWeight, X, A, B, T, GU, dH, alpha: float, dX=None, dA=None, dB=None, workspace=None,
+               stream=None, want_dx: bool = True):
+    """Returns (dX [M, K] (summed over gate and up), dA [2, r, K], dB [2I, r])."""
+    torch = _torch()
+    M, r = X.shape[0], A.shape[-2]
+    if dX is None and want_dx:
+        dX = torch.empty((M, w.K), dtype=torch.bfloat16, device=X.device)
+    if dA is None:
+        dA = torch.empty((2, r, w.K), dtype=torch.float32, device=X.device)
+    if dB is None:
+        dB = torch.empty((w.N, r), dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = alloc_workspace(swiglu_workspace_bytes(w, M, r), X.device)
+    st = load().qlora_swiglu_bwd(ctypes.byref(w.desc), M, r, float(alpha), _ptr(X), _ptr(A), _ptr(B), _ptr(T),
+                                 _ptr(GU), _ptr(dH), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(workspace),
+                                 workspace.numel(), _stream_ptr(stream))
+    _check("qlora_swiglu_bwd", st)
     return dX, dA, dB
 
 

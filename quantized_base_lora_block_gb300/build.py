@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libqlora.so")
 BUILD = os.path.join(HERE, "_build")
 SOURCES = ["api.cu", "dequant.cu", "gemm_tc.cu", "gemm_pair.cu", "reduce.cu", "grouped.cu", "stream.cu", "noalloc.cu",
-           "diag.cu"]
+           "diag.cu", "swiglu.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -301,10 +301,15 @@ struct ProjSplit {
 // columns; with fused projections (forward, ps->P > 1) a tile's adapter chunk
 // takes the `rank` columns of its projection.
 // out_f32 (debug): when set, the fp32 accumulators are written there
-// ([M x n_out]) instead of bf16 to `out`.
+// ([M x n_out]) instead of bf16 to `out`.  swiglu_i > 0 (forward, a base of
+// [gate rows; up rows] with I rows each, fused as two projections): `out`
+// receives G | U and swiglu_h H = silu(G) U ([M x I]) — from the pair
+// kernel's epilogue, or for launches of at most 128 rows by an elementwise
+// pass over G | U.
 static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M, int rank, int la_cols,
                                   const ProjSplit* ps, const void* a_op, const void* la, const void* lb, void* out,
-                                  cudaStream_t st, float* out_f32 = nullptr) {
+                                  cudaStream_t st, float* out_f32 = nullptr, int64_t swiglu_i = 0,
+                                  void* swiglu_h = nullptr) {
   if (out_f32) out = out_f32;  // the bf16 store map is then built but never used
   const int64_t N = w->N, K = w->K;
   // pair tiles on an SM pair; short problems use one CTA per 128 x 256 tile
@@ -372,7 +377,19 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
     a.nproj = ps->P;
     for (int p = 0; p < ps->P; ++p) a.proj_end[p] = (int)ps->end[p];
   }
-  return gemm_launch(w->fmt, dx, pair, maps, a, st);
+  if (swiglu_i > 0 && pair) {
+    // one adapter chunk of both projections' columns; each CTA's B half is
+    // shifted onto its projection's columns in the kernel
+    a.swiglu_i = (int)swiglu_i;
+    a.swiglu_h = static_cast<__nv_bfloat16*>(swiglu_h);
+    a.rank = la_cols;
+    a.nproj = 0;
+  }
+  cudaError_t e = gemm_launch(w->fmt, dx, pair, maps, a, st);
+  if (e == cudaSuccess && swiglu_i > 0 && !pair)
+    e = launch_swiglu_act(static_cast<const __nv_bfloat16*>(out), static_cast<__nv_bfloat16*>(swiglu_h), M,
+                          swiglu_i, st);
+  return e;
 }
 
 
@@ -681,9 +698,12 @@ static size_t multi_workspace(const qlora_weight_desc* w, const ProjSplit& ps, i
 }
 
 // Y32 (debug): when set, Y is written there as fp32 instead of bf16 to Y.
+// H (gate / up with SwiGLU, two projections of I rows): Y receives G | U and
+// H = silu(G) U.
 static int32_t linear_fwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, int64_t M, int32_t rank,
                                float alpha, const void* X, const void* A, const void* B, void* Y, float* T_save,
-                               void* workspace, size_t ws_bytes, void* stream, float* Y32 = nullptr) {
+                               void* workspace, size_t ws_bytes, void* stream, float* Y32 = nullptr,
+                               void* H = nullptr) {
   if (M < 0 || !std::isfinite(alpha)) return QLORA_ERR_INVALID;
   if (M == 0) return QLORA_OK;
   if (M > (1ll << 31) - 256) return QLORA_ERR_UNSUPPORTED;
@@ -716,7 +736,8 @@ static int32_t linear_fwd_impl(const qlora_weight_desc* w, const ProjSplit& ps, 
   if (launch_row_reduce_fin(rt, Q, st) != cudaSuccess) return QLORA_ERR_CUDA;
 
   // 2) Y = X deq(W)^T + sT B^T, each tile's adapter chunk from its projection
-  return cuda_status(run_dense_gemm(w, false, M, rank, Q, &ps, X, sT, B, Y, st, Y32));
+  const int64_t swiglu_i = H ? ps.end[0] : 0;
+  return cuda_status(run_dense_gemm(w, false, M, rank, Q, &ps, X, sT, B, Y, st, Y32, swiglu_i, H));
 }
 
 // dX32 (debug): when set, dX is written there as fp32 instead of bf16 to dX.
@@ -844,6 +865,64 @@ int32_t qlora_linear_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, fl
   ProjSplit ps;
   ps.end[0] = w->N;
   return linear_bwd_impl(w, ps, M, rank, alpha, X, A, B, T_save, dY, dX, dA, dB, workspace, ws_bytes, stream);
+}
+
+// Gate / up with SwiGLU: the fused two-projection call over [gate rows; up
+// rows] with the activation in the forward's epilogue and its derivative in
+// an elementwise pass before the backward.
+static int validate_swiglu(const qlora_weight_desc* w, int32_t rank, ProjSplit& ps) {
+  int v = validate_weight(w);
+  if (v != QLORA_OK) return v;
+  if ((v = validate_rank(rank)) != QLORA_OK) return v;
+  if (w->N % 512) return QLORA_ERR_UNSUPPORTED;  // I = N/2 a multiple of 256
+  if (2 * rank > 64) return QLORA_ERR_UNSUPPORTED;
+  ps.P = 2;
+  ps.end[0] = w->N / 2;
+  ps.end[1] = w->N;
+  return QLORA_OK;
+}
+
+size_t qlora_swiglu_workspace_bytes(const qlora_weight_desc* w, int64_t M, int32_t rank) {
+  ProjSplit ps;
+  if (M < 0 || validate_swiglu(w, rank, ps) != QLORA_OK) return 0;
+  if (M == 0) return 256;
+  return round256((size_t)M * w->N * 2) + multi_workspace(w, ps, M, rank);
+}
+
+int32_t qlora_swiglu_fwd(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha, const void* X,
+                         const void* A, const void* B, void* H, void* GU, float* T_save, void* workspace,
+                         size_t ws_bytes, void* stream) {
+  ProjSplit ps;
+  const int v = validate_swiglu(w, rank, ps);
+  if (v != QLORA_OK) return v;
+  if (M > 0 && !H) return QLORA_ERR_INVALID;
+  if (H && !aligned16(H)) return QLORA_ERR_ALIGN;
+  return linear_fwd_impl(w, ps, M, rank, alpha, X, A, B, GU, T_save, workspace, ws_bytes, stream, nullptr, H);
+}
+
+int32_t qlora_swiglu_bwd(const qlora_weight_desc* w, int64_t M, int32_t rank, float alpha, const void* X,
+                         const void* A, const void* B, const float* T_save, const void* GU, const void* dH,
+                         void* dX, float* dA, float* dB, void* workspace, size_t ws_bytes, void* stream) {
+  ProjSplit ps;
+  const int v = validate_swiglu(w, rank, ps);
+  if (v != QLORA_OK) return v;
+  if (M < 0 || !std::isfinite(alpha)) return QLORA_ERR_INVALID;
+  if (M == 0) return linear_bwd_impl(w, ps, M, rank, alpha, X, A, B, T_save, nullptr, dX, dA, dB, workspace, ws_bytes,
+                                     stream);
+  if (!GU || !dH) return QLORA_ERR_INVALID;
+  if (!aligned16(GU) || !aligned16(dH)) return QLORA_ERR_ALIGN;
+  if (!workspace || ws_bytes < qlora_swiglu_workspace_bytes(w, M, rank)) return QLORA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return QLORA_ERR_ALIGN;
+  // dY = [dG | dU] in the workspace's head, the backward's own layout after it
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t dy_bytes = round256((size_t)M * w->N * 2);
+  __nv_bfloat16* dY = reinterpret_cast<__nv_bfloat16*>(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_swiglu_grad(static_cast<const __nv_bfloat16*>(GU), static_cast<const __nv_bfloat16*>(dH), dY, M,
+                         w->N / 2, st) != cudaSuccess)
+    return QLORA_ERR_CUDA;
+  return linear_bwd_impl(w, ps, M, rank, alpha, X, A, B, T_save, dY, dX, dA, dB, ws + dy_bytes,
+                         ws_bytes - dy_bytes, stream);
 }
 
 // Debug: the same calls with the GEMM output (Y, resp. dX) written as the

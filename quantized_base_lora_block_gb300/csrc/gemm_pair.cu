@@ -203,6 +203,13 @@ __device__ __forceinline__ void raw_box_coords(int bn, int kb, int32_t& x, int32
   }
 }
 
+// First weight row (forward) of this CTA's share of a tile's B.
+template <int CFG>
+__device__ __forceinline__ int64_t b_first_row(const GemmArgs& a, int n0, uint32_t rank) {
+  if (a.swiglu_i > 0) return (rank ? (int64_t)a.swiglu_i : 0) + n0 / 2;
+  return n0 + PairCfg<CFG>::HALF_N * (int)rank;
+}
+
 struct PairTile {
   int m0, n0;
   int rows;  // grouped: rows of the tile that belong to its expert (from m0)
@@ -328,7 +335,8 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       for (int lt = 0; lt < my_tiles; ++lt) {
         const PairTile tc = pair_tile<DX, CFG>(args, pair + lt * num_pairs);
         const int am = tc.m0 + 128 * (int)rank;     // this CTA's A rows (+256 per accumulator)
-        const int bn = tc.n0 + HALF_N * (int)rank;  // this CTA's half of B
+        // this CTA's half of B (forward: its first weight row; dX: first output column)
+        const int bn = DX ? tc.n0 + HALF_N * (int)rank : (int)b_first_row<CFG>(args, tc.n0, rank);
         for (int kb = 0; kb < nkb_total; ++kb, ++it) {
           const int s = it % P_STAGES;
           const uint32_t ph = (it / P_STAGES) & 1;
@@ -379,8 +387,11 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
             for (int a = 0; a < NACC; ++a)
               tma_load_2d_pair(sa + a * 16384, &tm_la, fb, adapter_col(args, tc.n0), am + 256 * a);
             if (!DX) {
-              if (GROUPED) tma_load_3d_pair(sb, &tm_lb, fb, 0, bn, tc.e);
-              else tma_load_2d_pair(sb, &tm_lb, fb, 0, bn);
+              // SwiGLU: CTA 1's rows of B land rank columns in, where the
+              // up projection's T sits in the adapter chunk (x < 0 is zero-filled)
+              const int lbx = args.swiglu_i > 0 ? -(args.rank / 2) * (int)rank : 0;  // rank = 2 r here
+              if (GROUPED) tma_load_3d_pair(sb, &tm_lb, fb, lbx, bn, tc.e);
+              else tma_load_2d_pair(sb, &tm_lb, fb, lbx, bn);
             } else {
 #pragma unroll
               for (int j = 0; j < HALF_N / 64; ++j) {
@@ -481,6 +492,51 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
         if (!ok) break;
         tc_fence_after();
         const int row0 = tc.m0 + 256 * a + 128 * (int)rank;
+        if (!DX && !GROUPED && args.swiglu_i > 0) {
+          // SwiGLU: TMEM columns [0, TN/2) hold gate, [TN/2, TN) the up
+          // values of the same output columns; 32 columns of each at a
+          // time, stored from registers: G, U (bf16) and H = silu(G) U
+          const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * (NACC * TN) + a * TN;
+          const int64_t row = row0 + row_in_tile;
+          const bool rok = row < args.M;
+          const int64_t I = args.swiglu_i;
+#pragma unroll 1
+          for (int c = 0; c < TN / 64; ++c) {
+            uint32_t gv[32], uv[32];
+            tmem_ld_32x32b_x32(tb + 32 * c, gv);
+            tmem_ld_32x32b_x32(tb + TN / 2 + 32 * c, uv);
+            tc_wait_ld();
+            if (c + 1 == TN / 64) {  // every value of this accumulator is in registers: release it
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&bars->acc_empty[buf * NACC + a]), 0));
+            }
+            const int64_t col = tc.n0 / 2 + 32 * c;  // gate / H column
+            if (rok && col < I) {
+              uint4* dg = reinterpret_cast<uint4*>(args.out + row * 2 * I + col);
+              uint4* du = reinterpret_cast<uint4*>(args.out + row * 2 * I + I + col);
+              uint4* dh = reinterpret_cast<uint4*>(args.swiglu_h + row * I + col);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                // H from G and U as stored (bf16), like the elementwise pass
+                float g[8], u[8], h[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  g[k] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(gv[8 * q + k])));
+                  u[k] = __bfloat162float(__float2bfloat16_rn(__uint_as_float(uv[8 * q + k])));
+                  h[k] = swiglu_h_f32(g[k], u[k]);
+                }
+                dg[q] = make_uint4(pack_bf16x2(g[0], g[1]), pack_bf16x2(g[2], g[3]), pack_bf16x2(g[4], g[5]),
+                                   pack_bf16x2(g[6], g[7]));
+                du[q] = make_uint4(pack_bf16x2(u[0], u[1]), pack_bf16x2(u[2], u[3]), pack_bf16x2(u[4], u[5]),
+                                   pack_bf16x2(u[6], u[7]));
+                dh[q] = make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]),
+                                   pack_bf16x2(h[6], h[7]));
+              }
+            }
+          }
+          continue;
+        }
         constexpr int NCH = TN / 64;
         const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + buf * (NACC * TN) + a * TN;
         uint32_t v[64];
@@ -610,7 +666,7 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       const PairTile tc = pair_tile<DX, CFG>(args, pair + c.lt * num_pairs);
       if constexpr (GROUPED) c.wv = &tab.w[tc.e];
       if (!DX) {
-        const int64_t row = tc.n0 + HALF_N * (int)rank + d;
+        const int64_t row = b_first_row<CFG>(args, tc.n0, rank) + d;
         c.row_ok = row < args.w_rows;
         c.base = row * args.w_lines_per_row;
       } else {
@@ -812,7 +868,8 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     bool ok = true;
     for (int lt = 0; lt < my_tiles && ok; ++lt) {
       const PairTile tc = pair_tile<DX, CFG>(args, pair + lt * num_pairs);
-      const int ncol = tc.n0 + HALF_N * (int)rank;  // forward: first weight row; dX: first output column
+      // forward: first weight row; dX: first output column
+      const int ncol = DX ? tc.n0 + HALF_N * (int)rank : (int)b_first_row<CFG>(args, tc.n0, rank);
       for (int kb = 0; kb < nkb_total; ++kb, ++it) {
         const uint32_t rs = it % Raw::STAGES;
         if (!mbar_wait(smem_u32(&bars->raw_empty[rs]), ((it / Raw::STAGES) & 1) ^ 1, abort, args.err)) {

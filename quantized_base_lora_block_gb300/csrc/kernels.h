@@ -168,6 +168,19 @@ struct GroupedSched {
   int4* rows64;
   int2* ranges;
 };
+// Gate / up with SwiGLU, elementwise parts (swiglu.cu): H = silu(G) U from
+// GU = [G | U] ([M x 2I] bf16), and dY = [dG | dU] from dH and GU.
+// swiglu_h_f32 takes G and U as stored (bf16 values) and is the one formula
+// both the pair GEMM's epilogue and swiglu_act_kernel use, so that H does not
+// depend on which of the two computed it.
+__device__ __forceinline__ float swiglu_sigmoid_f32(float g) { return 1.0f / (1.0f + __expf(-g)); }
+__device__ __forceinline__ float swiglu_h_f32(float g_bf16, float u_bf16) {
+  return g_bf16 * swiglu_sigmoid_f32(g_bf16) * u_bf16;
+}
+cudaError_t launch_swiglu_act(const __nv_bfloat16* GU, __nv_bfloat16* H, int64_t M, int64_t I, cudaStream_t st);
+cudaError_t launch_swiglu_grad(const __nv_bfloat16* GU, const __nv_bfloat16* dH, __nv_bfloat16* dY, int64_t M,
+                               int64_t I, cudaStream_t st);
+
 cudaError_t launch_grouped_schedule(const int32_t* offsets, int E, int64_t M_total, int tile_rows, int nblk_f,
                                     int nblk_d, const GroupedSched& s, int* err, cudaStream_t st);
 
@@ -211,6 +224,15 @@ struct GemmArgs {
   int n_fastest;         // pair kernel tile order: 1 = output column blocks fastest
   int raw_on;            // pair kernel: quantised bytes through the TMA raw ring (maps.w / maps.aq)
   int raw_dq;            // pair kernel, NF4 dX: absmax codes and group scales through the raw ring
+  // Gate / up with SwiGLU (forward, pair kernel): swiglu_i = I > 0 reads the
+  // base as [gate rows; up rows] (N = 2I) and gives each tile's CTA 0 the
+  // gate rows and CTA 1 the matching up rows (columns n0/2 .. of each), so a
+  // tile holds gate and up of the same columns; the epilogue writes G | U
+  // to `out` ([M x 2I]) and H = silu(G) U to `swiglu_h` ([M x I]).  The
+  // adapter chunk takes all 2 rank columns of sT; CTA 1's B box is shifted
+  // by rank columns so each half meets its own T.
+  int swiglu_i;
+  __nv_bfloat16* swiglu_h;
   // Fused projections (forward): projection p owns output columns
   // [proj_end[p-1], proj_end[p]) and adapter columns [p rank, (p+1) rank) of
   // the adapter A operand; a tile never spans two projections.  nproj <= 1:
