@@ -520,6 +520,57 @@ def unit_of_linear(d):
             "dB": d["dB"]}
 
 
+def swiglu_leg(q, torch, units, wl, steps, stream):
+    """gate|up of the layer with the SwiGLU activation (H = silu(G) U in the
+    GEMM epilogue, its derivative in an elementwise pass before the fused
+    backward) against the same fused unit without it, on the same weights;
+    dH is the gate block of the unit's dY.  Every launch on `stream`."""
+    u = next((u for u in units if u["name"] == "gate_proj|up_proj"), None)
+    if u is None or u["Ns"][0] != u["Ns"][1]:
+        return None
+    M, r, alpha, I = wl.M, wl.rank, wl.alpha, u["Ns"][0]
+    ws = q.alloc_workspace(q.swiglu_workspace_bytes(u["W"], M, r), u["X"].device)
+    H = torch.empty((M, I), dtype=torch.bfloat16, device=u["X"].device)
+    GU, T = torch.empty_like(u["Y"]), torch.empty_like(u["T"])
+    dH = u["dY"][:, :I].contiguous()
+
+    def plain():
+        q.multi_linear_fwd(u["W"], u["Ns"], u["X"], u["A"], u["B"], alpha, Y=u["Y"], T=u["T"], workspace=ws,
+                           stream=stream)
+        q.multi_linear_bwd(u["W"], u["Ns"], u["X"], u["A"], u["B"], u["T"], u["dY"], alpha, dX=u["dX"],
+                           dA=u["dA"], dB=u["dB"], workspace=ws, stream=stream)
+
+    def act():
+        q.swiglu_fwd(u["W"], u["X"], u["A"], u["B"], alpha, H=H, GU=GU, T=T, workspace=ws, stream=stream)
+        q.swiglu_bwd(u["W"], u["X"], u["A"], u["B"], T, GU, dH, alpha, dX=u["dX"], dA=u["dA"], dB=u["dB"],
+                     workspace=ws, stream=stream)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    ms_plain, ms_act = timed(plain), timed(act)
+    assert q.device_error() == 0, "device error in the SwiGLU leg"
+    flops = sum(syn.linear_flops(M, u["K"], n, r) for n in u["Ns"])
+    # elementwise derivative: reads G, U, dH, writes dG, dU (bf16); the
+    # epilogue adds the H store
+    grad_bytes = 10 * M * I
+    return {"unit": "gate_proj|up_proj + SwiGLU", "M": M, "I": I, "K": u["K"], "rank": r,
+            "ms_fwd_bwd": ms_act, "ms_fwd_bwd_without_activation": ms_plain,
+            "tflops": flops / (ms_act / 1e3) / 1e12,
+            "activation_overhead_us": 1e3 * (ms_act - ms_plain),
+            "derivative_pass_bytes": grad_bytes,
+            "note": "the overhead is the derivative pass plus the H store in the epilogue"}
+
+
 def config_leg(q, torch, name, steps, dev):
     """The layer step of another configuration (fused launches where the
     fused call supports them), timed on its own: ms per step, tokens/s,
@@ -853,6 +904,9 @@ def main():
     if rank == 0 and not args.no_context:
         deq_res = dequant_leg(q, torch, L, wl, peaks)
         lib_res = library_leg(q, torch, L, wl, 5)
+    swiglu_res = None
+    if rank == 0 and not args.no_context:
+        swiglu_res = swiglu_leg(q, torch, units, wl, 10, stream)
     cfg_res = None
     if not args.no_configs and rank == 0:
         cfg_res = [config_leg(q, torch, name, 10, dev)
@@ -888,7 +942,7 @@ def main():
                        "met": flops_step / t_step / 1e12 >= 0.6 * NOMINAL_BF16_TFLOPS},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clk, "stream": stream_res, "moe": moe_res, "configs": cfg_res,
-            "dequant_blocks": deq_res, "library_baseline": lib_res,
+            "dequant_blocks": deq_res, "library_baseline": lib_res, "swiglu": swiglu_res,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
