@@ -956,8 +956,16 @@ static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, c
   }
   // grouped: num_tiles is the schedule's upper bound (the count itself is on
   // the device)
-  const int pairs = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
+  int pairs = args.num_tiles < max_clusters ? args.num_tiles : max_clusters;
   if (pairs <= 0) return cudaSuccess;
+  if constexpr (!GROUPED) {
+    // the fewest pairs that finish the tiles in the same number of rounds
+    // (e.g. 128 tiles: 64 pairs, two rounds each, instead of 76 of which
+    // 24 would idle through the second); the SMs left free take the work
+    // launched beside the GEMM (the backward's dA / dB reduction)
+    const int rounds = (args.num_tiles + pairs - 1) / pairs;
+    pairs = (args.num_tiles + rounds - 1) / rounds;
+  }
   cfg.gridDim = dim3(2 * pairs);
   cfg.numAttrs = 2;
   if constexpr (GROUPED) {
