@@ -173,7 +173,7 @@ struct GroupedSched {
 // swiglu_h_f32 takes G and U as stored (bf16 values) and is the one formula
 // both the pair GEMM's epilogue and swiglu_act_kernel use, so that H does not
 // depend on which of the two computed it.
-__device__ __forceinline__ float swiglu_sigmoid_f32(float g) { return 1.0f / (1.0f + __expf(-g)); }
+__device__ __forceinline__ float swiglu_sigmoid_f32(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 __device__ __forceinline__ float swiglu_h_f32(float g_bf16, float u_bf16) {
   return g_bf16 * swiglu_sigmoid_f32(g_bf16) * u_bf16;
 }
