@@ -52,11 +52,11 @@ def parse_args():
     p.add_argument("--no-moe", action="store_true", help="skip the grouped MoE leg")
     p.add_argument("--no-context", action="store_true",
                    help="skip the dequant_blocks GB/s and library-composition baseline legs")
-    p.add_argument("--case", default=None, choices=["gemm_m128", "dequant", "linear_m4096"],
+    p.add_argument("--case", default=None, choices=["gemm_m128", "dequant", "linear_m4096", "swiglu"],
                    help="run one small case of a kernel family --steps times and print its time (for profiling): "
                         "gemm_m128 = Llama gate fwd+bwd at 128 rows (one-CTA GEMM), dequant = dequant_blocks of "
                         "the Llama gate base, linear_m4096 = Llama gate fwd+bwd at 4096 rows (reductions and pair "
-                        "GEMM)")
+                        "GEMM), swiglu = Llama gate|up with SwiGLU fwd+bwd at 4096 rows")
     p.add_argument("--only-moe", action="store_true",
                    help="run the grouped MoE leg alone and print its result (for profiling)")
     p.add_argument("--no-configs", action="store_true",
@@ -443,13 +443,25 @@ def run_case(args):
 
     q.load()
     wl = syn.WORKLOADS["llama31_8b_nf4dq"]
-    M = {"gemm_m128": 128, "dequant": 1, "linear_m4096": 4096}[args.case]
+    M = {"gemm_m128": 128, "dequant": 1, "linear_m4096": 4096, "swiglu": 4096}[args.case]
     gate = [i for i, l in enumerate(wl.linears) if l.name == "gate_proj"][0]
     inp = syn.make_linear_inputs(wl, gate, seed=0, M=M)
     w = q.DeviceWeight.from_packed(inp["W"])
     X, A, B, dY = (q.bf16_from_bits(inp[k]) for k in ("X", "A", "B", "dY"))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if args.case == "dequant":
+    if args.case == "swiglu":
+        up = [i for i, l in enumerate(wl.linears) if l.name == "up_proj"][0]
+        inu = syn.make_linear_inputs(wl, up, seed=0, M=M)
+        w = q.DeviceWeight.from_packed(q.stack_weights([inp["W"], inu["W"]]))
+        A = q.bf16_from_bits(np.stack([inp["A"], inu["A"]]))
+        B = q.bf16_from_bits(np.concatenate([inp["B"], inu["B"]], axis=0))
+        ws = q.alloc_workspace(q.swiglu_workspace_bytes(w, M, wl.rank))
+        H, GU, T = q.swiglu_fwd(w, X, A, B, wl.alpha, workspace=ws)
+
+        def f():
+            q.swiglu_fwd(w, X, A, B, wl.alpha, H=H, GU=GU, T=T, workspace=ws)
+            q.swiglu_bwd(w, X, A, B, T, GU, dY, wl.alpha, workspace=ws)
+    elif args.case == "dequant":
         out = torch.empty((w.N, w.K), dtype=torch.bfloat16, device="cuda")
         f = lambda: q.dequant_blocks(w, out=out)  # noqa: E731
     else:
