@@ -709,13 +709,16 @@ def main():
         d["ws"] = ws
     stream = torch.cuda.current_stream(dev)
 
-    def step_units(us):
+    def step_units_on(us, st):
         for u in us:
             q.multi_linear_fwd(u["W"], u["Ns"], u["X"], u["A"], u["B"], alpha, Y=u["Y"], T=u["T"], workspace=ws,
-                               stream=stream)
+                               stream=st)
         for u in reversed(us):
             q.multi_linear_bwd(u["W"], u["Ns"], u["X"], u["A"], u["B"], u["T"], u["dY"], alpha, dX=u["dX"],
-                               dA=u["dA"], dB=u["dB"], workspace=ws, stream=stream)
+                               dA=u["dA"], dB=u["dB"], workspace=ws, stream=st)
+
+    def step_units(us):
+        step_units_on(us, stream)
 
     def step():
         step_units(units)
@@ -743,6 +746,28 @@ def main():
     torch.cuda.synchronize()
     launches = q.launch_count() - n0
     ms = e0.elapsed_time(e1)
+    # The same step captured once as a CUDA graph (the calls enqueue only
+    # device work, so they capture as they are) and replayed K times.
+    graph_res = None
+    try:
+        cap = torch.cuda.Stream(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            step_units_on(units, cap)
+        g.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        ms_graph = g0.elapsed_time(g1) / args.steps
+        graph_res = {"ms_per_step": ms_graph, "value": M / (ms_graph / 1e3) * world, "unit": "tokens/s",
+                     "note": "the step's calls captured once as a CUDA graph and replayed (same kernels)"}
+        del g
+    except Exception as e:  # capture is an extra, the headline pass above stands
+        graph_res = {"error": str(e)[:200]}
     # The same K steps again with CUDA events around every fused-GEMM launch
     # (on the stream it is launched on) for the kernel's own time.  Those
     # events lengthen a step by ~3.6%, so the headline pass above runs
@@ -954,7 +979,7 @@ def main():
                        "met": flops_step / t_step / 1e12 >= 0.6 * NOMINAL_BF16_TFLOPS},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clk, "stream": stream_res, "moe": moe_res, "configs": cfg_res,
-            "dequant_blocks": deq_res, "library_baseline": lib_res, "swiglu": swiglu_res,
+            "dequant_blocks": deq_res, "library_baseline": lib_res, "swiglu": swiglu_res, "graph": graph_res,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
