@@ -799,6 +799,18 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
           }
         }
       }
+      // NF4 dX: decode in registers before waiting for the slot, so the
+      // arithmetic overlaps the wait and only the stores follow the slot's
+      // release (in place, the slot is free once its bytes are; elsewhere the
+      // extra live registers spill)
+      constexpr bool EARLY = DX && !Raw::INPLACE && FMT == FMT_NF4;
+      uint4 out[8];
+      if constexpr (EARLY) {
+        if (ok && valid && c.kb < nkb) {
+          if (dq_cache) resolve_dq(r);
+          decode_line<FMT>(r, *c.wv, out);
+        }
+      }
       if (lane == 0 && ok) ok = mbar_wait_cluster(smem_u32(&bars->empty[s]), ph ^ 1, abort, args.err);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       // in place: every line of the group has been read before any decoded
@@ -808,9 +820,10 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
       if (c.kb < nkb) {
         const uint32_t dst = sB0 + s * P_B_BYTES + soff;
         if (valid) {
-          if (dq_cache) resolve_dq(r);
-          uint4 out[8];
-          decode_line<FMT>(r, *c.wv, out);
+          if constexpr (!EARLY) {
+            if (dq_cache) resolve_dq(r);
+            decode_line<FMT>(r, *c.wv, out);
+          }
 #pragma unroll
           for (int q = 0; q < 8; ++q) sts_v4(dst + ((q ^ swz) << 4), out[q]);
         } else {
