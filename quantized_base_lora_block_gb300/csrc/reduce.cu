@@ -265,11 +265,23 @@ __global__ void __launch_bounds__(NTHR) rr_fin_kernel(const RowReduce jb) {
 // half); result out[j][q], or out[q][j] when transposed, = scale (sum hi +
 // sum lo).
 // ---------------------------------------------------------------------------
+// Threads of the column reduction: for wide adapter chunks (Q >= 48, a
+// multiple of 16) 8 warps, warp w taking columns 16 (w % 4) .. of the tile
+// and half w / 4 of the 2Q (measured: Qwen3-0.6B q|k|v backward 145 vs
+// 151 us); else 4 warps with all 2Q each (8 warps of 16 S columns made the
+// Q = 16 launches slower: each warp repeats the tile's transposed loads).
 template <int Q>
-__global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const ColReduce jbb) {
+constexpr int cr_threads() {
+  return (Q % 16 == 0 && Q >= 48) ? 2 * NTHR : NTHR;
+}
+
+template <int Q>
+__global__ void __launch_bounds__(cr_threads<Q>()) cr_fin_kernel(const ColReduce ja, const ColReduce jbb) {
   constexpr int NS = kColStages;
   constexpr int Q2 = 2 * Q;
   constexpr int SP = Q2 + 8;
+  constexpr int CT = cr_threads<Q>();       // threads of this CTA
+  constexpr int QH = CT == NTHR ? Q2 : Q;   // S columns per warp
   extern __shared__ __align__(128) uint8_t cr_smem[];
   __nv_bfloat16* sL = reinterpret_cast<__nv_bfloat16*>(cr_smem);  // NS x [64 x 72]
   __nv_bfloat16* sS = sL + NS * TP * LPITCH;                         // NS x [64 x (2Q + 8)]
@@ -315,22 +327,24 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
     __nv_bfloat16* dL = sL + buf * TP * LPITCH;
     __nv_bfloat16* dS = sS + buf * TP * SP;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int piece = tid + i * NTHR;
+    for (int i = 0; i < 512 / CT; ++i) {  // 64 x 64 tile = 512 16-byte pieces
+      const int piece = tid + i * CT;
       const int r = piece >> 3, c8 = (piece & 7) * 8;
       const bool ok = (pp + r) < p_end;
       cp_async16(s_addr(dL + r * LPITCH + c8), L + (ok ? (pp + r) : 0) * J + j0 + c8, ok);
     }
-    for (int piece = tid; piece < TP * (Q2 / 8); piece += NTHR) {  // 64 rows x 2Q bf16
+    for (int piece = tid; piece < TP * (Q2 / 8); piece += CT) {  // 64 rows x 2Q bf16
       const int r = piece / (Q2 / 8), c8 = (piece % (Q2 / 8)) * 8;
       const bool ok = (pp + r) < p_end;
       cp_async16(s_addr(dS + r * SP + c8), S2 + (ok ? (pp + r) : 0) * Q2 + c8, ok);
     }
   };
 
-  float acc[Q2 / 8][4];
+  const int wj = warp & 3;                          // 16-column group of the tile
+  const int qbase = CT == NTHR ? 0 : (warp >> 2) * QH;  // first S column of this warp
+  float acc[QH / 8][4];
 #pragma unroll
-  for (int t = 0; t < Q2 / 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+  for (int t = 0; t < QH / 8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 
 #pragma unroll
   for (int s = 0; s < NS - 1; ++s) {
@@ -354,15 +368,15 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
       {  // A = L^T (m = j, k = p) from the [p][j] tile, transposed load
         const int i = lane >> 3;
         const int p = kk * 16 + (i >> 1) * 8 + (lane & 7);
-        const int j = warp * 16 + (i & 1) * 8;
+        const int j = wj * 16 + (i & 1) * 8;
         ldsm_x4_t(s_addr(tL + p * LPITCH + j), a[0], a[1], a[2], a[3]);
       }
 #pragma unroll
-      for (int nt = 0; nt < Q2 / 8; nt += 2) {  // Q2 is a multiple of 16
+      for (int nt = 0; nt < QH / 8; nt += 2) {  // QH is a multiple of 16
         uint32_t b0, b1, b2, b3;
         const int i = lane >> 3;
         const int p = kk * 16 + (i & 1) * 8 + (lane & 7);
-        const int q = nt * 8 + (i >> 1) * 8;
+        const int q = qbase + nt * 8 + (i >> 1) * 8;
         ldsm_x4_t(s_addr(tS + p * SP + q), b0, b1, b2, b3);
         mma_bf16_16816(acc[nt], a, b0, b1);
         mma_bf16_16816(acc[nt + 1], a, b2, b3);
@@ -377,9 +391,9 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
   {
     const int g = lane >> 2, t4 = lane & 3;
 #pragma unroll
-    for (int nt = 0; nt < Q2 / 8; ++nt) {
-      const int q = nt * 8 + 2 * t4;
-      const int r0 = warp * 16 + g;
+    for (int nt = 0; nt < QH / 8; ++nt) {
+      const int q = qbase + nt * 8 + 2 * t4;
+      const int r0 = wj * 16 + g;
       *reinterpret_cast<float2*>(sP + r0 * Q2 + q) = make_float2(acc[nt][0], acc[nt][1]);
       *reinterpret_cast<float2*>(sP + (r0 + 8) * Q2 + q) = make_float2(acc[nt][2], acc[nt][3]);
     }
@@ -395,7 +409,7 @@ __global__ void __launch_bounds__(NTHR) cr_fin_kernel(const ColReduce ja, const 
   int qoff = 0;
   if (jb.win > 0)
     for (int p = 0; p + 1 < jb.nproj; ++p) qoff += j0 >= jb.proj_end[p] ? jb.win : 0;
-  for (int it = (int)rank * NTHR + tid; it < TJ * (QW / 4); it += (int)splits * NTHR) {
+  for (int it = (int)rank * CT + tid; it < TJ * (QW / 4); it += (int)splits * CT) {
     int jj, q;
     if (jb.transposed) {  // out[q][j]: consecutive items along j
       q = (it / TJ) * 4;
@@ -503,7 +517,7 @@ cudaError_t launch_pack_adapters(const AdapterPack& ap, int64_t N, int64_t K, __
 // shared-memory limit.
 template <typename... Args>
 static cudaError_t launch_clustered(void (*kern)(Args...), dim3 grid, size_t smem, int splits, cudaStream_t st,
-                                    bool& attr_done, Args... args) {
+                                    bool& attr_done, int threads, Args... args) {
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess)
@@ -520,7 +534,7 @@ static cudaError_t launch_clustered(void (*kern)(Args...), dim3 grid, size_t sme
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(NTHR);
+  cfg.blockDim = dim3((unsigned)threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -536,8 +550,8 @@ static cudaError_t launch_rr_fin_q(const RowReduce& r, cudaStream_t st) {
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   if (r.sp.splits > kMaxClusterSplits) return cudaErrorInvalidValue;
   static bool attr_qj = false, attr_jq = false;
-  if (r.s_qj) return launch_clustered(rr_fin_kernel<Q, true>, grid, smem, r.sp.splits, st, attr_qj, r);
-  return launch_clustered(rr_fin_kernel<Q, false>, grid, smem, r.sp.splits, st, attr_jq, r);
+  if (r.s_qj) return launch_clustered(rr_fin_kernel<Q, true>, grid, smem, r.sp.splits, st, attr_qj, NTHR, r);
+  return launch_clustered(rr_fin_kernel<Q, false>, grid, smem, r.sp.splits, st, attr_jq, NTHR, r);
 }
 
 template <int Q>
@@ -548,7 +562,7 @@ static cudaError_t launch_cr_fin_q(const ColReduce& a, const ColReduce& b, cudaS
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   if (a.sp.splits > kMaxClusterSplits || (b.tiles > 0 && b.sp.splits != a.sp.splits)) return cudaErrorInvalidValue;
   static bool attr = false;
-  return launch_clustered(cr_fin_kernel<Q>, grid, smem, a.sp.splits, st, attr, a, b);
+  return launch_clustered(cr_fin_kernel<Q>, grid, smem, a.sp.splits, st, attr, cr_threads<Q>(), a, b);
 }
 
 #define QLORA_RANK_DISPATCH_FIN(FN, ...)     \
