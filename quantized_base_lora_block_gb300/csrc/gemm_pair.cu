@@ -596,6 +596,31 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
             }
             continue;
           }
+          if constexpr (Raw::OUT_BUFS == 1 && !DX) {
+            if (args.direct_out) {
+              // rows stored straight from registers, without the staging
+              // tile and the TMA store (chosen by the host for forward
+              // outputs of at most 4096 columns, where it measured faster)
+              if (store && row0 + row_in_tile < args.M) {
+                uint4* dst =
+                    reinterpret_cast<uint4*>(args.out + (int64_t)(row0 + row_in_tile) * args.n_out + tc.n0 + 64 * c);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                  const uint32_t* w = v + 8 * q;
+                  dst[q] = make_uint4(pack_bf16x2(__uint_as_float(w[0]), __uint_as_float(w[1])),
+                                      pack_bf16x2(__uint_as_float(w[2]), __uint_as_float(w[3])),
+                                      pack_bf16x2(__uint_as_float(w[4]), __uint_as_float(w[5])),
+                                      pack_bf16x2(__uint_as_float(w[6]), __uint_as_float(w[7])));
+                }
+              }
+              if (!last) {
+                tmem_ld_32x32b_x32(tcol + 64 * (c + 1), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                tmem_ld_32x32b_x32(tcol + 64 * (c + 1) + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                tc_wait_ld();
+              }
+              continue;
+            }
+          }
           const uint32_t stile = sOut + (nstored % Raw::OUT_BUFS) * P_STAGE_OUT_BYTES;
           if (store) {
             ++nstored;
