@@ -257,7 +257,7 @@ __device__ __forceinline__ PairTile pair_tile(const GemmArgs& a, int t) {
 // with its expert's weight view (tab) and adapter (3-D adapter and bf16
 // weight maps, expert index outermost); a pair CTA's 128-row block may hold
 // fewer rows of its expert, which are stored without the staging tile.
-template <int FMT, bool DX, int CFG, bool GROUPED>
+template <int FMT, bool DX, int CFG, bool GROUPED, bool DIRECT = false>
 __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     qgemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_w,
                       const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_lb,
@@ -596,8 +596,8 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
             }
             continue;
           }
-          if constexpr (Raw::OUT_BUFS == 1 && !DX) {
-            if (args.direct_out) {
+          if constexpr (DIRECT || (Raw::OUT_BUFS == 1 && !DX)) {
+            if (DIRECT || args.direct_out) {
               // rows stored straight from registers, without the staging
               // tile and the TMA store (chosen by the host for forward
               // outputs of at most 4096 columns, where it measured faster)
@@ -964,10 +964,10 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
 }
 
 // ---------------------------------------------------------------------------
-template <int FMT, bool DX, int CFG, bool GROUPED>
+template <int FMT, bool DX, int CFG, bool GROUPED, bool DIRECT = false>
 static cudaError_t launch_pair_one(const GemmMaps& maps, const GemmArgs& args, const GroupTable* tab,
                                    cudaStream_t st) {
-  auto kern = qgemm_pair_kernel<FMT, DX, CFG, GROUPED>;
+  auto kern = qgemm_pair_kernel<FMT, DX, CFG, GROUPED, DIRECT>;
   constexpr size_t P_SMEM_BYTES = p_smem_bytes<FMT, CFG, DX>();
   static int max_clusters = -1;  // per instantiation
   cudaLaunchConfig_t cfg = {};
@@ -1048,6 +1048,12 @@ static cudaError_t launch_quant(int fmt, bool dx, const GemmMaps& maps, const Ge
                                 cudaStream_t st) {
   switch (fmt) {
     case FMT_NF4:
+      if constexpr (CFG == 3 && !G) {
+        // dX with outputs of at most 4096 columns: its own instantiation
+        // storing rows from registers (a run-time choice inside one kernel
+        // made every dX launch slower)
+        if (dx && args.direct_out) return launch_pair_one<FMT_NF4, true, CFG, G, true>(maps, args, tab, st);
+      }
       return dx ? launch_pair_one<FMT_NF4, true, CFG, G>(maps, args, tab, st)
                 : launch_pair_one<FMT_NF4, false, CFG, G>(maps, args, tab, st);
     case FMT_Q8_0:
