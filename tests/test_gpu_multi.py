@@ -69,6 +69,18 @@ def test_three_projections(lib, fmt, dq, M):
     check_f32(got["dB"], ref["dB"], "dB")
 
 
+@pytest.mark.parametrize("Ns,r", [([256, 512, 256], 8), ([256, 256], 24), ([512, 256], 32), ([256, 256, 256], 16)])
+def test_projection_windows(lib, Ns, r):
+    """dB of each projection uses only that projection's columns of T: ranks
+    whose windows are not aligned to 16 columns (8, 24) and adapter chunks of
+    up to 64 columns, on 64-column tiles of dY."""
+    d = make_multi(300, 256, Ns, r, "q8_0", False, seed=r)
+    got, ref = run_multi(lib, d), oracle_multi(d)
+    check_bf16(got["dX"], ref["dX"], "dX")
+    check_f32(got["dA"], ref["dA"], "dA")
+    check_f32(got["dB"], ref["dB"], "dB")
+
+
 def test_one_projection_is_the_single_linear(lib):
     """P = 1 runs the same kernels as qlora_linear_fwd / _bwd: bitwise equal."""
     from gpu_helpers import run_layer
