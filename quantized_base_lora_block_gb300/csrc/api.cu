@@ -371,11 +371,6 @@ static cudaError_t run_dense_gemm(const qlora_weight_desc* w, bool dx, int64_t M
   // registers: measured on the Llama layer, o and down forward 2-5 % and
   // gate|up dX 2 % faster that way, wider outputs 1-4 % slower
   a.direct_out = (pair == 2 || (pair == 3 && w->fmt == QLORA_FMT_NF4)) && a.n_out <= 4096 ? 1 : 0;
-  // Every caller launches, right before this GEMM, the row reduction that
-  // writes the adapter operand (sT or sU) and nothing else this GEMM reads;
-  // that reduction waits for its own predecessors before it lets this GEMM
-  // start, so only the adapter chunk has to wait for it.
-  a.late_dep = 1;
   // Tile order.  Forward: row blocks fastest while the activation fits in L2
   // next to the streamed weight slabs (measured: gate 133 MB of DRAM traffic
   // this way vs 234 MB the other way); beyond ~64 MB (e.g. the 14336-wide

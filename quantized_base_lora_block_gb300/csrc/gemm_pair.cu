@@ -319,13 +319,9 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
   // launched with programmatic stream serialisation: the set-up above
-  // overlaps the previous kernel's tail, and the next kernel may start its
-  // own set-up.  Nothing global is touched before the previous kernel has
-  // finished, except with late_dep: then that kernel wrote only the adapter
-  // operands, so the base chunks (activation, weights) run beside its tail
-  // and the producer waits for it before its first adapter-chunk copy.
-  const bool late_dep = !GROUPED && has_lora && args.late_dep;
-  if (!late_dep) griddep_wait();
+  // overlaps the previous kernel's tail; nothing global is touched before it
+  // has finished, and the next kernel may start its own set-up
+  griddep_wait();
   griddep_launch_dependents();
   // grouped: the tile count comes from the schedule kernel (earlier in the
   // stream, complete once griddep_wait returned)
@@ -336,7 +332,6 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
-      bool dep_done = !late_dep;
       for (int lt = 0; lt < my_tiles; ++lt) {
         const PairTile tc = pair_tile<DX, CFG>(args, pair + lt * num_pairs);
         const int am = tc.m0 + 128 * (int)rank;     // this CTA's A rows (+256 per accumulator)
@@ -347,10 +342,6 @@ __global__ void __launch_bounds__(p_threads<FMT, CFG>(), 1)
           const uint32_t ph = (it / P_STAGES) & 1;
           if (!mbar_wait_cluster(smem_u32(&bars->empty[s]), ph ^ 1, abort, args.err)) goto producer_done;
           const bool lora = kb == nkb;
-          if (lora && !dep_done) {  // the adapter operand is the previous kernel's output
-            griddep_wait();
-            dep_done = true;
-          }
           const uint32_t sa = sA0 + s * P_A_BYTES, sb = sB0 + s * P_B_BYTES;
           const uint32_t bytes = P_A_BYTES + ((FMT == FMT_BF16 || lora) ? P_B_BYTES : 0);
           // CTA 0 expects both CTAs' bytes; every copy completes on CTA 0's barrier

@@ -225,10 +225,6 @@ struct GemmArgs {
   int raw_on;            // pair kernel: quantised bytes through the TMA raw ring (maps.w / maps.aq)
   int raw_dq;            // pair kernel, NF4 dX: absmax codes and group scales through the raw ring
   int direct_out;        // pair kernel with one staging tile: bf16 rows stored from registers
-  // pair kernel, dense: the kernel just before this one in the stream writes
-  // only the adapter operands and starts this one only after waiting for its
-  // own predecessors, so only the adapter chunk's copies wait for it
-  int late_dep;
   // Gate / up with SwiGLU (forward, pair kernel): swiglu_i = I > 0 reads the
   // base as [gate rows; up rows] (N = 2I) and gives each tile's CTA 0 the
   // gate rows and CTA 1 the matching up rows (columns n0/2 .. of each), so a
