@@ -285,6 +285,23 @@ def test_swiglu_hand_worked():
     assert dU.tolist() == [[0.0, 2.0 * s(2.0), -0.5 * s(-1.0)]]
 
 
+def test_swiglu_forward_hand_worked():
+    # K = 1 and B = 0 (the adapters add nothing): G = X Wg^T = [0, 2, -1],
+    # U = X Wu^T = [3, 1, 2], H = silu(G) U = [0, 2 s(2), -2 s(-1)], and
+    # T = [X Ag^T | X Au^T] = [1 | 1]
+    X = np.array([[1.0]])
+    Wg = np.array([[0.0], [2.0], [-1.0]])
+    Wu = np.array([[3.0], [1.0], [2.0]])
+    A = np.array([[1.0]])
+    Bz = np.zeros((3, 1))
+    H, G, U, T = oracle.swiglu_fwd(X, Wg, Wu, A, A, Bz, Bz, 1.0)
+    s = lambda x: 1.0 / (1.0 + np.exp(-x))  # noqa: E731
+    assert G.tolist() == [[0.0, 2.0, -1.0]] and U.tolist() == [[3.0, 1.0, 2.0]] and T.tolist() == [[1.0, 1.0]]
+    assert H[0, 0] == 0.0
+    assert np.isclose(H[0, 1], 2.0 * s(2.0) * 1.0, rtol=1e-15)
+    assert np.isclose(H[0, 2], -1.0 * s(-1.0) * 2.0, rtol=1e-15)
+
+
 def test_swiglu_gradients_by_finite_differences():
     """<dH, H> is smooth in X, A, B: central differences (fp64) match the
     analytic gradients of the oracle to ~1e-7 relative."""
