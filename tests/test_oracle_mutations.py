@@ -24,6 +24,7 @@ SOURCE = open(oracle_src.__file__, encoding="utf-8").read()
 # pin name -> (module, function, arguments)
 PINS = {
     "bf16_vs_torch": (pins, "test_bf16_round_matches_torch", ()),
+    "nf4_levels": (pins, "test_nf4_levels_match_normalfloat_construction", ()),
     "nf4_round_trip_1": (pins, "test_nf4_every_code_round_trips", (1.0,)),
     "nf4_round_trip_3.5": (pins, "test_nf4_every_code_round_trips", (3.5,)),
     "nf4_dq_closed_form": (pins, "test_nf4_double_quant_decode_closed_form", ()),
@@ -154,6 +155,32 @@ MISTAKES = [
     ("SwiGLU derivative factor dropped",
      "    return dH * U * sg * (1.0 + G * (1.0 - sg)), dH * G * sg",
      "    return dH * U * sg, dH * G * sg",
+     ["swiglu_hand_worked", "swiglu_fd"]),
+    ("one NF4 level off in its last digit",
+     "    0.44070974, 0.5626169, 0.72295666, 1.0,\n", "    0.44070974, 0.5626168, 0.72295666, 1.0,\n",
+     ["nf4_levels"]),
+    ("Q8_0 block scale not applied",
+     "    prod = (q * d[:, None]).astype(np.float32)", "    prod = (q * np.float32(1.0)).astype(np.float32)",
+     ["q8_0_minus_128"]),
+    ("E4M3 NaN code read as a number",
+     "    return np.where((e == 15) & (m == 7), np.nan, v)", "    return v",
+     ["e4m3_vs_torch"]),
+    ("grouped forward drops each expert's last row",
+     "        lo, hi = int(offsets[e]), int(offsets[e + 1])\n        if hi > lo:\n            Y[lo:hi]",
+     "        lo, hi = int(offsets[e]), int(offsets[e + 1]) - 1\n        if hi > lo:\n            Y[lo:hi]",
+     ["grouped_distinct", "grouped_hand_worked"]),
+    ("fused projections' T blocks in reverse order",
+     "np.concatenate([t for _, t in outs], axis=1)", "np.concatenate([t for _, t in outs[::-1]], axis=1)",
+     ["multi_hand_worked", "multi_block_diagonal"]),
+    ("fused projections' dB blocks in reverse order",
+     'np.concatenate([g["dB"] for g in gs], axis=0)', 'np.concatenate([g["dB"] for g in gs[::-1]], axis=0)',
+     ["multi_hand_worked", "multi_block_diagonal"]),
+    ("stacked adapters' dB from U instead of T",
+     "        dB.append(s * (dY.T @ T))\n", "        dB.append(s * (dY.T @ U))\n",
+     ["stacked_fd"]),
+    ("SwiGLU dU from U instead of G",
+     "    return dH * U * sg * (1.0 + G * (1.0 - sg)), dH * G * sg",
+     "    return dH * U * sg * (1.0 + G * (1.0 - sg)), dH * U * sg",
      ["swiglu_hand_worked", "swiglu_fd"]),
     ("SwiGLU gate and up swapped",
      "    H = G * _sigmoid(G) * U\n", "    H = U * _sigmoid(U) * G\n",
