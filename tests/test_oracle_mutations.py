@@ -36,6 +36,7 @@ PINS = {
     "finite_differences": (pins, "test_backward_matches_central_finite_differences", ()),
     "brute_force": (pins, "test_against_brute_force_loops", ()),
     "hand_worked": (pins, "test_hand_worked_example", ()),
+    "row_subsets": (pins, "test_row_subsets_and_adapter_grads_agree_with_full", ()),
     "grouped_distinct": (pins, "test_grouped_distinct_experts_against_row_loops", ()),
     "grouped_hand_worked": (pins, "test_grouped_hand_worked_two_experts", ()),
     "multi_hand_worked": (pins, "test_multi_projection_hand_worked", ()),
@@ -78,6 +79,13 @@ MISTAKES = [
     ("dA from T instead of U",
      "    dB = s * (dY.T @ T)\n    dA = s * (U.T @ X)\n", "    dB = s * (dY.T @ T)\n    dA = s * (T.T @ X)\n",
      ["finite_differences", "brute_force", "hand_worked"]),
+    ("sampled-row dX without its adapter term",
+     "    return dY @ Wd + s * ((dY @ B) @ A)\n", "    return dY @ Wd\n",
+     ["row_subsets"]),
+    ("all-row adapter gradients: dB from U",
+     '    return {"T": T, "U": U, "dA": s * (U.T @ X), "dB": s * (dY.T @ T)}',
+     '    return {"T": T, "U": U, "dA": s * (U.T @ X), "dB": s * (dY.T @ U)}',
+     ["row_subsets"]),
     ("bf16 rounding truncates",
      "    u = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)\n",
      "    u = (u >> np.uint64(16)) << np.uint64(16)\n",
